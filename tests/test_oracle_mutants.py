@@ -1,0 +1,79 @@
+"""Planted mistakes in the oracle must fail at least one pin.
+
+Each case copies ``oracle/ep_oracle.c`` to a temporary directory, applies one
+textual change that models a plausible slip (a flipped comparison, a dropped
+term, a wrong index or sign, a transposed operand), builds it with gcc and runs
+the whole pin battery of ``pins.py`` against it. A pin battery that lets a
+mutant through is not pinning that part of the oracle. CPU only.
+"""
+import pathlib
+
+import pytest
+
+import oracle
+import pins
+
+MUTANTS = [
+    ("topk tie goes to the higher index",
+     "(best < 0 || l[e] > l[best])) best = e;", "(best < 0 || l[e] >= l[best])) best = e;"),
+    ("group score is the minimum",
+     "if (l[g * gsize + i] > s) s = l[g * gsize + i];", "if (l[g * gsize + i] < s) s = l[g * gsize + i];"),
+    ("group ranking tie to the higher group",
+     "(best < 0 || gscore[g] > gscore[best])) best = g;", "(best < 0 || gscore[g] >= gscore[best])) best = g;"),
+    ("softmax exponent sign flipped",
+     "p[e] = exp((double)l[e] - m);", "p[e] = exp(m - (double)l[e]);"),
+    ("renormalisation dropped",
+     "w[t * k + j] = renormalize ? p[idx[t * k + j]] / s : p[idx[t * k + j]];",
+     "w[t * k + j] = p[idx[t * k + j]];"),
+    ("softmax denominator not shifted by the max",
+     "            S += p[e];", "            S += exp((double)l[e]);"),
+    ("rank offset indexed by rank, not by first expert",
+     "rank_offset[r] = expert_offset[r * epr];", "rank_offset[r] = expert_offset[r];"),
+    ("offset scan off by one expert",
+     "expert_offset[e + 1] = expert_offset[e] + expert_count[e];",
+     "expert_offset[e + 1] = expert_offset[e] + expert_count[e + (e + 1 < E)];"),
+    ("tokens walked in reverse (unstable order)",
+     "    for (int64_t t = 0; t < T; ++t)\n        for (int32_t j = 0; j < k; ++j) {\n            int32_t e = idx[t * k + j];\n            slot[t * k + j] = cursor[e];",
+     "    for (int64_t t = T - 1; t >= 0; --t)\n        for (int32_t j = 0; j < k; ++j) {\n            int32_t e = idx[t * k + j];\n            slot[t * k + j] = cursor[e];"),
+    ("near traffic scheduled first",
+     "for (int c = 1; c >= 0; --c) {", "for (int c = 0; c <= 1; ++c) {"),
+    ("chunk row_begin missing the rank base",
+     "rec[3] = (int32_t)(rank_offset[r] + (a - seg_lo));", "rec[3] = (int32_t)(a - seg_lo);"),
+    ("worker share rounded up",
+     "int64_t hi = N[c] * (w + 1) / W;", "int64_t hi = (N[c] * (w + 1) + W - 1) / W;"),
+    ("hop class from the rank, not the node",
+     "int c = (r / ranks_per_node == self_node) ? 0 : 1;", "int c = (r == self_rank) ? 0 : 1;"),
+    ("meta transposed",
+     "meta[s] = (int32_t)(t * k + j);", "meta[s] = (int32_t)(j * T + t);"),
+    ("combine weight operand transposed",
+     "acc = fmaf(w[t * k + j], orc_bf16_to_f32(y[s * H + h]), acc);",
+     "acc = fmaf(w[j * T + t], orc_bf16_to_f32(y[s * H + h]), acc);"),
+    ("combine drops the last term",
+     "            for (int32_t j = 0; j < k; ++j) {\n                int64_t s = slot[t * k + j];\n                if (s < 0 || s >= T * k) return ORC_EINVAL;\n                acc",
+     "            for (int32_t j = 0; j < k - 1; ++j) {\n                int64_t s = slot[t * k + j];\n                if (s < 0 || s >= T * k) return ORC_EINVAL;\n                acc"),
+    ("bf16 ties rounded away from zero",
+     "if (low > 0x8000u || (low == 0x8000u && (keep & 1u)))", "if (low >= 0x8000u)"),
+    ("bf16 truncation",
+     "        keep += 1u;                      /* carries into the exponent: ok  */", "        keep += 0u;"),
+]
+
+
+def _battery(o):
+    failed = []
+    for pin in pins.ALL_PINS:
+        try:
+            pin(o)
+        except (AssertionError, oracle.OracleError, IndexError, ValueError) as exc:  # noqa: PERF203
+            failed.append((pin.__name__, type(exc).__name__))
+    return failed
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(tmp_path: pathlib.Path, name, old, new):
+    src = oracle.SOURCE.read_text()
+    assert src.count(old) == 1, f"mutation site not unique/absent: {name}"
+    mutated = tmp_path / "ep_oracle_mutant.c"
+    mutated.write_text(src.replace(old, new))
+    lib = oracle.build(mutated, tmp_path / "libmutant.so", force=True)
+    failed = _battery(oracle.Oracle(lib))
+    assert failed, f"no pin caught the mutant: {name}"
