@@ -1,0 +1,444 @@
+#!/usr/bin/env python
+"""Benchmark of the MoE expert-parallel hot path on GB300.
+
+One step = one pass of the whole path over one synthetic batch:
+ep_route -> ep_layout -> ep_dispatch -> ep_combine (the expert FFN between
+dispatch and combine is outside the library; its output buffer y is filled once
+before timing with the synthetic expert's rows for this batch, which are the
+same every step because routing is deterministic).
+
+Default workload: prefill-shaped, skewed (T=4096, H=7168, E=256 over R=32,
+top-8, Zipf 1.2 expert popularity). ``--config`` selects another workload.
+
+Printed: one JSON line (rank 0). ``value`` is achieved algorithmic GB/s of the
+whole step (bytes every step must move at least once / device time), ``e2e``
+the same through the public API with the host<->device copies of the step's
+inputs and result inside the timed region, ``roofline`` the dominant kernel
+against the measured HBM copy bandwidth, ``cpu_baseline`` the CPU oracle on a
+bounded sample of the same workload.
+
+``--impl reference`` times the CPU oracle (the only reference implementation
+of this path) on the same workload, each step a bounded token sample.
+
+Multi-GPU (torchrun, one process per GPU): every rank runs its own batch of
+the workload (data-parallel shards, no exchange between ranks); value = bytes
+of all ranks / the slowest rank's time ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import pathlib
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = pathlib.Path(__file__).resolve().parent
+if str(ROOT) not in sys.path:
+    sys.path.insert(0, str(ROOT))
+
+METRIC = "dispatch+combine µs/layer and achieved HBM GB/s (fraction of GB300 peak), 1 GPU"
+FALLBACK_HBM_GBS = 6800.0
+KERNELS = ("route", "layout", "dispatch", "combine")
+# Kernels that profiles/dram_traffic.txt refers to, with the files whose contents fix them.
+KERNEL_SOURCES = {
+    "route": ["combine_router_softmax_gb300/csrc/route.cu"],
+    "layout": ["combine_router_softmax_gb300/csrc/layout.cu"],
+    "dispatch": ["combine_router_softmax_gb300/csrc/dispatch.cu"],
+    "combine": ["combine_router_softmax_gb300/csrc/combine.cu"],
+}
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
+    p.add_argument("--config", default="prefill", help="workload name (tiny, decode, prefill, mid, sweep-<dist>-T<n>)")
+    p.add_argument("--e2e-steps", type=int, default=None, help="steps of the end-to-end leg (default min(steps, 200))")
+    p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU work of the oracle baseline")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-clocks", action="store_true")
+    return p.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (barrier + max over ranks; no data-path collective)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def rank_workload(w, rank: int):
+    """Rank r's shard: the same shapes with its own seed (independent tokens)."""
+    return w.with_(seed=w.seed + rank) if rank else w
+
+
+def reduce_max(value: float, world: int, device=None) -> float:
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) during the timed region."""
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int, enabled: bool = True):
+        self.proc = None
+        self.idx = device_index
+        if not enabled:
+            return
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={device_index}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], None, set()
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                sm.append(float(f[2]))
+                smax = float(f[3])
+            except ValueError:
+                continue
+            names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+            for name, val in zip(names, f[6:10]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# roofline inputs
+# ---------------------------------------------------------------------------
+
+def measured_peak_gbs():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        try:
+            return float(json.loads(p.read_text())["hbm_gbs"]), "measured"
+        except (KeyError, ValueError):
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash(kernel: str) -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES[kernel] + ["combine_router_softmax_gb300/csrc/ep_internal.cuh"]:
+        h.update((ROOT / rel).read_bytes())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    this workload and the kernel source has not changed since."""
+    p = ROOT / "profiles" / "dram_traffic.txt"
+    if not p.exists():
+        return None
+    try:
+        data = json.loads(p.read_text())
+        ent = data[workload][kernel]
+    except (KeyError, ValueError):
+        return None
+    if ent.get("source_sha256_16") != kernel_source_hash(kernel):
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline / reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample_pass(orc, w, T_s: int, logits, x):
+    """One pass of the oracle over the first T_s tokens of the workload."""
+    return orc.run_path(logits[:T_s], x[:T_s], E=w.E, R=w.R, k=w.k, n_groups=w.n_groups,
+                        topk_groups=w.topk_groups, renormalize=w.renormalize, ranks_per_node=w.ranks_per_node,
+                        self_rank=w.self_rank, W=w.num_workers)
+
+
+def pick_sample_tokens(orc, w, logits, x, target_s: float) -> int:
+    T_s = min(w.T, 16)
+    while True:
+        t0 = time.perf_counter()
+        oracle_sample_pass(orc, w, T_s, logits, x)
+        dt = time.perf_counter() - t0
+        if T_s >= w.T or dt >= target_s / 4:
+            break
+        T_s = min(w.T, T_s * 4)
+    scale = target_s / max(dt, 1e-6)
+    return max(1, min(w.T, int(T_s * scale)))
+
+
+def cpu_baseline(w, seconds: float) -> dict:
+    import ep_synth
+    import oracle
+
+    orc = oracle.get()
+    T_probe = min(w.T, 4096)
+    logits = ep_synth.gate_logits(w.seed, T_probe, w.E, w.zipf_s)
+    x = ep_synth.hidden_bf16_bits(w.seed, T_probe, w.H)
+    T_s = pick_sample_tokens(orc, w.with_(T=T_probe), logits, x, min(seconds / 3, 2.0))
+    ws = w.with_(T=T_s)
+    reps, t_total = 0, 0.0
+    while t_total < seconds or reps < 1:
+        t0 = time.perf_counter()
+        oracle_sample_pass(orc, w, T_s, logits, x)
+        t_total += time.perf_counter() - t0
+        reps += 1
+    gbs = ws.total_bytes() * reps / t_total / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"first {T_s} of {w.T} tokens of {w.name}, whole path (route, layout, schedule, dispatch, "
+                      f"expert, combine), {reps} passes in {t_total:.1f} s, single-threaded C; "
+                      f"host has {os.cpu_count()} cores"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import ep_synth
+    import oracle
+
+    w = ep_synth.get_workload(args.config)
+    orc = oracle.get()
+    T_probe = min(w.T, 4096)
+    logits = ep_synth.gate_logits(w.seed, T_probe, w.E, w.zipf_s)
+    x = ep_synth.hidden_bf16_bits(w.seed, T_probe, w.H)
+    # each step a bounded sample: the whole --steps/--warmup run stays near two minutes
+    per_step = min(0.5, 120.0 / max(1, args.steps + args.warmup))
+    T_s = pick_sample_tokens(orc, w.with_(T=T_probe), logits, x, per_step)
+    for _ in range(args.warmup):
+        oracle_sample_pass(orc, w, T_s, logits, x)
+    times = []
+    t_all = time.perf_counter()
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_sample_pass(orc, w, T_s, logits, x)
+        times.append(time.perf_counter() - t0)
+    wall = time.perf_counter() - t_all
+    ws = w.with_(T=T_s)
+    gbs = ws.total_bytes() * len(times) / sum(times) / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * sum(times) / len(times), 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32/f64 (CPU oracle)",
+        "data": "synthetic", "config": workload_config(w, args, extra={"sample_tokens": T_s}),
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"first {T_s} of {w.T} tokens per step, whole path, single-threaded C"},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "wall_s": round(wall, 3),
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w, args, extra=None) -> dict:
+    cfg = {"workload": w.note or w.name, "name": w.name, "T": w.T, "H": w.H, "E": w.E, "R": w.R, "k": w.k,
+           "n_groups": w.n_groups, "topk_groups": w.topk_groups, "renormalize": w.renormalize,
+           "zipf_s": w.zipf_s, "ranks_per_node": w.ranks_per_node, "num_workers": w.num_workers,
+           "bytes_per_step": w.total_bytes(), "parallelism": f"dp{args.gpus} (independent shards)",
+           "l2": "flushed before every timed step (write of 2x L2)"}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_gb300(args):
+    import numpy as np
+    import torch
+
+    rank, world, local_rank = dist_env()
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+
+    import combine_router_softmax_gb300 as ep
+    import ep_synth
+
+    w0 = ep_synth.get_workload(args.config)
+    w = rank_workload(w0, rank)
+    cfg = ep.EpConfig.from_workload(w)
+    logits_np = ep_synth.gate_logits(w.seed, w.T, w.E, w.zipf_s)
+    x_np = ep_synth.hidden_bf16_bits(w.seed, w.T, w.H)
+
+    buf = ep.LayerBuffers.allocate(cfg, device=device)
+    buf.logits.copy_(torch.from_numpy(logits_np))
+    buf.x.copy_(torch.from_numpy(x_np.view(np.int16)).view(torch.bfloat16))
+    stream = torch.cuda.current_stream(device)
+    bound = buf.bind(stream)
+
+    # expert output for this batch (outside the timed step)
+    bound.route(); bound.layout(); bound.dispatch()
+    rows = torch.arange(w.T * w.k, device=device, dtype=torch.int32)
+    e = torch.searchsorted(buf.expert_offset, rows, right=True) - 1
+    buf.y.copy_((buf.send.float() * ((e + 1).float() / w.E)[:, None]).to(torch.bfloat16))
+    del rows, e
+    torch.cuda.synchronize()
+
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=device)
+
+    def step():
+        bound.route(); bound.layout(); bound.dispatch(); bound.combine()
+
+    for _ in range(max(args.warmup, 0)):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    clocks = ClockSampler(local_rank, enabled=not args.no_clocks)
+    time.sleep(0.3 if not args.no_clocks else 0)
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.fill_(1)
+        e5 = ev[i]
+        e5[0].record(stream); bound.route()
+        e5[1].record(stream); bound.layout()
+        e5[2].record(stream); bound.dispatch()
+        e5[3].record(stream); bound.combine()
+        e5[4].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+
+    per = {n: [] for n in KERNELS}
+    step_ms = []
+    for e5 in ev:
+        for j, n in enumerate(KERNELS):
+            per[n].append(e5[j].elapsed_time(e5[j + 1]))
+        step_ms.append(e5[0].elapsed_time(e5[4]))
+    local_total_ms = sum(step_ms)
+    max_total_ms = reduce_max(local_total_ms, world, device)
+    bytes_step = w.total_bytes()
+    value = world * K * bytes_step / (max_total_ms * 1e-3) / 1e9
+    ms_per_step = max_total_ms / K
+
+    kb = w.algorithmic_bytes()
+    kern_ms = {n: sum(v) / len(v) for n, v in per.items()}
+    dom = max(kern_ms, key=kern_ms.get)
+    peak, peak_kind = measured_peak_gbs()
+    achieved = kb[dom] / (kern_ms[dom] * 1e-3) / 1e9
+
+    # end to end: pinned host inputs in, result out, every step
+    E2E = args.e2e_steps if args.e2e_steps is not None else min(K, 200)
+    h_logits = torch.from_numpy(logits_np).pin_memory()
+    h_x = torch.from_numpy(x_np.view(np.int16)).view(torch.bfloat16).pin_memory()
+    h_out = torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory()
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(E2E)]
+    for i in range(E2E + 3):
+        flush.fill_(1)
+        if i >= 3:
+            e2e_ev[i - 3][0].record(stream)
+        buf.logits.copy_(h_logits, non_blocking=True)
+        buf.x.copy_(h_x, non_blocking=True)
+        step()
+        h_out.copy_(buf.out, non_blocking=True)
+        if i >= 3:
+            e2e_ev[i - 3][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(sum(a.elapsed_time(b) for a, b in e2e_ev), world, device) / E2E
+    e2e_val = world * bytes_step / (e2e_ms * 1e-3) / 1e9
+
+    # the result must be the one the path computes (cheap self-check of the last step)
+    assert torch.equal(h_out.to(device), buf.out)
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16 rows, fp32 routing and combine accumulation",
+        "data": "synthetic",
+        "config": workload_config(w0, args),
+        "us_per_layer": round(ms_per_step * 1e3, 2),
+        "hbm_fraction": round(value / world / peak, 4),
+        "kernel_us": {n: round(v * 1e3, 2) for n, v in kern_ms.items()},
+        "roofline": {
+            "bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": ncu_traffic(dom, w0.name),
+            "algorithmic_bytes_per_launch": kb[dom], "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+            if peak_kind == "measured" else "fallback 6.8 TB/s",
+        },
+        "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h_logits.numel() * 4 + h_x.numel() * 2,
+                "d2h_bytes_per_step": h_out.numel() * 2, "ms_per_step": round(e2e_ms, 5), "steps": E2E},
+        "gpu_launches": K * 6,
+        "clocks": clk,
+        "wall_s": round(wall, 3),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w0, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gb300(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,201 @@
+// ep_api.cu -- the extern "C" entry points declared in include/ep.h.
+//
+// Every entry point checks its arguments on the host and returns a status
+// before anything is enqueued; only then does it call the launcher of its
+// kernels. Nothing here allocates device memory or synchronises.
+#include <mutex>
+
+#include "ep_internal.cuh"
+
+namespace ep {
+
+namespace {
+constexpr int kMaxDevices = 64;
+int g_sm_count[kMaxDevices] = {0};
+
+struct OccEntry {
+    const void *fn;
+    int dev;
+    int threads;
+    size_t smem;
+    int blocks;
+};
+std::mutex g_occ_mu;
+OccEntry g_occ[64];
+int g_occ_n = 0;
+}  // namespace
+
+int sm_count(int device) {
+    if (device < 0 || device >= kMaxDevices) return 0;
+    int v = g_sm_count[device];
+    if (v == 0) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return 0;
+        g_sm_count[device] = v;
+    }
+    return v;
+}
+
+int current_device_sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    return sm_count(dev);
+}
+
+int max_blocks_per_sm(const void *fn, int threads, size_t smem) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    std::lock_guard<std::mutex> lock(g_occ_mu);
+    for (int i = 0; i < g_occ_n; ++i)
+        if (g_occ[i].fn == fn && g_occ[i].dev == dev && g_occ[i].threads == threads && g_occ[i].smem == smem)
+            return g_occ[i].blocks;
+    int b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, threads, smem) != cudaSuccess || b <= 0) {
+        cudaGetLastError();
+        b = 1;
+    }
+    if (g_occ_n < 64) g_occ[g_occ_n++] = OccEntry{fn, dev, threads, smem, b};
+    return b;
+}
+
+}  // namespace ep
+
+namespace {
+
+using ep::kMaxE;
+using ep::kMaxGroups;
+using ep::kMaxK;
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape checks shared by all entry points.
+ep_status check_config(const ep_config *c) {
+    if (!c) return EP_ERR_INVALID_ARG;
+    if (c->T < 0 || c->E <= 0 || c->R <= 0 || c->k <= 0 || c->n_groups <= 0 || c->topk_groups <= 0)
+        return EP_ERR_INVALID_ARG;
+    if (c->E % c->R != 0 || c->k > c->E || c->E % c->n_groups != 0 || c->topk_groups > c->n_groups)
+        return EP_ERR_INVALID_ARG;
+    if ((int64_t)c->topk_groups * (c->E / c->n_groups) < c->k) return EP_ERR_INVALID_ARG;
+    if (c->renormalize != 0 && c->renormalize != 1) return EP_ERR_INVALID_ARG;
+    if ((int64_t)c->T * c->k > INT32_MAX) return EP_ERR_INVALID_ARG;
+    if (c->E > kMaxE || c->k > kMaxK || c->n_groups > kMaxGroups) return EP_ERR_UNSUPPORTED;
+    return EP_OK;
+}
+
+ep_status check_rows(const ep_config *c) {
+    if (c->H <= 0) return EP_ERR_INVALID_ARG;
+    if (c->H % 8 != 0) return EP_ERR_UNSUPPORTED;
+    return EP_OK;
+}
+
+ep_status check_schedule(const ep_config *c) {
+    if (c->ranks_per_node <= 0 || c->self_rank < 0 || c->self_rank >= c->R || c->num_workers < 0)
+        return EP_ERR_INVALID_ARG;
+    return EP_OK;
+}
+
+ep_status resolve_workers(const ep_config *c, int32_t *W) {
+    if (c->num_workers > 0) {
+        *W = c->num_workers;
+        return EP_OK;
+    }
+    const int sms = ep::current_device_sm_count();
+    if (sms <= 0) return EP_ERR_CUDA;
+    *W = sms;
+    return EP_OK;
+}
+
+ep_status from_cuda(cudaError_t e) { return e == cudaSuccess ? EP_OK : EP_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char *ep_status_string(int status) {
+    switch (status) {
+        case EP_OK: return "EP_OK";
+        case EP_ERR_INVALID_ARG: return "EP_ERR_INVALID_ARG: bad argument (null pointer, size or alignment)";
+        case EP_ERR_UNSUPPORTED: return "EP_ERR_UNSUPPORTED: shape outside the built kernels";
+        case EP_ERR_CUDA: return "EP_ERR_CUDA: CUDA launch or query failed";
+        case EP_ERR_CAPACITY: return "EP_ERR_CAPACITY: output table or workspace too small";
+        default: return "EP_ERR_UNKNOWN";
+    }
+}
+
+int ep_version(void) { return 100; }
+
+ep_status ep_layout_workspace_size(const ep_config *cfg, size_t *bytes) {
+    ep_status st = check_config(cfg);
+    if (st != EP_OK) return st;
+    if (!bytes) return EP_ERR_INVALID_ARG;
+    *bytes = ep::layout_workspace(cfg->T, cfg->E).bytes;
+    return EP_OK;
+}
+
+ep_status ep_schedule_capacity(const ep_config *cfg, int32_t *capacity) {
+    ep_status st = check_config(cfg);
+    if (st != EP_OK) return st;
+    if ((st = check_schedule(cfg)) != EP_OK) return st;
+    if (!capacity) return EP_ERR_INVALID_ARG;
+    int32_t W = 0;
+    if ((st = resolve_workers(cfg, &W)) != EP_OK) return st;
+    const int64_t cap = 2 * (int64_t)W + cfg->R;
+    if (cap > INT32_MAX) return EP_ERR_INVALID_ARG;
+    *capacity = (int32_t)cap;
+    return EP_OK;
+}
+
+ep_status ep_route(const ep_config *cfg, const float *logits, int32_t *topk_idx, float *topk_w,
+                   cudaStream_t stream) {
+    ep_status st = check_config(cfg);
+    if (st != EP_OK) return st;
+    if (cfg->T == 0) return EP_OK;
+    if (!logits || !topk_idx || !topk_w) return EP_ERR_INVALID_ARG;
+    return from_cuda(ep::launch_route(*cfg, logits, topk_idx, topk_w, stream));
+}
+
+ep_status ep_layout(const ep_config *cfg, const int32_t *topk_idx, int32_t *expert_count, int32_t *expert_offset,
+                    int32_t *rank_count, int32_t *rank_offset, int32_t *slot, ep_chunk *chunks,
+                    int32_t chunk_capacity, int32_t *n_chunks, int32_t *worker_begin, void *workspace,
+                    size_t workspace_bytes, cudaStream_t stream) {
+    ep_status st = check_config(cfg);
+    if (st != EP_OK) return st;
+    if ((st = check_schedule(cfg)) != EP_OK) return st;
+    if (!expert_count || !expert_offset || !rank_count || !rank_offset || !chunks || !n_chunks || !worker_begin)
+        return EP_ERR_INVALID_ARG;
+    if (cfg->T > 0 && (!topk_idx || !slot)) return EP_ERR_INVALID_ARG;
+    int32_t W = 0;
+    if ((st = resolve_workers(cfg, &W)) != EP_OK) return st;
+    if ((int64_t)chunk_capacity < 2 * (int64_t)W + cfg->R) return EP_ERR_CAPACITY;
+    const size_t need = ep::layout_workspace(cfg->T, cfg->E).bytes;
+    if (need > 0) {
+        if (!workspace) return EP_ERR_INVALID_ARG;
+        if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return EP_ERR_INVALID_ARG;
+        if (workspace_bytes < need) return EP_ERR_CAPACITY;
+    }
+    return from_cuda(ep::launch_layout(*cfg, W, topk_idx, expert_count, expert_offset, rank_count, rank_offset,
+                                       slot, chunks, n_chunks, worker_begin, workspace, stream));
+}
+
+ep_status ep_dispatch(const ep_config *cfg, const ep_bf16 *x, const int32_t *slot, ep_bf16 *send,
+                      int32_t *slot_meta, cudaStream_t stream) {
+    ep_status st = check_config(cfg);
+    if (st != EP_OK) return st;
+    if ((st = check_rows(cfg)) != EP_OK) return st;
+    if (cfg->T == 0) return EP_OK;
+    if (!x || !slot || !send || !slot_meta) return EP_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(send)) return EP_ERR_INVALID_ARG;
+    return from_cuda(ep::launch_dispatch(*cfg, x, slot, send, slot_meta, stream));
+}
+
+ep_status ep_combine(const ep_config *cfg, const ep_bf16 *y, const int32_t *slot, const float *topk_w,
+                     ep_bf16 *out, cudaStream_t stream) {
+    ep_status st = check_config(cfg);
+    if (st != EP_OK) return st;
+    if ((st = check_rows(cfg)) != EP_OK) return st;
+    if (cfg->T == 0) return EP_OK;
+    if (!y || !slot || !topk_w || !out) return EP_ERR_INVALID_ARG;
+    if (!aligned16(y) || !aligned16(out)) return EP_ERR_INVALID_ARG;
+    return from_cuda(ep::launch_combine(*cfg, y, slot, topk_w, out, stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,201 @@
+/*
+ * ep.h -- C ABI of the GB300 (sm_103a) MoE expert-parallel hot path:
+ * router softmax + top-k, dispatch layout, dispatch scatter, combine.
+ *
+ * The operations are the ones the UBEP article ("NJU x Huawei UBEP:
+ * Reengineering MoE Expert Parallelism", kad8.com) names for an expert-parallel
+ * communication library: each token is dispatched to the device that hosts each
+ * of its selected experts and gathered back in the Combine phase (opening
+ * section); the dispatch needs token counts, offsets from prefix sums and a
+ * reordering of tokens ("Three Bottlenecks" / BSP Serialization, "Kernel
+ * Decomposition"); and per-worker traffic is balanced across hop-latency
+ * classes ("Hierarchical Token-Level Scheduling" / Latency Homogenization).
+ * Here the R expert-parallel ranks are R contiguous partitions of one send
+ * buffer on one GPU: there is no peer traffic and no collective.
+ *
+ * Conventions for every entry point
+ *  - All tensor pointers are DEVICE pointers (cudaMalloc / torch CUDA memory)
+ *    on the current device, row-major and densely packed. The caller allocates
+ *    and owns every buffer; the library allocates nothing and keeps no state
+ *    between calls besides cached device attributes.
+ *  - Work is enqueued on `stream` (0 = legacy default stream) and is
+ *    asynchronous: results are ready when the stream reaches that point.
+ *  - bf16 tensors are passed as `ep_bf16` (the 16-bit pattern of a bfloat16).
+ *    x, send, y and out must be 16-byte aligned; H must be a multiple of 8 so
+ *    that every row is a whole number of 16-byte vectors.
+ *  - Arguments are checked on the host before anything is launched: a bad
+ *    argument returns EP_ERR_INVALID_ARG / EP_ERR_UNSUPPORTED /
+ *    EP_ERR_CAPACITY with nothing enqueued. EP_ERR_CUDA reports a launch error
+ *    (cudaGetLastError after the launch). No C++ exception crosses the ABI.
+ *  - T = 0 is valid: route, dispatch and combine enqueue nothing; layout still
+ *    writes its (all-zero) counts, offsets and schedule.
+ */
+#ifndef EP_GB300_H
+#define EP_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum ep_status {
+    EP_OK = 0,
+    EP_ERR_INVALID_ARG = 1, /* null pointer, inconsistent sizes, misaligned buffer      */
+    EP_ERR_UNSUPPORTED = 2, /* outside the built kernels: H % 8 != 0, k > 32, E > 1024,
+                               n_groups > 32                                            */
+    EP_ERR_CUDA = 3,        /* a CUDA launch or attribute query failed                  */
+    EP_ERR_CAPACITY = 4     /* chunk table or workspace smaller than required           */
+} ep_status;
+
+/* One layer's shape. */
+typedef struct ep_config {
+    int32_t T;              /* tokens on this GPU (>= 0); T * k <= INT32_MAX              */
+    int32_t H;              /* hidden size: bf16 elements per token row (> 0)             */
+    int32_t E;              /* experts (1 .. 1024)                                        */
+    int32_t R;              /* virtual expert-parallel ranks; E % R == 0; rank r owns
+                               experts [r E/R, (r+1) E/R)                                 */
+    int32_t k;              /* experts per token (1 .. min(E, 32))                        */
+    int32_t n_groups;       /* expert groups for group-limited routing; 1 = no limit;
+                               E % n_groups == 0, n_groups <= 32                          */
+    int32_t topk_groups;    /* groups kept per token (1 .. n_groups);
+                               topk_groups * (E / n_groups) >= k                           */
+    int32_t renormalize;    /* 1: top-k weights renormalised to sum to 1; 0: raw softmax  */
+    int32_t ranks_per_node; /* ranks sharing one node: defines the hop classes (>= 1)     */
+    int32_t self_rank;      /* the sending rank whose view the schedule models [0, R)     */
+    int32_t num_workers;    /* W, workers of the chunk schedule; 0 = the device SM count  */
+} ep_config;
+
+/* One record of the chunk schedule: rows [row_begin, row_begin + row_count)
+ * of the send buffer, all bound for dst_rank, handled by `worker`.
+ * hop_class 0 = a rank on the sender's node, 1 = a rank on another node. */
+typedef struct ep_chunk {
+    int32_t worker;
+    int32_t hop_class;
+    int32_t dst_rank;
+    int32_t row_begin;
+    int32_t row_count;
+} ep_chunk;
+
+typedef uint16_t ep_bf16;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *ep_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int ep_version(void);
+
+/* Bytes of device scratch that ep_layout needs for `cfg` (it depends on T and
+ * E only). The workspace needs no initialisation and may be reused across
+ * calls on the same stream. */
+ep_status ep_layout_workspace_size(const ep_config *cfg, size_t *bytes);
+
+/* Number of ep_chunk records ep_layout may write for `cfg`: 2 W + R
+ * (W = num_workers, or the current device's SM count when num_workers = 0). */
+ep_status ep_schedule_capacity(const ep_config *cfg, int32_t *capacity);
+
+/*
+ * ep_route -- router softmax and top-k for every token.
+ *
+ * Defines (the pages give no router; this is the plainest reading of
+ * "each token is dispatched to the device hosting its selected expert"):
+ *   p[t, e]       = softmax over all E experts of logits[t, :]
+ *   topk_idx[t,:] = the k experts with the largest logits, in descending order;
+ *                   equal logits go to the lower expert index. With
+ *                   n_groups > 1 only experts of the topk_groups groups with
+ *                   the largest per-group maximum logit are eligible (ties to
+ *                   the lower group index).
+ *   topk_w[t, j]  = p[t, idx_j] / sum_i p[t, idx_i] if renormalize, else p[t, idx_j]
+ *
+ * logits   : const float [T, E]  gate logits; must be finite
+ * topk_idx : int32 [T, k]        output
+ * topk_w   : float [T, k]        output (fp32; within a few ulp of exact)
+ */
+ep_status ep_route(const ep_config *cfg, const float *logits, int32_t *topk_idx, float *topk_w,
+                   cudaStream_t stream);
+
+/*
+ * ep_layout -- counts, offsets, the stable slot of every (token, expert)
+ * pair and the per-destination chunk schedule.
+ *
+ * Defines (token counting, prefix sums, offsets and reordering of the BSP
+ * pipeline, done here as one metadata pass):
+ *   expert_count[e]  = #{(t, j) : topk_idx[t, j] = e}
+ *   expert_offset[e] = sum_{e' < e} expert_count[e'];     expert_offset[E] = T k
+ *   rank_offset[r]   = expert_offset[r E / R];            rank_offset[R] = T k
+ *   rank_count[r]    = rank_offset[r + 1] - rank_offset[r]
+ *   slot[t, j]       = expert_offset[e] + #{t' < t : e in topk_idx[t', :]}, e = topk_idx[t, j]
+ * i.e. send rows are ordered by (destination rank, expert, source token).
+ *
+ * Chunk schedule (Latency Homogenization): hop_class(r) = 0 if rank r is on
+ * the node of self_rank (r / ranks_per_node == self_rank / ranks_per_node),
+ * else 1. For each class c, the class's rank segments concatenated in
+ * ascending rank hold N_c rows; worker w takes positions
+ * [floor(N_c w / W), floor(N_c (w + 1) / W)) of each class, cut at rank
+ * boundaries into non-empty chunks. The table is ordered by worker, then
+ * class descending (other-node traffic first), then rank; worker_begin[w] is
+ * the index of worker w's first chunk and worker_begin[W] = *n_chunks.
+ *
+ * topk_idx      : const int32 [T, k]; each row holds k distinct experts in
+ *                 [0, E) (as ep_route writes). An id outside [0, E) gets
+ *                 slot -1 and is not counted; a repeated id within one row
+ *                 gives unspecified (but in-range) slots.
+ * expert_count  : int32 [E]      output
+ * expert_offset : int32 [E + 1]  output
+ * rank_count    : int32 [R]      output
+ * rank_offset   : int32 [R + 1]  output
+ * slot          : int32 [T, k]   output
+ * chunks        : ep_chunk [chunk_capacity] output; chunk_capacity >= 2 W + R
+ *                 (ep_schedule_capacity), else EP_ERR_CAPACITY
+ * n_chunks      : int32 [1]      output (device memory)
+ * worker_begin  : int32 [W + 1]  output
+ * workspace     : device scratch of >= ep_layout_workspace_size bytes,
+ *                 256-byte aligned; else EP_ERR_CAPACITY / EP_ERR_INVALID_ARG
+ */
+ep_status ep_layout(const ep_config *cfg, const int32_t *topk_idx,
+                    int32_t *expert_count, int32_t *expert_offset,
+                    int32_t *rank_count, int32_t *rank_offset, int32_t *slot,
+                    ep_chunk *chunks, int32_t chunk_capacity, int32_t *n_chunks,
+                    int32_t *worker_begin, void *workspace, size_t workspace_bytes,
+                    cudaStream_t stream);
+
+/*
+ * ep_dispatch -- scatter each token row to the send-buffer rows of its k
+ * slots ("each token must be dispatched to the device hosting its selected
+ * expert"; here the send buffer is partitioned by destination rank):
+ *   send[slot[t, j], :] = x[t, :]        (bit copy)
+ *   slot_meta[slot[t, j]] = t k + j      (source token and top-k position)
+ *
+ * x         : const bf16 [T, H]
+ * slot      : const int32 [T, k]  as written by ep_layout; entries outside
+ *             [0, T k) are skipped
+ * send      : bf16 [T k, H]       output
+ * slot_meta : int32 [T k]         output
+ */
+ep_status ep_dispatch(const ep_config *cfg, const ep_bf16 *x, const int32_t *slot, ep_bf16 *send,
+                      int32_t *slot_meta, cudaStream_t stream);
+
+/*
+ * ep_combine -- gather the k expert-output rows of every token back to token
+ * order and sum them with the top-k weights ("later gathered during the
+ * Combine phase"):
+ *   acc = 0; for j = 0 .. k-1: acc = fmaf(topk_w[t, j], y[slot[t, j], h], acc)
+ *   out[t, h] = bf16 round-to-nearest-even(acc)
+ * in fp32 with one fused multiply-add per term, in fixed j order.
+ *
+ * y      : const bf16 [T k, H]  expert outputs, in send-buffer (slot) order
+ * slot   : const int32 [T, k]   entries outside [0, T k) contribute nothing
+ * topk_w : const float [T, k]
+ * out    : bf16 [T, H]          output
+ */
+ep_status ep_combine(const ep_config *cfg, const ep_bf16 *y, const int32_t *slot, const float *topk_w,
+                     ep_bf16 *out, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EP_GB300_H */
