@@ -7,7 +7,7 @@ the dtype, shape and device the C ABI expects, pass raw device pointers and
 the current CUDA stream, and raise :class:`EpError` on a non-zero status.
 Every step of the path runs in the library's CUDA kernels; there is no CPU or
 PyTorch fallback. Importing this package loads the library and fails if it
-has not been built (``python -m combine_router_softmax_gb300.build``).
+has not been built (``python combine_router_softmax_gb300/build.py``).
 
 PyTorch is used for device memory and streams only.
 """
@@ -63,7 +63,7 @@ class EpChunk(ctypes.Structure):
 def _load() -> ctypes.CDLL:
     if not LIB_PATH.exists():
         raise ImportError(
-            f"{LIB_PATH.name} is not built; run `python -m combine_router_softmax_gb300.build` "
+            f"{LIB_PATH.name} is not built; run `python combine_router_softmax_gb300/build.py` "
             "(nvcc for sm_103a). There is no fallback path.")
     lib = ctypes.CDLL(str(LIB_PATH))
     P, vp = ctypes.POINTER, ctypes.c_void_p

@@ -5,7 +5,9 @@ under ``_build/``, then linked into ``combine_router_softmax_gb300/libep_gb300.s
 (CUDA runtime linked statically). ptxas resource usage (``-Xptxas -v``) goes
 to ``_build/ptxas.log``.
 
-Run ``python -m combine_router_softmax_gb300.build`` or call :func:`build`.
+Run ``python combine_router_softmax_gb300/build.py`` or call :func:`build`. This file
+is self-contained (it never imports the package, whose import loads the
+library), so other scripts load it by file path before the library exists.
 """
 from __future__ import annotations
 

@@ -13,9 +13,9 @@ HEADERS = sorted((ROOT / "include").glob("*.h"))
 
 @pytest.fixture(scope="module")
 def lib():
-    from combine_router_softmax_gb300 import build
+    import __graft_entry__
 
-    build.build()
+    __graft_entry__._cuda_build_module().build()
     import combine_router_softmax_gb300 as m
 
     return m
