@@ -26,7 +26,9 @@ EP_OK, EP_ERR_INVALID_ARG, EP_ERR_UNSUPPORTED, EP_ERR_CUDA, EP_ERR_CAPACITY = ra
 
 # Entry points declared in include/ep.h (checked by the ABI test).
 EXPORTS = ("ep_status_string", "ep_version", "ep_layout_workspace_size", "ep_schedule_capacity",
-           "ep_route", "ep_layout", "ep_dispatch", "ep_combine")
+           "ep_route", "ep_layout", "ep_dispatch", "ep_combine", "ep_layout_static")
+# Size of the device array ep_layout_static uses instead of a workspace (include/ep.h).
+EP_LAYOUT_STATIC_SCRATCH_BYTES = 1 << 20
 
 
 class EpError(RuntimeError):
@@ -76,10 +78,11 @@ def _load() -> ctypes.CDLL:
     lib.ep_schedule_capacity.argtypes = [cfgp, P(ctypes.c_int32)]
     lib.ep_route.argtypes = [cfgp, vp, vp, vp, vp]
     lib.ep_layout.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int32, vp, vp, vp, ctypes.c_size_t, vp]
+    lib.ep_layout_static.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int32, vp, vp, vp]
     lib.ep_dispatch.argtypes = [cfgp, vp, vp, vp, vp, vp]
     lib.ep_combine.argtypes = [cfgp, vp, vp, vp, vp, vp]
     for f in ("ep_layout_workspace_size", "ep_schedule_capacity", "ep_route", "ep_layout", "ep_dispatch",
-              "ep_combine"):
+              "ep_combine", "ep_layout_static"):
         getattr(lib, f).restype = ctypes.c_int
     return lib
 
@@ -171,6 +174,29 @@ def ep_layout(cfg: EpConfig, topk_idx, expert_count, expert_offset, rank_count, 
                           _ptr(n_chunks, torch.int32, (1,), "n_chunks"),
                           _ptr(worker_begin, torch.int32, None, "worker_begin"),
                           ws_ptr, ctypes.c_size_t(ws_bytes), _stream(stream)), "ep_layout")
+
+
+def ep_layout_static(cfg: EpConfig, topk_idx, expert_count, expert_offset, rank_count, rank_offset, slot, chunks,
+                     n_chunks, worker_begin, stream=None) -> None:
+    """``ep_layout`` without a workspace argument: the library's fixed device
+    scratch array stands in for it (for callers that cannot allocate; see
+    include/ep.h). The first call on a device should precede any stream capture."""
+    T, E, R, k = cfg.T, cfg.E, cfg.R, cfg.k
+    if chunks.dim() != 2 or chunks.shape[1] != 5:
+        raise ValueError("chunks: expected int32 [capacity, 5]")
+    W = (ep_schedule_capacity(cfg) - R) // 2
+    if worker_begin.dim() != 1 or worker_begin.numel() < W + 1:
+        raise ValueError(f"worker_begin: expected int32 [>= {W + 1}]")
+    _check(_lib.ep_layout_static(ctypes.byref(cfg), _ptr(topk_idx, torch.int32, (T, k), "topk_idx"),
+                                 _ptr(expert_count, torch.int32, (E,), "expert_count"),
+                                 _ptr(expert_offset, torch.int32, (E + 1,), "expert_offset"),
+                                 _ptr(rank_count, torch.int32, (R,), "rank_count"),
+                                 _ptr(rank_offset, torch.int32, (R + 1,), "rank_offset"),
+                                 _ptr(slot, torch.int32, (T, k), "slot"),
+                                 _ptr(chunks, torch.int32, None, "chunks"), ctypes.c_int32(chunks.shape[0]),
+                                 _ptr(n_chunks, torch.int32, (1,), "n_chunks"),
+                                 _ptr(worker_begin, torch.int32, None, "worker_begin"), _stream(stream)),
+           "ep_layout_static")
 
 
 def ep_dispatch(cfg: EpConfig, x, slot, send, slot_meta, stream=None) -> None:

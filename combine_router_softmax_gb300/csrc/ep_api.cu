@@ -10,7 +10,7 @@
 namespace ep {
 
 namespace {
-constexpr int kMaxDevices = 64;
+constexpr int kMaxDevices = kMaxDevices_;
 int g_sm_count[kMaxDevices] = {0};
 
 struct OccEntry {
@@ -199,3 +199,61 @@ ep_status ep_combine(const ep_config *cfg, const ep_bf16 *y, const int32_t *slot
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// ep_layout_static: ep_layout with its scratch in a fixed device array.
+//
+// For callers that cannot allocate device memory at call time and so cannot
+// supply ep_layout's workspace -- e.g. an engine that hands the library only
+// the input and output buffers it owns and has no allocator to lend (its
+// memory is carved up once at start-up), or code running where a device
+// allocation is not allowed. The scratch is a file-scope __device__ array of
+// EP_LAYOUT_STATIC_SCRATCH_BYTES that every GPU which loads this library
+// keeps until the process exits. Its device address is looked up once per
+// device, on the first call made with that device current.
+// ---------------------------------------------------------------------------
+namespace {
+
+static __device__ __align__(256) unsigned char g_layout_static_scratch[EP_LAYOUT_STATIC_SCRATCH_BYTES];
+
+std::mutex g_static_mu;
+void *g_static_addr[ep::kMaxDevices_] = {nullptr};
+
+// Device address of g_layout_static_scratch on the current device (set-up on first use).
+ep_status static_scratch_address(void **addr) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= ep::kMaxDevices_) return EP_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_layout_static_scratch) != cudaSuccess || !p) {
+            cudaGetLastError();
+            return EP_ERR_CUDA;
+        }
+        g_static_addr[dev] = p;
+    }
+    *addr = g_static_addr[dev];
+    return EP_OK;
+}
+
+}  // namespace
+
+extern "C" ep_status ep_layout_static(const ep_config *cfg, const int32_t *topk_idx, int32_t *expert_count,
+                                      int32_t *expert_offset, int32_t *rank_count, int32_t *rank_offset,
+                                      int32_t *slot, ep_chunk *chunks, int32_t chunk_capacity, int32_t *n_chunks,
+                                      int32_t *worker_begin, cudaStream_t stream) {
+    ep_status st = check_config(cfg);
+    if (st != EP_OK) return st;
+    if ((st = check_schedule(cfg)) != EP_OK) return st;
+    if (!expert_count || !expert_offset || !rank_count || !rank_offset || !chunks || !n_chunks || !worker_begin)
+        return EP_ERR_INVALID_ARG;
+    if (cfg->T > 0 && (!topk_idx || !slot)) return EP_ERR_INVALID_ARG;
+    if (ep::layout_workspace(cfg->T, cfg->E).bytes > (size_t)EP_LAYOUT_STATIC_SCRATCH_BYTES) return EP_ERR_CAPACITY;
+    int32_t W = 0;
+    if ((st = resolve_workers(cfg, &W)) != EP_OK) return st;
+    if ((int64_t)chunk_capacity < 2 * (int64_t)W + cfg->R) return EP_ERR_CAPACITY;
+    void *scratch = nullptr;
+    if ((st = static_scratch_address(&scratch)) != EP_OK) return st;
+    return from_cuda(ep::launch_layout(*cfg, W, topk_idx, expert_count, expert_offset, rank_count, rank_offset,
+                                       slot, chunks, n_chunks, worker_begin, scratch, stream));
+}

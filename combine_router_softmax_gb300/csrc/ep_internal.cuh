@@ -20,6 +20,8 @@ constexpr int kFullMask = -1;  // all 32 lanes (as unsigned in shuffles)
 constexpr int kLayoutWarps = 8;
 constexpr int kLayoutTokens = 32 * kLayoutWarps;
 
+constexpr int kMaxDevices_ = 64;  // device ordinals with cached attributes
+
 // Largest shapes the kernels are built for.
 constexpr int kMaxE = 1024;
 constexpr int kMaxK = 32;

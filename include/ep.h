@@ -17,7 +17,8 @@
  *  - All tensor pointers are DEVICE pointers (cudaMalloc / torch CUDA memory)
  *    on the current device, row-major and densely packed. The caller allocates
  *    and owns every buffer; the library allocates nothing and keeps no state
- *    between calls besides cached device attributes.
+ *    between calls besides cached device attributes (and the fixed scratch
+ *    array of ep_layout_static, below).
  *  - Work is enqueued on `stream` (0 = legacy default stream) and is
  *    asynchronous: results are ready when the stream reaches that point.
  *  - bf16 tensors are passed as `ep_bf16` (the 16-bit pattern of a bfloat16).
@@ -193,6 +194,41 @@ ep_status ep_dispatch(const ep_config *cfg, const ep_bf16 *x, const int32_t *slo
  */
 ep_status ep_combine(const ep_config *cfg, const ep_bf16 *y, const int32_t *slot, const float *topk_w,
                      ep_bf16 *out, cudaStream_t stream);
+
+/*
+ * ep_layout_static -- ep_layout for callers that cannot allocate device memory.
+ *
+ * The paper has no counterpart: this is a property of this library, not of the
+ * method. Some callers cannot call cudaMalloc (or any allocator) when they run
+ * the layout -- for example an engine that hands a library only the input and
+ * output buffers it owns, with all of its device memory carved up once at
+ * start-up and no allocator to lend, or code running where a device
+ * allocation is not allowed. They cannot pass ep_layout's workspace.
+ *
+ * This entry point computes exactly what ep_layout computes (same arguments
+ * and outputs, same errors) but takes its scratch from a fixed device array
+ * inside the library of EP_LAYOUT_STATIC_SCRATCH_BYTES (1 MiB), which every
+ * GPU that loads the library holds until the process exits. It calls no
+ * cudaMalloc, cudaFree or other allocating routine.
+ *  - Limit: shapes whose ep_layout_workspace_size exceeds
+ *    EP_LAYOUT_STATIC_SCRATCH_BYTES return EP_ERR_CAPACITY with nothing
+ *    enqueued (4 * E * ceil(T / 256) bytes, rounded up to 256: e.g. E = 256
+ *    allows T <= 262144 tokens).
+ *  - Set-up: the first call on a device (made with that device current) looks
+ *    up the array's device address; make that first call before any stream
+ *    capture. Later calls on the device reuse the address.
+ *  - Sharing: every call on a device shares the one array, which keeps the
+ *    last call's contents (the kernels overwrite all of it they read). Calls
+ *    whose work overlaps on the GPU -- on different streams, or from
+ *    different threads -- race on it: order them on one stream.
+ */
+#define EP_LAYOUT_STATIC_SCRATCH_BYTES (1u << 20)
+
+ep_status ep_layout_static(const ep_config *cfg, const int32_t *topk_idx,
+                           int32_t *expert_count, int32_t *expert_offset,
+                           int32_t *rank_count, int32_t *rank_offset, int32_t *slot,
+                           ep_chunk *chunks, int32_t chunk_capacity, int32_t *n_chunks,
+                           int32_t *worker_begin, cudaStream_t stream);
 
 #ifdef __cplusplus
 }
