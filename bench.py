@@ -63,6 +63,7 @@ def parse_args(argv=None):
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU work of the oracle baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
+    p.add_argument("--no-graph", action="store_true", help="time the per-step launches only (no CUDA graph)")
     return p.parse_args(argv)
 
 
@@ -286,6 +287,28 @@ def workload_config(w, args, extra=None) -> dict:
 # GPU arm
 # ---------------------------------------------------------------------------
 
+def capture_step_graph(buf, device):
+    """route -> layout -> dispatch -> combine captured once into a CUDA graph.
+
+    Two eager passes on the capture stream first, so that every lazy set-up
+    inside the library (attributes, occupancy, symbol addresses) happens
+    outside the capture."""
+    import torch
+
+    cap = torch.cuda.Stream(device)
+    cap.wait_stream(torch.cuda.current_stream(device))
+    bound = buf.bind(cap)
+    with torch.cuda.stream(cap):
+        for _ in range(2):
+            bound.route(); bound.layout(); bound.dispatch(); bound.combine()
+    cap.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cap):
+        bound.route(); bound.layout(); bound.dispatch(); bound.combine()
+    torch.cuda.synchronize()
+    return g
+
+
 def run_gb300(args):
     import numpy as np
     import torch
@@ -332,6 +355,13 @@ def run_gb300(args):
         step()
     torch.cuda.synchronize()
 
+    graph = None if args.no_graph else capture_step_graph(buf, device)
+    if graph is not None:
+        for _ in range(max(args.warmup, 0)):
+            flush.fill_(1)
+            graph.replay()
+        torch.cuda.synchronize()
+
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
     clocks = ClockSampler(local_rank, enabled=not args.no_clocks)
@@ -358,12 +388,37 @@ def run_gb300(args):
         for j, n in enumerate(KERNELS):
             per[n].append(e5[j].elapsed_time(e5[j + 1]))
         step_ms.append(e5[0].elapsed_time(e5[4]))
-    local_total_ms = sum(step_ms)
-    max_total_ms = reduce_max(local_total_ms, world, device)
+    stream_ms_per_step = reduce_max(sum(step_ms), world, device) / K
     bytes_step = w.total_bytes()
+
+    if graph is not None:
+        # The same four calls captured once in a CUDA graph, replayed K times
+        # (L2 flushed before each replay, outside the events).
+        gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        clocks = ClockSampler(local_rank, enabled=not args.no_clocks)
+        time.sleep(0.3 if not args.no_clocks else 0)
+        barrier(world)
+        torch.cuda.synchronize()
+        gwall0 = time.perf_counter()
+        for a, b_ in gev:
+            flush.fill_(1)
+            a.record(stream)
+            graph.replay()
+            b_.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        wall += time.perf_counter() - gwall0
+        gclk = clocks.stop()
+        if gclk is not None:
+            clk = gclk
+        local_total_ms = sum(a.elapsed_time(b_) for a, b_ in gev)
+    else:
+        local_total_ms = sum(step_ms)
+    max_total_ms = reduce_max(local_total_ms, world, device)
     value = world * K * bytes_step / (max_total_ms * 1e-3) / 1e9
     ms_per_step = max_total_ms / K
 
+    launches_per_step = ep.ep_step_kernel_count(cfg)
     kb = w.algorithmic_bytes()
     kern_ms = {n: sum(v) / len(v) for n, v in per.items()}
     dom = max(kern_ms, key=kern_ms.get)
@@ -382,7 +437,10 @@ def run_gb300(args):
             e2e_ev[i - 3][0].record(stream)
         buf.logits.copy_(h_logits, non_blocking=True)
         buf.x.copy_(h_x, non_blocking=True)
-        step()
+        if graph is not None:
+            graph.replay()
+        else:
+            step()
         h_out.copy_(buf.out, non_blocking=True)
         if i >= 3:
             e2e_ev[i - 3][1].record(stream)
@@ -408,6 +466,9 @@ def run_gb300(args):
         "data": "synthetic",
         "config": workload_config(w0, args),
         "us_per_layer": round(ms_per_step * 1e3, 2),
+        "timing": "CUDA graph of the four C-ABI calls, replayed per step" if graph is not None
+                  else "four C-ABI calls launched per step",
+        "stream_us_per_layer": round(stream_ms_per_step * 1e3, 2),
         "hbm_fraction": round(value / world / peak, 4),
         "kernel_us": {n: round(v * 1e3, 2) for n, v in kern_ms.items()},
         "roofline": {
@@ -418,7 +479,7 @@ def run_gb300(args):
         },
         "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h_logits.numel() * 4 + h_x.numel() * 2,
                 "d2h_bytes_per_step": h_out.numel() * 2, "ms_per_step": round(e2e_ms, 5), "steps": E2E},
-        "gpu_launches": K * 6,
+        "gpu_launches": K * launches_per_step * (2 if graph is not None else 1),
         "clocks": clk,
         "wall_s": round(wall, 3),
     }

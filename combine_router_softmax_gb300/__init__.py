@@ -25,7 +25,8 @@ LIB_PATH = _PKG / "libep_gb300.so"
 EP_OK, EP_ERR_INVALID_ARG, EP_ERR_UNSUPPORTED, EP_ERR_CUDA, EP_ERR_CAPACITY = range(5)
 
 # Entry points declared in include/ep.h (checked by the ABI test).
-EXPORTS = ("ep_status_string", "ep_version", "ep_layout_workspace_size", "ep_schedule_capacity",
+EXPORTS = ("ep_status_string", "ep_version", "ep_device_error", "ep_step_kernel_count",
+           "ep_layout_workspace_size", "ep_schedule_capacity",
            "ep_route", "ep_layout", "ep_dispatch", "ep_combine", "ep_layout_static")
 # Size of the device array ep_layout_static uses instead of a workspace (include/ep.h).
 EP_LAYOUT_STATIC_SCRATCH_BYTES = 1 << 20
@@ -74,6 +75,8 @@ def _load() -> ctypes.CDLL:
     lib.ep_status_string.restype = ctypes.c_char_p
     lib.ep_version.argtypes = []
     lib.ep_version.restype = ctypes.c_int
+    lib.ep_device_error.argtypes = [P(ctypes.c_int32)]
+    lib.ep_step_kernel_count.argtypes = [cfgp, P(ctypes.c_int32)]
     lib.ep_layout_workspace_size.argtypes = [cfgp, P(ctypes.c_size_t)]
     lib.ep_schedule_capacity.argtypes = [cfgp, P(ctypes.c_int32)]
     lib.ep_route.argtypes = [cfgp, vp, vp, vp, vp]
@@ -81,8 +84,8 @@ def _load() -> ctypes.CDLL:
     lib.ep_layout_static.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int32, vp, vp, vp]
     lib.ep_dispatch.argtypes = [cfgp, vp, vp, vp, vp, vp]
     lib.ep_combine.argtypes = [cfgp, vp, vp, vp, vp, vp]
-    for f in ("ep_layout_workspace_size", "ep_schedule_capacity", "ep_route", "ep_layout", "ep_dispatch",
-              "ep_combine", "ep_layout_static"):
+    for f in ("ep_device_error", "ep_step_kernel_count", "ep_layout_workspace_size", "ep_schedule_capacity", "ep_route", "ep_layout",
+              "ep_dispatch", "ep_combine", "ep_layout_static"):
         getattr(lib, f).restype = ctypes.c_int
     return lib
 
@@ -128,6 +131,20 @@ def _stream(stream) -> ctypes.c_void_p:
     if stream is None:
         stream = torch.cuda.current_stream()
     return ctypes.c_void_p(stream.cuda_stream)
+
+
+def ep_device_error() -> int:
+    """Device-side error flags of the current device (read and cleared; synchronous)."""
+    v = ctypes.c_int32(0)
+    _check(_lib.ep_device_error(ctypes.byref(v)), "ep_device_error")
+    return int(v.value)
+
+
+def ep_step_kernel_count(cfg: EpConfig) -> int:
+    """Kernels one route + layout + dispatch + combine pass enqueues on the current device."""
+    v = ctypes.c_int32(0)
+    _check(_lib.ep_step_kernel_count(ctypes.byref(cfg), ctypes.byref(v)), "ep_step_kernel_count")
+    return int(v.value)
 
 
 def ep_layout_workspace_size(cfg: EpConfig) -> int:

@@ -123,11 +123,22 @@ const char *ep_status_string(int status) {
 
 int ep_version(void) { return 100; }
 
+ep_status ep_device_error(int32_t *flags) {
+    if (!flags) return EP_ERR_INVALID_ARG;
+    int32_t *word = nullptr;
+    if (ep::dispatch_error_word(&word) != cudaSuccess) return EP_ERR_CUDA;
+    int32_t v = 0;
+    if (cudaMemcpy(&v, word, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return EP_ERR_CUDA;
+    if (v != 0 && cudaMemset(word, 0, sizeof v) != cudaSuccess) return EP_ERR_CUDA;
+    *flags = v;
+    return EP_OK;
+}
+
 ep_status ep_layout_workspace_size(const ep_config *cfg, size_t *bytes) {
     ep_status st = check_config(cfg);
     if (st != EP_OK) return st;
     if (!bytes) return EP_ERR_INVALID_ARG;
-    *bytes = ep::layout_workspace(cfg->T, cfg->E).bytes;
+    *bytes = ep::layout_workspace(*cfg).bytes;
     return EP_OK;
 }
 
@@ -141,6 +152,20 @@ ep_status ep_schedule_capacity(const ep_config *cfg, int32_t *capacity) {
     const int64_t cap = 2 * (int64_t)W + cfg->R;
     if (cap > INT32_MAX) return EP_ERR_INVALID_ARG;
     *capacity = (int32_t)cap;
+    return EP_OK;
+}
+
+ep_status ep_step_kernel_count(const ep_config *cfg, int32_t *kernels) {
+    ep_status st = check_config(cfg);
+    if (st != EP_OK) return st;
+    if (!kernels) return EP_ERR_INVALID_ARG;
+    if (cfg->T == 0) {
+        *kernels = 1;  // the layout's scan still runs
+        return EP_OK;
+    }
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return EP_ERR_CUDA;
+    *kernels = 3 + ep::layout_kernel_count(*cfg);
     return EP_OK;
 }
 
@@ -166,7 +191,7 @@ ep_status ep_layout(const ep_config *cfg, const int32_t *topk_idx, int32_t *expe
     int32_t W = 0;
     if ((st = resolve_workers(cfg, &W)) != EP_OK) return st;
     if ((int64_t)chunk_capacity < 2 * (int64_t)W + cfg->R) return EP_ERR_CAPACITY;
-    const size_t need = ep::layout_workspace(cfg->T, cfg->E).bytes;
+    const size_t need = ep::layout_workspace(*cfg).bytes;
     if (need > 0) {
         if (!workspace) return EP_ERR_INVALID_ARG;
         if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return EP_ERR_INVALID_ARG;
@@ -248,7 +273,7 @@ extern "C" ep_status ep_layout_static(const ep_config *cfg, const int32_t *topk_
     if (!expert_count || !expert_offset || !rank_count || !rank_offset || !chunks || !n_chunks || !worker_begin)
         return EP_ERR_INVALID_ARG;
     if (cfg->T > 0 && (!topk_idx || !slot)) return EP_ERR_INVALID_ARG;
-    if (ep::layout_workspace(cfg->T, cfg->E).bytes > (size_t)EP_LAYOUT_STATIC_SCRATCH_BYTES) return EP_ERR_CAPACITY;
+    if (ep::layout_workspace(*cfg).bytes > (size_t)EP_LAYOUT_STATIC_SCRATCH_BYTES) return EP_ERR_CAPACITY;
     int32_t W = 0;
     if ((st = resolve_workers(cfg, &W)) != EP_OK) return st;
     if ((int64_t)chunk_capacity < 2 * (int64_t)W + cfg->R) return EP_ERR_CAPACITY;

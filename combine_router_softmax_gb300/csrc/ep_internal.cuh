@@ -29,12 +29,15 @@ constexpr int kMaxGroups = 32;
 
 inline int64_t layout_blocks(int64_t T) { return (T + kLayoutTokens - 1) / kLayoutTokens; }
 
-// Workspace carve-up for ep_layout (all offsets 256-byte aligned).
+// Workspace carve-up for ep_layout (offsets 256-byte aligned). The fused path
+// uses [CTA][E] counts at block_counts_off and two sync words at sync_off; the
+// fallback path uses [E][ceil(T/256)] counts at block_counts_off.
 struct LayoutWorkspace {
-    size_t block_counts_off;  // int32 [E][nb]: per-CTA expert histograms, then their exclusive scan
+    size_t block_counts_off;
+    size_t sync_off;
     size_t bytes;
 };
-LayoutWorkspace layout_workspace(int64_t T, int32_t E);
+LayoutWorkspace layout_workspace(const ep_config &c);
 
 // Cached device properties (per device ordinal).
 int sm_count(int device);
@@ -48,6 +51,9 @@ cudaError_t launch_layout(const ep_config &c, int32_t W, const int32_t *idx, int
                           int32_t *expert_offset, int32_t *rank_count, int32_t *rank_offset, int32_t *slot,
                           ep_chunk *chunks, int32_t *n_chunks, int32_t *worker_begin, void *workspace,
                           cudaStream_t s);
+
+// Kernels launch_layout enqueues for c on the current device (1 fused, or 3).
+int layout_kernel_count(const ep_config &c);
 
 cudaError_t launch_dispatch(const ep_config &c, const ep_bf16 *x, const int32_t *slot, ep_bf16 *send,
                             int32_t *meta, cudaStream_t s);
@@ -73,5 +79,84 @@ __device__ __forceinline__ void st_v4(uint4 *p, const uint4 &v) {
                  "r"(v.w)
                  : "memory");
 }
+
+// ---------------------------------------------------------------------------
+// Bulk async copies (TMA, non-tensor form) and mbarriers, sm_90+ PTX.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+// Make barrier initialisation visible to the async (bulk copy) proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait on one mbarrier phase: false if it did not complete in time.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint32_t max_polls) {
+    for (uint32_t i = 0; i < max_polls; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        __nanosleep(32);
+    }
+    return false;
+}
+
+// global -> shared bulk copy completing on an mbarrier (dst, src, bytes 16-B aligned).
+__device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst_smem)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// shared -> global bulk copy, tracked by this thread's bulk groups.
+__device__ __forceinline__ void bulk_s2g(void *dst, const void *src_smem, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src_smem)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until at most N of this thread's bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// Wait until at most N of this thread's bulk groups are incomplete.
+template <int N>
+__device__ __forceinline__ void bulk_wait() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Device-side error flags (bit values), one word per translation unit that
+// can set them; ep_device_error() collects and clears them.
+constexpr int32_t kErrDispatchWait = 1;  // a dispatch CTA gave up waiting for a bulk copy
+cudaError_t dispatch_error_word(int32_t **addr);
 
 }  // namespace ep

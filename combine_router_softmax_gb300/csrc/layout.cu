@@ -3,23 +3,26 @@
 //
 // The UBEP article's BSP pipeline counts tokens, computes offsets by prefix
 // sums and reorders tokens ("Three Bottlenecks" / BSP Serialization); its
-// "Kernel Decomposition" gives those metadata steps to a few cores and the
-// row movement to the rest. Here the metadata is three short kernels:
+// "Kernel Decomposition" replaces the global barriers between those phases by
+// cores that poll global memory for the metadata they need. Here:
 //
-//  1. rank   : each CTA takes 256 consecutive tokens (32 per warp). A warp
-//              walks its 32 tokens in order with one shared-memory counter per
-//              expert (lanes j < k handle the k distinct experts of a token at
-//              once), which yields each pair's rank among the warp's earlier
-//              pairs of the same expert. The 8 warp histograms are then
-//              scanned per expert, giving each pair its rank inside the CTA
-//              and the CTA's per-expert count (written expert-major to the
-//              workspace). No atomics decide an order, so slots are
-//              deterministic.
-//  2. scan   : one CTA scans the expert-major [E][nb] counts (exclusive),
-//              which turns every CTA's count into the base of its run inside
-//              the expert's segment; it then writes the expert and rank
-//              counts/offsets and builds the chunk schedule.
-//  3. final  : slot = CTA base of (expert, CTA) + rank inside the CTA.
+//  * rank phase (every CTA, on its own tokens): a warp walks its 32 tokens in
+//    order with one shared-memory counter per expert (lanes j < k take the k
+//    distinct experts of a token at once), giving each pair its rank among
+//    the warp's earlier pairs of the same expert; the per-warp histograms are
+//    scanned per expert. No atomic decides an order, so slots are
+//    deterministic.
+//
+//  * fused path (one cooperative launch, all CTAs co-resident): each CTA
+//    publishes its per-expert counts, then meets the others at a bounded grid
+//    barrier (an arrival counter polled with acquire loads, no SyncAll-style
+//    second kernel). Every CTA then reads the whole [CTA][expert] count table
+//    and computes, redundantly and in parallel, the expert offsets and its
+//    own prefix inside each expert's segment, and writes its final slots.
+//    CTA 0 writes the counts/offsets and the last CTA the chunk schedule.
+//
+//  * fallback (T beyond what one co-resident grid holds): three kernels --
+//    rank, a one-CTA scan (+ schedule), finalize.
 //
 // Schedule ("Hierarchical Token-Level Scheduling" / Latency Homogenization):
 // every worker gets an equal share of each hop class. One thread per worker
@@ -32,80 +35,51 @@
 
 namespace ep {
 
-LayoutWorkspace layout_workspace(int64_t T, int32_t E) {
+namespace {
+
+constexpr int kScanThreads = 1024;
+constexpr int kFusedMaxWarps = 32;
+constexpr size_t kFusedSmemBudget = 160 * 1024;
+constexpr unsigned kBarrierSpinLimit = 1u << 22;  // polls of ~64 ns before giving up
+
+size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+// Shared memory of the fused kernel for nw warps.
+size_t fused_smem_bytes(int nw, int32_t E, int32_t R, int32_t k) {
+    return sizeof(int32_t) * ((size_t)nw * E + 2 * (size_t)nw * 32 * k + 3 * (size_t)E + 2 + 2 * (size_t)R + 3);
+}
+
+// Warps per fused CTA (8, 16 or 32): the fewest that keep the grid at <= 32
+// CTAs, within the shared-memory budget. 0 if not even 8 fit.
+int fused_warps(int64_t T, int32_t E, int32_t R, int32_t k) {
+    int best = 0;
+    for (int nw = kLayoutWarps; nw <= kFusedMaxWarps; nw <<= 1) {
+        if (fused_smem_bytes(nw, E, R, k) > kFusedSmemBudget) break;
+        best = nw;
+        if ((T + 32 * nw - 1) / (32 * nw) <= 32) break;
+    }
+    return best;
+}
+
+}  // namespace
+
+LayoutWorkspace layout_workspace(const ep_config &c) {
     LayoutWorkspace w;
-    const int64_t nb = layout_blocks(T);
+    const int64_t nb = layout_blocks(c.T);
     w.block_counts_off = 0;
-    size_t bytes = sizeof(int32_t) * (size_t)nb * (size_t)E;
-    w.bytes = (bytes + 255) & ~(size_t)255;
+    const int nw = fused_warps(c.T, c.E, c.R, c.k);
+    const int64_t nbf = nw > 0 ? (c.T + 32 * nw - 1) / (32 * nw) : nb;
+    w.sync_off = align256(sizeof(int32_t) * (size_t)nbf * (size_t)c.E);
+    const size_t fallback = align256(sizeof(int32_t) * (size_t)nb * (size_t)c.E);
+    const size_t fused = nbf > 1 ? w.sync_off + 256 : w.sync_off;
+    w.bytes = c.T == 0 ? 0 : (fallback > fused ? fallback : fused);
     return w;
 }
 
 namespace {
 
-constexpr int kScanThreads = 1024;
-
 // ---------------------------------------------------------------------------
-// 1. per-CTA ranks and histograms
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kLayoutWarps * 32)
-layout_rank_kernel(const int32_t *__restrict__ idx, int32_t T, int32_t E, int32_t k, int32_t nb,
-                   int32_t *__restrict__ block_counts, int32_t *__restrict__ slot) {
-    extern __shared__ int32_t sm[];
-    int32_t *cnt = sm;                                  // [warps][E]
-    int32_t *tile_e = cnt + kLayoutWarps * E;           // [warps][32 k] expert ids
-    int32_t *tile_r = tile_e + kLayoutWarps * 32 * k;   // [warps][32 k] rank within the warp
-
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    for (int i = threadIdx.x; i < kLayoutWarps * E; i += blockDim.x) cnt[i] = 0;
-
-    const int64_t t0 = (int64_t)blockIdx.x * kLayoutTokens + (int64_t)warp * 32;
-    const int64_t left = (int64_t)T - t0;
-    const int ntok = left <= 0 ? 0 : (left >= 32 ? 32 : (int)left);
-    const int npair = ntok * k;
-    int32_t *te = tile_e + warp * 32 * k;
-    int32_t *tr = tile_r + warp * 32 * k;
-    int32_t *wc = cnt + warp * E;
-    for (int i = lane; i < npair; i += 32) te[i] = __ldg(idx + t0 * k + i);
-    __syncthreads();
-
-    for (int tt = 0; tt < ntok; ++tt) {
-        if (lane < k) {
-            const int e = te[tt * k + lane];
-            int r = -1;
-            if ((unsigned)e < (unsigned)E) {
-                r = wc[e];
-                wc[e] = r + 1;
-            }
-            tr[tt * k + lane] = r;
-        }
-        __syncwarp();
-    }
-    __syncthreads();
-
-    // Exclusive scan over the warps, per expert; the CTA total goes out.
-    for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        int run = 0;
-#pragma unroll
-        for (int w = 0; w < kLayoutWarps; ++w) {
-            const int c = cnt[w * E + e];
-            cnt[w * E + e] = run;
-            run += c;
-        }
-        block_counts[(int64_t)e * nb + blockIdx.x] = run;
-    }
-    __syncthreads();
-
-    for (int i = lane; i < npair; i += 32) {
-        const int e = te[i];
-        const int r = tr[i];
-        slot[t0 * k + i] = r < 0 ? -1 : wc[e] + r;
-    }
-}
-
-// ---------------------------------------------------------------------------
-// 2. scan, counts/offsets, chunk schedule (one CTA)
+// shared device pieces
 // ---------------------------------------------------------------------------
 
 // Exclusive scan of one value per thread over the CTA; returns the prefix and
@@ -138,33 +112,132 @@ __device__ __forceinline__ int64_t cta_exclusive_scan(int64_t x, int64_t *s_warp
     return base + inc - x;
 }
 
-// Class prefix sums in closed form. Class 0 (near) is ranks [n_lo, n_hi);
-// class 1 (far) is [0, n_lo) followed by [n_hi, R). P_c(i) is the number of
-// rows in the first i ranks of class c; rank_of(c, i) is that i-th rank.
-struct ClassView {
-    const int32_t *ro;  // rank_offset, R + 1 entries
-    int32_t n_lo, n_hi, R;
-    __device__ int32_t size(int c) const { return c == 0 ? n_hi - n_lo : R - (n_hi - n_lo); }
-    __device__ int32_t rank_of(int c, int32_t i) const {
-        return c == 0 ? n_lo + i : (i < n_lo ? i : i + (n_hi - n_lo));
+// 32-bit exclusive scan of one value per thread over the CTA (s_warp: 32 ints).
+__device__ __forceinline__ int cta_exclusive_scan32(int x, int *s_warp, int *total) {
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    int inc = x;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, inc, d);
+        if (lane >= d) inc += o;
     }
-    __device__ int64_t prefix(int c, int32_t i) const {
-        if (c == 0) return (int64_t)ro[n_lo + i] - ro[n_lo];
-        if (i <= n_lo) return ro[i];
-        return (int64_t)ro[n_lo] + ((int64_t)ro[i + (n_hi - n_lo)] - ro[n_hi]);
+    if (lane == 31) s_warp[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        int wv = lane < nwarps ? s_warp[lane] : 0;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, wv, d);
+            if (lane >= d) wv += o;
+        }
+        if (lane < nwarps) s_warp[lane] = wv;
     }
-};
+    __syncthreads();
+    const int base = warp > 0 ? s_warp[warp - 1] : 0;
+    *total = s_warp[nwarps - 1];
+    __syncthreads();
+    return base + inc - x;
+}
 
-// Largest i in [0, n) with P(i) <= x, for P non-decreasing and P(0) <= x.
+// Threads that share one expert's work in a CTA of nw warps: the largest power
+// of two <= min(32 nw / E, nw, 32), at least 1.
+__device__ __forceinline__ int threads_per_expert(int32_t E, int nw) {
+    int cap = (32 * nw) / E;
+    if (cap > nw) cap = nw;
+    if (cap > 32) cap = 32;
+    int t = 1;
+    while (2 * t <= cap) t <<= 1;
+    return t;
+}
+
+// Rank phase for the CTA's tokens [t_cta, t_cta + 32 nw). On return (after a
+// CTA barrier): tile_e / tile_r hold each pair's expert and its rank among the
+// same warp's earlier pairs of that expert (-1 for an id outside [0, E));
+// cnt[w][e] holds the number of pairs of expert e in warps < w; and
+// cta_count[e * stride] the CTA's total for expert e.
+//
+// A warp ranks 32 consecutive pairs (token order) per step: __match_any_sync
+// groups the lanes holding the same expert, a lane's rank inside the step is
+// the number of lower lanes in its group, and the group's highest lane
+// advances the warp's shared counter for that expert. The k experts of one
+// token are distinct, so lanes of one token never match each other.
+__device__ void cta_rank_tokens(const int32_t *__restrict__ idx, int32_t T, int32_t E, int32_t k, int64_t t_cta,
+                                int32_t *cnt, int32_t *tile_e, int32_t *tile_r, int32_t *cta_count,
+                                int64_t stride) {
+    const int nw = blockDim.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    for (int i = threadIdx.x; i < nw * E; i += blockDim.x) cnt[i] = 0;
+
+    const int64_t t0 = t_cta + (int64_t)warp * 32;
+    const int64_t left = (int64_t)T - t0;
+    const int ntok = left <= 0 ? 0 : (left >= 32 ? 32 : (int)left);
+    const int npair = ntok * k;
+    int32_t *te = tile_e + warp * 32 * k;
+    int32_t *tr = tile_r + warp * 32 * k;
+    int32_t *wc = cnt + warp * E;
+    for (int i = lane; i < npair; i += 32) te[i] = __ldg(idx + t0 * k + i);
+    __syncthreads();
+
+    const unsigned below = (1u << lane) - 1u;
+    const unsigned above = ~((2u << lane) - 1u);
+    for (int p0 = 0; p0 < npair; p0 += 32) {
+        const int p = p0 + lane;
+        const int e = p < npair ? te[p] : -1;
+        const bool valid = (unsigned)e < (unsigned)E;
+        const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : E + lane);
+        const int basec = valid ? wc[e] : 0;
+        __syncwarp();
+        if (valid && (peers & above) == 0) wc[e] = basec + __popc(peers);
+        if (p < npair) tr[p] = valid ? basec + __popc(peers & below) : -1;
+        __syncwarp();
+    }
+    __syncthreads();
+
+    // Exclusive scan over the warps, per expert. tpe consecutive threads share
+    // an expert, each scanning a contiguous run of nw / tpe warps; a shuffle
+    // scan joins the runs. Rounds are uniform across the CTA (shuffles need
+    // every lane).
+    const int tpe = threads_per_expert(E, nw);
+    const int sub = (int)threadIdx.x % tpe;
+    const int runlen = nw / tpe;
+    const int per_round = blockDim.x / tpe;
+    for (int base = 0; base < E; base += per_round) {
+        const int e0 = base + (int)threadIdx.x / tpe;
+        const bool act = e0 < E;
+        int local = 0;
+        if (act)
+            for (int w = sub * runlen; w < (sub + 1) * runlen; ++w) local += cnt[w * E + e0];
+        int incl = local;
+        for (int d = 1; d < tpe; d <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, incl, d, tpe);
+            if (sub >= d) incl += o;
+        }
+        if (act) {
+            int run = incl - local;
+            for (int w = sub * runlen; w < (sub + 1) * runlen; ++w) {
+                const int c = cnt[w * E + e0];
+                cnt[w * E + e0] = run;
+                run += c;
+            }
+            if (sub == tpe - 1) cta_count[(int64_t)e0 * stride] = incl;
+        }
+    }
+    __syncthreads();
+}
+
+// Largest i in [0, n) with P[i] <= x, for P non-decreasing with P[0] <= x.
 // 4-ary search: three independent pivot compares narrow the range 4x per step.
-__device__ __forceinline__ int32_t quaternary_search(const ClassView &cv, int c, int32_t n, int64_t x) {
-    int32_t lo = 0, hi = n;  // answer in [lo, hi), P(lo) <= x
+__device__ __forceinline__ int32_t quaternary_search(const int32_t *P, int32_t n, int32_t x) {
+    int32_t lo = 0, hi = n;  // answer in [lo, hi), P[lo] <= x
     while (hi - lo > 1) {
         const int32_t len = hi - lo;
         const int32_t q1 = lo + len / 4, q2 = lo + len / 2, q3 = lo + (3 * len) / 4;
-        const bool c1 = cv.prefix(c, q1) <= x;
-        const bool c2 = cv.prefix(c, q2) <= x;
-        const bool c3 = cv.prefix(c, q3) <= x;
+        const bool c1 = P[q1] <= x;
+        const bool c2 = P[q2] <= x;
+        const bool c3 = P[q3] <= x;
         if (c3) {
             lo = q3;
         } else if (c2) {
@@ -180,35 +253,276 @@ __device__ __forceinline__ int32_t quaternary_search(const ClassView &cv, int c,
     return lo;
 }
 
-// Walk worker w's share of class c; count chunks, or write them from `pos`.
-__device__ int32_t worker_class_chunks(const ClassView &cv, int c, int64_t N, int32_t w, int32_t W,
-                                       ep_chunk *chunks, int32_t pos, bool write) {
-    const int64_t lo = N * w / W;
-    const int64_t hi = N * (w + 1) / W;
-    if (hi <= lo) return 0;
-    const int32_t n = cv.size(c);
-    int32_t i = quaternary_search(cv, c, n, lo);
-    int32_t cnt = 0;
-    for (; i < n; ++i) {
-        const int64_t seg_lo = cv.prefix(c, i);
-        if (seg_lo >= hi) break;
-        const int64_t seg_hi = cv.prefix(c, i + 1);
-        const int64_t a = lo > seg_lo ? lo : seg_lo;
-        const int64_t b = hi < seg_hi ? hi : seg_hi;
-        if (b <= a) continue;
-        if (write) {
-            const int32_t r = cv.rank_of(c, i);
-            ep_chunk ch;
-            ch.worker = w;
-            ch.hop_class = c;
-            ch.dst_rank = r;
-            ch.row_begin = (int32_t)(cv.ro[r] + (a - seg_lo));
-            ch.row_count = (int32_t)(b - a);
-            chunks[pos + cnt] = ch;
+// floor(N w / W) for the share boundaries (32-bit whenever it cannot overflow).
+__device__ __forceinline__ int32_t share_bound(int32_t N, int32_t w, int32_t W) {
+    if ((uint64_t)(uint32_t)N * (uint32_t)W <= 0xffffffffull) return (int32_t)((uint32_t)N * (uint32_t)w / (uint32_t)W);
+    return (int32_t)((int64_t)N * w / W);
+}
+
+// The chunk schedule, built by one whole CTA from rank offsets in shared
+// memory. Class 0 (near) is ranks [n_lo, n_hi) of self_rank's node; class 1
+// (far) is [0, n_lo) followed by [n_hi, R). s_P (R + 2 ints of shared memory)
+// receives each class's prefix sums P_c[i] = rows in its first i ranks. A
+// worker finds the first and last rank its share touches by two quaternary
+// searches per class, counts the non-empty ranks in between, and after a CTA
+// scan over the counts writes its chunks.
+__device__ void cta_build_schedule(const int32_t *s_roff, int32_t R, int32_t W, int32_t ranks_per_node,
+                                   int32_t self_rank, ep_chunk *chunks, int32_t *n_chunks, int32_t *worker_begin,
+                                   int *s_warp, int32_t *s_P) {
+    const int32_t node = self_rank / ranks_per_node;
+    const int32_t n_lo = node * ranks_per_node;
+    const int32_t n_hi = n_lo + ranks_per_node < R ? n_lo + ranks_per_node : R;
+    const int32_t n0 = n_hi - n_lo, n1 = R - n0;
+    int32_t *P1 = s_P;           // far class: n1 + 1 entries
+    int32_t *P0 = s_P + n1 + 1;  // near class: n0 + 1 entries
+    for (int32_t i = threadIdx.x; i <= n1; i += blockDim.x)
+        P1[i] = i <= n_lo ? s_roff[i] : s_roff[n_lo] + (s_roff[i + n0] - s_roff[n_hi]);
+    for (int32_t i = threadIdx.x; i <= n0; i += blockDim.x) P0[i] = s_roff[n_lo + i] - s_roff[n_lo];
+    __syncthreads();
+    const int32_t N[2] = {P0[n0], P1[n1]};
+
+    int carry = 0;
+    for (int32_t wb = 0; wb < W; wb += blockDim.x) {
+        const int32_t w = wb + (int32_t)threadIdx.x;
+        int32_t first[2] = {0, 0}, last[2] = {-1, -1}, lo[2] = {0, 0}, hi[2] = {0, 0};
+        int cnt = 0;
+        if (w < W) {
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int32_t *P = c ? P1 : P0;
+                const int32_t n = c ? n1 : n0;
+                lo[c] = share_bound(N[c], w, W);
+                hi[c] = share_bound(N[c], w + 1, W);
+                if (hi[c] > lo[c]) {
+                    first[c] = quaternary_search(P, n, lo[c]);
+                    last[c] = quaternary_search(P, n, hi[c] - 1);
+                    for (int32_t i = first[c]; i <= last[c]; ++i) cnt += P[i + 1] > P[i] ? 1 : 0;
+                }
+            }
         }
-        ++cnt;
+        int tile_total;
+        const int pos0 = carry + cta_exclusive_scan32(cnt, s_warp, &tile_total);
+        if (w < W) {
+            worker_begin[w] = pos0;
+            int pos = pos0;
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c = 1 - cc;  // other-node traffic first
+                const int32_t *P = c ? P1 : P0;
+                for (int32_t i = first[c]; i <= last[c]; ++i) {
+                    if (P[i + 1] == P[i]) continue;
+                    const int32_t r = c ? (i < n_lo ? i : i + n0) : n_lo + i;
+                    const int32_t a = lo[c] > P[i] ? lo[c] : P[i];
+                    const int32_t bnd = hi[c] < P[i + 1] ? hi[c] : P[i + 1];
+                    ep_chunk ch;
+                    ch.worker = w;
+                    ch.hop_class = c;
+                    ch.dst_rank = r;
+                    ch.row_begin = s_roff[r] + (a - P[i]);
+                    ch.row_count = bnd - a;
+                    chunks[pos++] = ch;
+                }
+            }
+        }
+        carry += tile_total;
     }
-    return cnt;
+    if (threadIdx.x == 0) {
+        worker_begin[W] = carry;
+        *n_chunks = carry;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// fused path
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void red_release_gpu_add(unsigned *p, unsigned v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Grid barrier for co-resident CTAs: after a CTA barrier, thread 0 fences the
+// CTA's global writes, arrives with a release add and polls with acquire
+// loads. Bounded: returns false (for every thread of the CTA) if the count did
+// not arrive in time.
+__device__ bool grid_barrier(unsigned *arrivals, unsigned expected) {
+    __shared__ int s_ok;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        red_release_gpu_add(arrivals, 1u);
+        int ok = 1;
+        unsigned spins = 0;
+        while (ld_acquire_gpu(arrivals) < expected) {
+            if (++spins > kBarrierSpinLimit) {
+                ok = 0;
+                break;
+            }
+            if (spins > 64) __nanosleep(32);
+        }
+        __threadfence();
+        s_ok = ok;
+    }
+    __syncthreads();
+    return s_ok != 0;
+}
+
+__global__ void __launch_bounds__(kFusedMaxWarps * 32)
+layout_fused_kernel(const int32_t *__restrict__ idx, int32_t T, int32_t E, int32_t R, int32_t k, int32_t nb,
+                    int32_t *__restrict__ counts, unsigned *__restrict__ sync, int32_t *__restrict__ expert_count,
+                    int32_t *__restrict__ expert_offset, int32_t *__restrict__ rank_count,
+                    int32_t *__restrict__ rank_offset, int32_t *__restrict__ slot, ep_chunk *__restrict__ chunks,
+                    int32_t *__restrict__ n_chunks, int32_t *__restrict__ worker_begin, int32_t W,
+                    int32_t ranks_per_node, int32_t self_rank) {
+    extern __shared__ int32_t sm[];
+    const int nw = blockDim.x >> 5;
+    int32_t *cnt = sm;                         // [nw][E]
+    int32_t *tile_e = cnt + nw * E;            // [nw][32 k]
+    int32_t *tile_r = tile_e + nw * 32 * k;    // [nw][32 k]
+    int32_t *s_tot = tile_r + nw * 32 * k;     // [E]   pairs of expert e, all CTAs
+    int32_t *s_pre = s_tot + E;                // [E]   pairs of expert e in CTAs before this one
+    int32_t *s_eoff = s_pre + E;               // [E+2] expert offsets (+ total)
+    int32_t *s_roff = s_eoff + E + 2;          // [R+1] rank offsets
+    int32_t *s_P = s_roff + R + 1;             // [R+2] class prefix sums (schedule)
+    __shared__ int s_warp32[32];
+
+    const int b = blockIdx.x;
+    const int64_t t_cta = (int64_t)b * 32 * nw;
+    cta_rank_tokens(idx, T, E, k, t_cta, cnt, tile_e, tile_r, counts + (int64_t)b * E, 1);
+
+    if (nb > 1 && !grid_barrier(&sync[0], (unsigned)nb)) {
+        if (threadIdx.x == 0) {
+            atomicExch(&sync[1], 1u);
+            atomicExch(n_chunks, -1);
+        }
+        return;
+    }
+
+    // Expert totals over all CTAs and this CTA's prefix inside each expert.
+    // tpe threads share a column of the [CTA][E] table, each summing every
+    // tpe-th row; integer adds into shared memory make the order irrelevant.
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        s_tot[e] = 0;
+        s_pre[e] = 0;
+    }
+    __syncthreads();
+    {
+        const int tpe = threads_per_expert(E, nw);
+        const int sub = (int)threadIdx.x % tpe;
+        for (int e = (int)threadIdx.x / tpe; e < E; e += blockDim.x / tpe) {
+            int tot = 0, pre = 0;
+            // rows sub, sub + tpe, ...: issue up to 32 loads before using any
+            for (int q0 = sub; q0 < nb; q0 += 32 * tpe) {
+                int cv[32];
+#pragma unroll
+                for (int u = 0; u < 32; ++u) {
+                    const int q = q0 + u * tpe;
+                    cv[u] = q < nb ? __ldcg(counts + (int64_t)q * E + e) : 0;
+                }
+#pragma unroll
+                for (int u = 0; u < 32; ++u) {
+                    tot += cv[u];
+                    pre += q0 + u * tpe < b ? cv[u] : 0;
+                }
+            }
+            if (tpe == 1) {
+                s_tot[e] = tot;
+                s_pre[e] = pre;
+            } else {
+                atomicAdd(&s_tot[e], tot);
+                atomicAdd(&s_pre[e], pre);
+            }
+        }
+    }
+    __syncthreads();
+
+    // Exclusive scan of the totals: each thread scans a contiguous run.
+    {
+        const int per = (E + blockDim.x - 1) / blockDim.x;
+        const int e0 = threadIdx.x * per;
+        const int e1 = e0 + per < E ? e0 + per : E;
+        int local = 0;
+        for (int e = e0; e < e1; ++e) local += s_tot[e];
+        int total;
+        int run = cta_exclusive_scan32(local, s_warp32, &total);
+        for (int e = e0; e < e1; ++e) {
+            s_eoff[e] = run;
+            run += s_tot[e];
+        }
+        if (threadIdx.x == 0) s_eoff[E] = total;
+    }
+    __syncthreads();
+
+    // Final slots of this CTA's pairs.
+    {
+        const int lane = threadIdx.x & 31;
+        const int warp = threadIdx.x >> 5;
+        const int64_t t0 = t_cta + (int64_t)warp * 32;
+        const int64_t left = (int64_t)T - t0;
+        const int ntok = left <= 0 ? 0 : (left >= 32 ? 32 : (int)left);
+        const int npair = ntok * k;
+        const int32_t *te = tile_e + warp * 32 * k;
+        const int32_t *tr = tile_r + warp * 32 * k;
+        const int32_t *wc = cnt + warp * E;
+        for (int i = lane; i < npair; i += 32) {
+            const int e = te[i];
+            const int r = tr[i];
+            slot[t0 * k + i] = r < 0 ? -1 : s_eoff[e] + s_pre[e] + wc[e] + r;
+        }
+    }
+
+    const int32_t epr = E / R;
+    if (b == 0) {
+        for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+            expert_offset[e] = s_eoff[e];
+            if (e < E) expert_count[e] = s_tot[e];
+        }
+        for (int r = threadIdx.x; r < R; r += blockDim.x) {
+            rank_offset[r] = s_eoff[r * epr];
+            rank_count[r] = s_eoff[(r + 1) * epr] - s_eoff[r * epr];
+        }
+        if (threadIdx.x == 0) rank_offset[R] = s_eoff[E];
+    }
+    if (b == nb - 1) {
+        for (int r = threadIdx.x; r <= R; r += blockDim.x) s_roff[r] = s_eoff[r * epr];
+        __syncthreads();
+        cta_build_schedule(s_roff, R, W, ranks_per_node, self_rank, chunks, n_chunks, worker_begin, s_warp32, s_P);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// fallback path: rank / scan (+ schedule) / finalize
+// ---------------------------------------------------------------------------
+
+__global__ void __launch_bounds__(kLayoutWarps * 32)
+layout_rank_kernel(const int32_t *__restrict__ idx, int32_t T, int32_t E, int32_t k, int32_t nb,
+                   int32_t *__restrict__ block_counts, int32_t *__restrict__ slot) {
+    extern __shared__ int32_t sm[];
+    int32_t *cnt = sm;                                  // [warps][E]
+    int32_t *tile_e = cnt + kLayoutWarps * E;           // [warps][32 k]
+    int32_t *tile_r = tile_e + kLayoutWarps * 32 * k;   // [warps][32 k]
+    const int64_t t_cta = (int64_t)blockIdx.x * kLayoutTokens;
+    cta_rank_tokens(idx, T, E, k, t_cta, cnt, tile_e, tile_r, block_counts + blockIdx.x, nb);
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int64_t t0 = t_cta + (int64_t)warp * 32;
+    const int64_t left = (int64_t)T - t0;
+    const int ntok = left <= 0 ? 0 : (left >= 32 ? 32 : (int)left);
+    const int npair = ntok * k;
+    const int32_t *te = tile_e + warp * 32 * k;
+    const int32_t *tr = tile_r + warp * 32 * k;
+    const int32_t *wc = cnt + warp * E;
+    for (int i = lane; i < npair; i += 32) {
+        const int e = te[i];
+        const int r = tr[i];
+        slot[t0 * k + i] = r < 0 ? -1 : wc[e] + r;
+    }
 }
 
 __global__ void __launch_bounds__(kScanThreads)
@@ -258,41 +572,11 @@ layout_scan_kernel(int32_t *__restrict__ block_counts, int32_t nb, int32_t E, in
     for (int r = threadIdx.x; r < R; r += blockDim.x) rank_count[r] = s_roff[r + 1] - s_roff[r];
 
     // (c) chunk schedule.
-    ClassView cv;
-    cv.ro = s_roff;
-    cv.R = R;
-    const int32_t node = self_rank / ranks_per_node;
-    cv.n_lo = node * ranks_per_node;
-    cv.n_hi = cv.n_lo + ranks_per_node < R ? cv.n_lo + ranks_per_node : R;
-    const int64_t N0 = (int64_t)s_roff[cv.n_hi] - s_roff[cv.n_lo];
-    const int64_t N1 = (int64_t)s_total - N0;
-
-    int64_t carry = 0;
-    for (int32_t wb = 0; wb < W; wb += blockDim.x) {
-        const int32_t w = wb + (int32_t)threadIdx.x;
-        int32_t c1 = 0, c0 = 0;
-        if (w < W) {
-            c1 = worker_class_chunks(cv, 1, N1, w, W, chunks, 0, false);
-            c0 = worker_class_chunks(cv, 0, N0, w, W, chunks, 0, false);
-        }
-        int64_t tile_total;
-        const int64_t first = carry + cta_exclusive_scan(c1 + c0, s_warp, &tile_total);
-        if (w < W) {
-            worker_begin[w] = (int32_t)first;
-            worker_class_chunks(cv, 1, N1, w, W, chunks, (int32_t)first, true);
-            worker_class_chunks(cv, 0, N0, w, W, chunks, (int32_t)(first + c1), true);
-        }
-        carry += tile_total;
-    }
-    if (threadIdx.x == 0) {
-        worker_begin[W] = (int32_t)carry;
-        *n_chunks = (int32_t)carry;
-    }
+    __shared__ int s_warp32[32];
+    __shared__ int32_t s_P[kMaxE + 2];
+    cta_build_schedule(s_roff, R, W, ranks_per_node, self_rank, chunks, n_chunks, worker_begin, s_warp32, s_P);
 }
 
-// ---------------------------------------------------------------------------
-// 3. slot = CTA base + rank inside the CTA
-// ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256)
 layout_finalize_kernel(const int32_t *__restrict__ idx, const int32_t *__restrict__ block_base,
                        int32_t *__restrict__ slot, int64_t npairs, int32_t k, int32_t E, int32_t nb) {
@@ -311,16 +595,12 @@ size_t rank_smem_bytes(int32_t E, int32_t k) {
     return sizeof(int32_t) * ((size_t)kLayoutWarps * E + 2 * (size_t)kLayoutWarps * 32 * k);
 }
 
-}  // namespace
-
-cudaError_t launch_layout(const ep_config &c, int32_t W, const int32_t *idx, int32_t *expert_count,
-                          int32_t *expert_offset, int32_t *rank_count, int32_t *rank_offset, int32_t *slot,
-                          ep_chunk *chunks, int32_t *n_chunks, int32_t *worker_begin, void *workspace,
-                          cudaStream_t s) {
+cudaError_t launch_fallback(const ep_config &c, int32_t W, const int32_t *idx, int32_t *expert_count,
+                            int32_t *expert_offset, int32_t *rank_count, int32_t *rank_offset, int32_t *slot,
+                            ep_chunk *chunks, int32_t *n_chunks, int32_t *worker_begin, void *workspace,
+                            cudaStream_t s) {
     const int64_t nb = layout_blocks(c.T);
-    const LayoutWorkspace ws = layout_workspace(c.T, c.E);
-    int32_t *block_counts = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + ws.block_counts_off);
-
+    int32_t *block_counts = static_cast<int32_t *>(workspace);
     if (nb > 0) {
         const size_t smem = rank_smem_bytes(c.E, c.k);
         if (smem > 48 * 1024) {
@@ -348,6 +628,65 @@ cudaError_t launch_layout(const ep_config &c, int32_t W, const int32_t *idx, int
         e = cudaGetLastError();
     }
     return e;
+}
+
+}  // namespace
+
+static bool layout_fused_fits(const ep_config &c, int *nw_out, int64_t *nb_out) {
+    if (c.T == 0) return false;
+    const int nw = fused_warps(c.T, c.E, c.R, c.k);
+    if (nw == 0) return false;
+    const int64_t nb = (c.T + 32 * nw - 1) / (32 * nw);
+    const size_t smem = fused_smem_bytes(nw, c.E, c.R, c.k);
+    static bool attr_set[kMaxDevices_] = {false};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices_) return false;
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(layout_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kFusedSmemBudget) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        attr_set[dev] = true;
+    }
+    const int per_sm = max_blocks_per_sm(reinterpret_cast<const void *>(layout_fused_kernel), nw * 32, smem);
+    if (nb > (int64_t)sm_count(dev) * per_sm) return false;
+    *nw_out = nw;
+    *nb_out = nb;
+    return true;
+}
+
+int layout_kernel_count(const ep_config &c) {
+    int nw = 0;
+    int64_t nb = 0;
+    if (layout_fused_fits(c, &nw, &nb)) return 1;
+    return layout_blocks(c.T) > 0 ? 3 : 1;
+}
+
+cudaError_t launch_layout(const ep_config &c, int32_t W, const int32_t *idx, int32_t *expert_count,
+                          int32_t *expert_offset, int32_t *rank_count, int32_t *rank_offset, int32_t *slot,
+                          ep_chunk *chunks, int32_t *n_chunks, int32_t *worker_begin, void *workspace,
+                          cudaStream_t s) {
+    int nw = 0;
+    int64_t nb = 0;
+    if (!layout_fused_fits(c, &nw, &nb))
+        return launch_fallback(c, W, idx, expert_count, expert_offset, rank_count, rank_offset, slot, chunks,
+                               n_chunks, worker_begin, workspace, s);
+
+    const LayoutWorkspace ws = layout_workspace(c);
+    int32_t *counts = static_cast<int32_t *>(workspace);
+    unsigned *sync = reinterpret_cast<unsigned *>(static_cast<char *>(workspace) + ws.sync_off);
+    if (nb > 1) {
+        cudaError_t e = cudaMemsetAsync(sync, 0, 2 * sizeof(unsigned), s);
+        if (e != cudaSuccess) return e;
+    }
+    const size_t smem = fused_smem_bytes(nw, c.E, c.R, c.k);
+    int32_t T = c.T, E = c.E, R = c.R, k = c.k, nbi = (int32_t)nb, rpn = c.ranks_per_node, self = c.self_rank;
+    void *args[] = {(void *)&idx, &T, &E, &R, &k, &nbi, (void *)&counts, (void *)&sync, (void *)&expert_count,
+                    (void *)&expert_offset, (void *)&rank_count, (void *)&rank_offset, (void *)&slot,
+                    (void *)&chunks, (void *)&n_chunks, (void *)&worker_begin, &W, &rpn, &self};
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(layout_fused_kernel), dim3((unsigned)nb),
+                                       dim3((unsigned)(nw * 32)), args, smem, s);
 }
 
 }  // namespace ep

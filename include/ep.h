@@ -89,6 +89,14 @@ const char *ep_status_string(int status);
 /* Library version, major * 10000 + minor * 100 + patch. */
 int ep_version(void);
 
+/* Device-side error flags of the current device, read and cleared
+ * (synchronous: waits for work already enqueued on the device). Kernels never
+ * trap; a wait that runs out sets a flag here instead and the kernel returns.
+ *   bit 0 (1): an ep_dispatch CTA gave up waiting for a bulk copy to land; its
+ *              remaining rows were not written.
+ * (ep_layout reports its own bounded wait through *n_chunks = -1.) */
+ep_status ep_device_error(int32_t *flags);
+
 /* Bytes of device scratch that ep_layout needs for `cfg` (it depends on T and
  * E only). The workspace needs no initialisation and may be reused across
  * calls on the same stream. */
@@ -97,6 +105,12 @@ ep_status ep_layout_workspace_size(const ep_config *cfg, size_t *bytes);
 /* Number of ep_chunk records ep_layout may write for `cfg`: 2 W + R
  * (W = num_workers, or the current device's SM count when num_workers = 0). */
 ep_status ep_schedule_capacity(const ep_config *cfg, int32_t *capacity);
+
+/* Number of kernels one ep_route + ep_layout + ep_dispatch + ep_combine pass
+ * enqueues for `cfg` on the current device (the layout is one cooperative
+ * kernel when all its CTAs fit on the GPU at once, else three), for callers
+ * that size CUDA graphs or count launches. */
+ep_status ep_step_kernel_count(const ep_config *cfg, int32_t *kernels);
 
 /*
  * ep_route -- router softmax and top-k for every token.
@@ -155,6 +169,13 @@ ep_status ep_route(const ep_config *cfg, const float *logits, int32_t *topk_idx,
  * worker_begin  : int32 [W + 1]  output
  * workspace     : device scratch of >= ep_layout_workspace_size bytes,
  *                 256-byte aligned; else EP_ERR_CAPACITY / EP_ERR_INVALID_ARG
+ *
+ * When every layout CTA fits on the GPU at once, the layout is one
+ * cooperative launch whose CTAs meet at a grid barrier in the workspace (two
+ * words zeroed by an enqueued memset). That wait is bounded: a CTA that gives
+ * up sets *n_chunks = -1 and leaves its slots unwritten (this cannot happen
+ * under a cooperative launch, which only starts when all CTAs are resident).
+ * Larger T uses three ordinary kernels.
  */
 ep_status ep_layout(const ep_config *cfg, const int32_t *topk_idx,
                     int32_t *expert_count, int32_t *expert_offset,
@@ -212,7 +233,7 @@ ep_status ep_combine(const ep_config *cfg, const ep_bf16 *y, const int32_t *slot
  * cudaMalloc, cudaFree or other allocating routine.
  *  - Limit: shapes whose ep_layout_workspace_size exceeds
  *    EP_LAYOUT_STATIC_SCRATCH_BYTES return EP_ERR_CAPACITY with nothing
- *    enqueued (4 * E * ceil(T / 256) bytes, rounded up to 256: e.g. E = 256
+ *    enqueued (the size is about 4 * E * ceil(T / 256) bytes: e.g. E = 256
  *    allows T <= 262144 tokens).
  *  - Set-up: the first call on a device (made with that device current) looks
  *    up the array's device address; make that first call before any stream

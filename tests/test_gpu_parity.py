@@ -149,8 +149,11 @@ def test_combine_bit_exact(ep, orc, k, E, H, T):
 
 
 @pytest.mark.parametrize("k,E,H,T", [(1, 8, 8, 300), (2, 8, 296, 129), (8, 256, 7168, 40), (5, 32, 1024, 77),
-                                     (32, 1024, 64, 9)])
+                                     (32, 1024, 64, 9), (4, 64, 520, 1000), (8, 256, 4096, 2000),
+                                     (12, 64, 2048, 333), (32, 1024, 1024, 31), (8, 128, 24576, 17)])
 def test_dispatch_bit_exact(ep, orc, k, E, H, T):
+    """Oracle slots into ep_dispatch; covers the vector path (short rows, k % 4 != 0)
+    and the bulk-copy path (k % 4 == 0, rows >= 1 KiB), ragged T."""
     logits = ep_synth.gate_logits(8, T, E)
     idx, _ = orc.route(logits, k)
     lay = orc.layout(idx, E, 1)
@@ -290,3 +293,63 @@ def test_argument_errors(ep):
         ep.ep_layout(cfg, b.topk_idx, b.expert_count, b.expert_offset, b.rank_count, b.rank_offset, b.slot,
                      b.chunks[:3], b.n_chunks, b.worker_begin, b.workspace)
     assert ei.value.status == ep.EP_ERR_CAPACITY
+
+
+@pytest.mark.parametrize("E,k,renorm", [(4, 1, 1), (4, 3, 0), (16, 5, 1), (32, 8, 1), (32, 2, 0), (64, 4, 1),
+                                        (128, 8, 0), (512, 6, 1), (1024, 8, 1), (1024, 7, 0), (96, 8, 1)])
+def test_route_shapes(ep, orc, E, k, renorm):
+    """Every lanes-per-token variant of the route kernels (1 .. 32 lanes), ties included."""
+    T = 333
+    logits = ep_synth.gate_logits(17, T, E)
+    logits[::3] = np.round(logits[::3] * 2) / 2  # every third token: coarse grid, many ties
+    cfg = ep.EpConfig.make(T=T, H=8, E=E, R=1, k=k, renormalize=renorm, num_workers=2)
+    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    ep.ep_route(cfg, torch.from_numpy(logits).cuda(), idx, w)
+    torch.cuda.synchronize()
+    r_idx, r_w = orc.route(logits, k, renormalize=renorm)
+    assert_route(dict(idx=idx.cpu().numpy(), w=w.cpu().numpy()), dict(idx=r_idx, w=r_w), logits, renorm)
+
+
+def test_route_unaligned_logits(ep, orc):
+    """A logits pointer that is not 16-byte aligned takes the general kernel."""
+    T, E, k = 50, 256, 8
+    logits = ep_synth.gate_logits(18, T, E)
+    buf = torch.empty(T * E + 1, dtype=torch.float32, device="cuda")
+    view = buf[1:].view(T, E)
+    view.copy_(torch.from_numpy(logits))
+    cfg = ep.EpConfig.make(T=T, H=8, E=E, R=1, k=k, num_workers=2)
+    idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    ep.ep_route(cfg, view, idx, w)
+    torch.cuda.synchronize()
+    r_idx, r_w = orc.route(logits, k)
+    assert_route(dict(idx=idx.cpu().numpy(), w=w.cpu().numpy()), dict(idx=r_idx, w=r_w), logits, 1)
+
+
+@pytest.mark.parametrize("T,E,R,k", [(400_000, 256, 32, 8), (160_000, 1024, 64, 32)])
+def test_layout_many_ctas(ep, orc, T, E, R, k):
+    """T beyond one co-resident grid: the three-kernel layout path."""
+    rng = np.random.default_rng(T)
+    base = rng.integers(0, E, size=(T, 1))
+    step = rng.integers(1, E // k + 1, size=(T, 1))
+    idx = ((base + step * np.arange(k)[None, :]) % E).astype(np.int32)  # k distinct experts per token
+    assert (np.sort(idx, axis=1)[:, 1:] != np.sort(idx, axis=1)[:, :-1]).all()
+    w = ep_synth.Workload("many", T=T, H=8, E=E, R=R, k=k, num_workers=152)
+    cfg = ep.EpConfig.from_workload(w)
+    b = ep.LayerBuffers.allocate(cfg)
+    b.topk_idx.copy_(torch.from_numpy(idx))
+    b.layout()
+    torch.cuda.synchronize()
+    lay = orc.layout(idx, E, R)
+    ch, wb = orc.schedule(lay["rank_offset"], w.ranks_per_node, w.self_rank, w.num_workers)
+    n = int(b.n_chunks.item())
+    g = dict(expert_count=b.expert_count.cpu().numpy(), expert_offset=b.expert_offset.cpu().numpy(),
+             rank_count=b.rank_count.cpu().numpy(), rank_offset=b.rank_offset.cpu().numpy(),
+             slot=b.slot.cpu().numpy(), chunks=b.chunks[:n].cpu().numpy(), worker_begin=b.worker_begin.cpu().numpy())
+    assert_layout(g, dict(chunks=ch, worker_begin=wb, **lay))
+
+
+def test_no_device_error_flags(ep):
+    """No kernel ran out of a bounded wait during the tests above."""
+    assert ep.ep_device_error() == 0
