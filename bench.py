@@ -42,13 +42,13 @@ if str(ROOT) not in sys.path:
 
 METRIC = "dispatch+combine µs/layer and achieved HBM GB/s (fraction of GB300 peak), 1 GPU"
 FALLBACK_HBM_GBS = 6800.0
-KERNELS = ("route", "layout", "dispatch", "combine")
-# Kernels that profiles/dram_traffic.txt refers to, with the files whose contents fix them.
+# The files whose contents fix each timed kernel (profiles/dram_traffic.txt keys).
 KERNEL_SOURCES = {
-    "route": ["combine_router_softmax_gb300/csrc/route.cu"],
-    "layout": ["combine_router_softmax_gb300/csrc/layout.cu"],
-    "dispatch": ["combine_router_softmax_gb300/csrc/dispatch.cu"],
-    "combine": ["combine_router_softmax_gb300/csrc/combine.cu"],
+    "route": ["route.cu", "route_token.cuh"],
+    "layout": ["layout.cu", "block_common.cuh"],
+    "dispatch": ["dispatch.cu"],
+    "dispatch_fused": ["fused.cu", "block_common.cuh", "route_token.cuh"],
+    "combine": ["combine.cu"],
 }
 
 
@@ -64,6 +64,8 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
     p.add_argument("--no-graph", action="store_true", help="time the per-step launches only (no CUDA graph)")
+    p.add_argument("--separate", action="store_true",
+                   help="step = ep_route, ep_layout, ep_dispatch, ep_combine (default: ep_dispatch_fused, ep_combine)")
     return p.parse_args(argv)
 
 
@@ -164,8 +166,8 @@ def measured_peak_gbs():
 
 def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES[kernel] + ["combine_router_softmax_gb300/csrc/ep_internal.cuh"]:
-        h.update((ROOT / rel).read_bytes())
+    for rel in KERNEL_SOURCES[kernel] + ["ep_internal.cuh"]:
+        h.update((ROOT / "combine_router_softmax_gb300" / "csrc" / rel).read_bytes())
     return h.hexdigest()[:16]
 
 
@@ -277,7 +279,8 @@ def workload_config(w, args, extra=None) -> dict:
            "n_groups": w.n_groups, "topk_groups": w.topk_groups, "renormalize": w.renormalize,
            "zipf_s": w.zipf_s, "ranks_per_node": w.ranks_per_node, "num_workers": w.num_workers,
            "bytes_per_step": w.total_bytes(), "parallelism": f"dp{args.gpus} (independent shards)",
-           "l2": "flushed before every timed step (write of 2x L2)"}
+           "l2": "flushed before every timed step: 2x L2 written, then another 2x L2 read (no dirty line "
+                 "of the flush is written back inside the timed step)"}
     if extra:
         cfg.update(extra)
     return cfg
@@ -287,7 +290,7 @@ def workload_config(w, args, extra=None) -> dict:
 # GPU arm
 # ---------------------------------------------------------------------------
 
-def capture_step_graph(buf, device):
+def capture_step_graph(buf, device, fused: bool):
     """route -> layout -> dispatch -> combine captured once into a CUDA graph.
 
     Two eager passes on the capture stream first, so that every lazy set-up
@@ -298,15 +301,33 @@ def capture_step_graph(buf, device):
     cap = torch.cuda.Stream(device)
     cap.wait_stream(torch.cuda.current_stream(device))
     bound = buf.bind(cap)
+    calls = step_calls(bound, fused)
     with torch.cuda.stream(cap):
         for _ in range(2):
-            bound.route(); bound.layout(); bound.dispatch(); bound.combine()
+            for _, fn in calls:
+                fn()
     cap.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=cap):
-        bound.route(); bound.layout(); bound.dispatch(); bound.combine()
+        for _, fn in calls:
+            fn()
     torch.cuda.synchronize()
     return g
+
+
+def step_calls(bound, fused: bool):
+    """The C-ABI calls of one step, in order, with the names their bytes are booked under."""
+    if fused:
+        return [("dispatch_fused", bound.dispatch_fused), ("combine", bound.combine)]
+    return [("route", bound.route), ("layout", bound.layout), ("dispatch", bound.dispatch),
+            ("combine", bound.combine)]
+
+
+def call_bytes(w, name: str) -> int:
+    kb = w.algorithmic_bytes()
+    if name == "dispatch_fused":
+        return kb["route"] + kb["layout"] + kb["dispatch"]
+    return kb[name]
 
 
 def run_gb300(args):
@@ -337,7 +358,7 @@ def run_gb300(args):
     bound = buf.bind(stream)
 
     # expert output for this batch (outside the timed step)
-    bound.route(); bound.layout(); bound.dispatch()
+    bound.dispatch_fused()
     rows = torch.arange(w.T * w.k, device=device, dtype=torch.int32)
     e = torch.searchsorted(buf.expert_offset, rows, right=True) - 1
     buf.y.copy_((buf.send.float() * ((e + 1).float() / w.E)[:, None]).to(torch.bfloat16))
@@ -345,49 +366,61 @@ def run_gb300(args):
     torch.cuda.synchronize()
 
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=device)
+    flush_w = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=device)
+    flush_r = torch.ones(max(2 * l2, 256 << 20) // 4, dtype=torch.int32, device=device)
+    flush_sink = torch.empty((), dtype=torch.int64, device=device)
+
+    def flush_l2():
+        # Write 2x L2, then read another 2x L2: the step starts with none of its
+        # data in L2 and no dirty line left to write back inside the timed region.
+        flush_w.fill_(1)
+        torch.sum(flush_r, dim=0, dtype=torch.int64, out=flush_sink)
+
+    calls = step_calls(bound, not args.separate)
 
     def step():
-        bound.route(); bound.layout(); bound.dispatch(); bound.combine()
+        for _, fn in calls:
+            fn()
 
     for _ in range(max(args.warmup, 0)):
-        flush.fill_(1)
+        flush_l2()
         step()
     torch.cuda.synchronize()
 
-    graph = None if args.no_graph else capture_step_graph(buf, device)
+    fused = not args.separate
+    graph = None if args.no_graph else capture_step_graph(buf, device, fused)
     if graph is not None:
         for _ in range(max(args.warmup, 0)):
-            flush.fill_(1)
+            flush_l2()
             graph.replay()
         torch.cuda.synchronize()
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    nc = len(calls)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nc + 1)] for _ in range(K)]
     clocks = ClockSampler(local_rank, enabled=not args.no_clocks)
     time.sleep(0.3 if not args.no_clocks else 0)
     barrier(world)
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
     for i in range(K):
-        flush.fill_(1)
-        e5 = ev[i]
-        e5[0].record(stream); bound.route()
-        e5[1].record(stream); bound.layout()
-        e5[2].record(stream); bound.dispatch()
-        e5[3].record(stream); bound.combine()
-        e5[4].record(stream)
+        flush_l2()
+        evs = ev[i]
+        for j, (_, fn) in enumerate(calls):
+            evs[j].record(stream)
+            fn()
+        evs[nc].record(stream)
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - wall0
     clk = clocks.stop()
 
-    per = {n: [] for n in KERNELS}
+    per = {n: [] for n, _ in calls}
     step_ms = []
-    for e5 in ev:
-        for j, n in enumerate(KERNELS):
-            per[n].append(e5[j].elapsed_time(e5[j + 1]))
-        step_ms.append(e5[0].elapsed_time(e5[4]))
+    for evs in ev:
+        for j, (n, _) in enumerate(calls):
+            per[n].append(evs[j].elapsed_time(evs[j + 1]))
+        step_ms.append(evs[0].elapsed_time(evs[nc]))
     stream_ms_per_step = reduce_max(sum(step_ms), world, device) / K
     bytes_step = w.total_bytes()
 
@@ -401,7 +434,7 @@ def run_gb300(args):
         torch.cuda.synchronize()
         gwall0 = time.perf_counter()
         for a, b_ in gev:
-            flush.fill_(1)
+            flush_l2()
             a.record(stream)
             graph.replay()
             b_.record(stream)
@@ -418,8 +451,8 @@ def run_gb300(args):
     value = world * K * bytes_step / (max_total_ms * 1e-3) / 1e9
     ms_per_step = max_total_ms / K
 
-    launches_per_step = ep.ep_step_kernel_count(cfg)
-    kb = w.algorithmic_bytes()
+    launches_per_step = ep.ep_step_kernel_count(cfg, fused=fused)
+    kb = {n: call_bytes(w, n) for n, _ in calls}
     kern_ms = {n: sum(v) / len(v) for n, v in per.items()}
     dom = max(kern_ms, key=kern_ms.get)
     peak, peak_kind = measured_peak_gbs()
@@ -432,7 +465,7 @@ def run_gb300(args):
     h_out = torch.empty((w.T, w.H), dtype=torch.bfloat16).pin_memory()
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(E2E)]
     for i in range(E2E + 3):
-        flush.fill_(1)
+        flush_l2()
         if i >= 3:
             e2e_ev[i - 3][0].record(stream)
         buf.logits.copy_(h_logits, non_blocking=True)
@@ -466,8 +499,9 @@ def run_gb300(args):
         "data": "synthetic",
         "config": workload_config(w0, args),
         "us_per_layer": round(ms_per_step * 1e3, 2),
-        "timing": "CUDA graph of the four C-ABI calls, replayed per step" if graph is not None
-                  else "four C-ABI calls launched per step",
+        "timing": ("CUDA graph of the step's C-ABI calls, replayed per step" if graph is not None
+                   else "the step's C-ABI calls launched per step"),
+        "calls": [n for n, _ in calls],
         "stream_us_per_layer": round(stream_ms_per_step * 1e3, 2),
         "hbm_fraction": round(value / world / peak, 4),
         "kernel_us": {n: round(v * 1e3, 2) for n, v in kern_ms.items()},

@@ -25,8 +25,9 @@ LIB_PATH = _PKG / "libep_gb300.so"
 EP_OK, EP_ERR_INVALID_ARG, EP_ERR_UNSUPPORTED, EP_ERR_CUDA, EP_ERR_CAPACITY = range(5)
 
 # Entry points declared in include/ep.h (checked by the ABI test).
-EXPORTS = ("ep_status_string", "ep_version", "ep_device_error", "ep_step_kernel_count",
-           "ep_layout_workspace_size", "ep_schedule_capacity",
+EXPORTS = ("ep_status_string", "ep_version", "ep_device_error", "ep_step_kernel_count", "ep_fused_step_kernel_count",
+           "ep_layout_workspace_size", "ep_dispatch_fused_workspace_size", "ep_schedule_capacity",
+           "ep_dispatch_fused",
            "ep_route", "ep_layout", "ep_dispatch", "ep_combine", "ep_layout_static")
 # Size of the device array ep_layout_static uses instead of a workspace (include/ep.h).
 EP_LAYOUT_STATIC_SCRATCH_BYTES = 1 << 20
@@ -77,14 +78,19 @@ def _load() -> ctypes.CDLL:
     lib.ep_version.restype = ctypes.c_int
     lib.ep_device_error.argtypes = [P(ctypes.c_int32)]
     lib.ep_step_kernel_count.argtypes = [cfgp, P(ctypes.c_int32)]
+    lib.ep_fused_step_kernel_count.argtypes = [cfgp, P(ctypes.c_int32)]
     lib.ep_layout_workspace_size.argtypes = [cfgp, P(ctypes.c_size_t)]
     lib.ep_schedule_capacity.argtypes = [cfgp, P(ctypes.c_int32)]
     lib.ep_route.argtypes = [cfgp, vp, vp, vp, vp]
     lib.ep_layout.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int32, vp, vp, vp, ctypes.c_size_t, vp]
     lib.ep_layout_static.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int32, vp, vp, vp]
     lib.ep_dispatch.argtypes = [cfgp, vp, vp, vp, vp, vp]
+    lib.ep_dispatch_fused_workspace_size.argtypes = [cfgp, P(ctypes.c_size_t)]
+    lib.ep_dispatch_fused.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int32, vp, vp, vp, vp, vp,
+                                      ctypes.c_size_t, vp]
     lib.ep_combine.argtypes = [cfgp, vp, vp, vp, vp, vp]
-    for f in ("ep_device_error", "ep_step_kernel_count", "ep_layout_workspace_size", "ep_schedule_capacity", "ep_route", "ep_layout",
+    for f in ("ep_dispatch_fused_workspace_size", "ep_dispatch_fused", "ep_fused_step_kernel_count",
+              "ep_device_error", "ep_step_kernel_count", "ep_layout_workspace_size", "ep_schedule_capacity", "ep_route", "ep_layout",
               "ep_dispatch", "ep_combine", "ep_layout_static"):
         getattr(lib, f).restype = ctypes.c_int
     return lib
@@ -140,10 +146,12 @@ def ep_device_error() -> int:
     return int(v.value)
 
 
-def ep_step_kernel_count(cfg: EpConfig) -> int:
-    """Kernels one route + layout + dispatch + combine pass enqueues on the current device."""
+def ep_step_kernel_count(cfg: EpConfig, fused: bool = False) -> int:
+    """Kernels one pass enqueues on the current device: route + layout + dispatch
+    + combine, or (fused=True) dispatch_fused + combine."""
     v = ctypes.c_int32(0)
-    _check(_lib.ep_step_kernel_count(ctypes.byref(cfg), ctypes.byref(v)), "ep_step_kernel_count")
+    f = _lib.ep_fused_step_kernel_count if fused else _lib.ep_step_kernel_count
+    _check(f(ctypes.byref(cfg), ctypes.byref(v)), "ep_step_kernel_count")
     return int(v.value)
 
 
@@ -216,6 +224,43 @@ def ep_layout_static(cfg: EpConfig, topk_idx, expert_count, expert_offset, rank_
            "ep_layout_static")
 
 
+def ep_dispatch_fused_workspace_size(cfg: EpConfig) -> int:
+    n = ctypes.c_size_t(0)
+    _check(_lib.ep_dispatch_fused_workspace_size(ctypes.byref(cfg), ctypes.byref(n)),
+           "ep_dispatch_fused_workspace_size")
+    return int(n.value)
+
+
+def ep_dispatch_fused(cfg: EpConfig, logits, x, topk_idx, topk_w, expert_count, expert_offset, rank_count,
+                      rank_offset, slot, chunks, n_chunks, worker_begin, send, slot_meta, workspace,
+                      stream=None) -> None:
+    """ep_route + ep_layout + ep_dispatch in one call (same outputs)."""
+    T, H, E, R, k = cfg.T, cfg.H, cfg.E, cfg.R, cfg.k
+    if chunks.dim() != 2 or chunks.shape[1] != 5:
+        raise ValueError("chunks: expected int32 [capacity, 5]")
+    W = (ep_schedule_capacity(cfg) - R) // 2
+    if worker_begin.dim() != 1 or worker_begin.numel() < W + 1:
+        raise ValueError(f"worker_begin: expected int32 [>= {W + 1}]")
+    if workspace.dtype != torch.uint8:
+        raise TypeError("workspace: expected a uint8 tensor")
+    _check(_lib.ep_dispatch_fused(ctypes.byref(cfg), _ptr(logits, torch.float32, (T, E), "logits"),
+                                  _ptr(x, torch.bfloat16, (T, H), "x"),
+                                  _ptr(topk_idx, torch.int32, (T, k), "topk_idx"),
+                                  _ptr(topk_w, torch.float32, (T, k), "topk_w"),
+                                  _ptr(expert_count, torch.int32, (E,), "expert_count"),
+                                  _ptr(expert_offset, torch.int32, (E + 1,), "expert_offset"),
+                                  _ptr(rank_count, torch.int32, (R,), "rank_count"),
+                                  _ptr(rank_offset, torch.int32, (R + 1,), "rank_offset"),
+                                  _ptr(slot, torch.int32, (T, k), "slot"),
+                                  _ptr(chunks, torch.int32, None, "chunks"), ctypes.c_int32(chunks.shape[0]),
+                                  _ptr(n_chunks, torch.int32, (1,), "n_chunks"),
+                                  _ptr(worker_begin, torch.int32, None, "worker_begin"),
+                                  _ptr(send, torch.bfloat16, (T * k, H), "send"),
+                                  _ptr(slot_meta, torch.int32, (T * k,), "slot_meta"),
+                                  _ptr(workspace, torch.uint8, None, "workspace"), ctypes.c_size_t(workspace.numel()),
+                                  _stream(stream)), "ep_dispatch_fused")
+
+
 def ep_dispatch(cfg: EpConfig, x, slot, send, slot_meta, stream=None) -> None:
     """x bf16 [T, H] -> send bf16 [T*k, H], slot_meta int32 [T*k]."""
     T, H, k = cfg.T, cfg.H, cfg.k
@@ -277,7 +322,8 @@ class LayerBuffers:
             chunks=torch.empty((cap, 5), **i32),
             n_chunks=torch.empty((1,), **i32),
             worker_begin=torch.empty((W + 1,), **i32),
-            workspace=torch.empty((max(ep_layout_workspace_size(cfg), 256),), dtype=torch.uint8, device=device),
+            workspace=torch.empty((max(ep_layout_workspace_size(cfg), ep_dispatch_fused_workspace_size(cfg), 256),),
+                                  dtype=torch.uint8, device=device),
             send=send,
             slot_meta=torch.empty((T * k,), **i32),
             y=send if y_is_send else torch.empty((T * k, H), dtype=torch.bfloat16, device=device),
@@ -297,6 +343,12 @@ class LayerBuffers:
 
     def combine(self, stream=None):
         ep_combine(self.cfg, self.y, self.slot, self.topk_w, self.out, stream)
+
+    def dispatch_fused(self, stream=None):
+        """route + layout + dispatch in one call."""
+        ep_dispatch_fused(self.cfg, self.logits, self.x, self.topk_idx, self.topk_w, self.expert_count,
+                          self.expert_offset, self.rank_count, self.rank_offset, self.slot, self.chunks,
+                          self.n_chunks, self.worker_begin, self.send, self.slot_meta, self.workspace, stream)
 
     def bind(self, stream=None) -> "BoundLayer":
         """Pre-marshalled C calls on this layer's buffers (same entry points,
@@ -349,7 +401,10 @@ class BoundLayer:
         self._combine = (self._cfg, _ptr(b.y, torch.bfloat16, (T * k, H), "y"), _ptr(b.slot, torch.int32, (T, k), "slot"),
                          _ptr(b.topk_w, torch.float32, (T, k), "topk_w"),
                          _ptr(b.out, torch.bfloat16, (T, H), "out"), st)
-        self._f = (_lib.ep_route, _lib.ep_layout, _lib.ep_dispatch, _lib.ep_combine)
+        self._fused = (self._cfg, self._route[1], self._dispatch[1], self._route[2], self._route[3],
+                       *self._layout[2:7], self._layout[7], self._layout[8], self._layout[9], self._layout[10],
+                       self._dispatch[3], self._dispatch[4], self._layout[11], self._layout[12], st)
+        self._f = (_lib.ep_route, _lib.ep_layout, _lib.ep_dispatch, _lib.ep_combine, _lib.ep_dispatch_fused)
 
     def route(self):
         rc = self._f[0](*self._route)
@@ -370,3 +425,8 @@ class BoundLayer:
         rc = self._f[3](*self._combine)
         if rc:
             raise EpError(rc, "ep_combine")
+
+    def dispatch_fused(self):
+        rc = self._f[4](*self._fused)
+        if rc:
+            raise EpError(rc, "ep_dispatch_fused")

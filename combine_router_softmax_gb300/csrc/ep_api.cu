@@ -125,12 +125,25 @@ int ep_version(void) { return 100; }
 
 ep_status ep_device_error(int32_t *flags) {
     if (!flags) return EP_ERR_INVALID_ARG;
-    int32_t *word = nullptr;
-    if (ep::dispatch_error_word(&word) != cudaSuccess) return EP_ERR_CUDA;
-    int32_t v = 0;
-    if (cudaMemcpy(&v, word, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return EP_ERR_CUDA;
-    if (v != 0 && cudaMemset(word, 0, sizeof v) != cudaSuccess) return EP_ERR_CUDA;
-    *flags = v;
+    int32_t *words[2] = {nullptr, nullptr};
+    if (ep::dispatch_error_word(&words[0]) != cudaSuccess) return EP_ERR_CUDA;
+    if (ep::fused_error_word(&words[1]) != cudaSuccess) return EP_ERR_CUDA;
+    int32_t all = 0;
+    for (int32_t *word : words) {
+        int32_t v = 0;
+        if (cudaMemcpy(&v, word, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return EP_ERR_CUDA;
+        if (v != 0 && cudaMemset(word, 0, sizeof v) != cudaSuccess) return EP_ERR_CUDA;
+        all |= v;
+    }
+    *flags = all;
+    return EP_OK;
+}
+
+ep_status ep_dispatch_fused_workspace_size(const ep_config *cfg, size_t *bytes) {
+    ep_status st = check_config(cfg);
+    if (st != EP_OK) return st;
+    if (!bytes) return EP_ERR_INVALID_ARG;
+    *bytes = ep::fused_workspace_bytes(*cfg);
     return EP_OK;
 }
 
@@ -169,6 +182,20 @@ ep_status ep_step_kernel_count(const ep_config *cfg, int32_t *kernels) {
     return EP_OK;
 }
 
+ep_status ep_fused_step_kernel_count(const ep_config *cfg, int32_t *kernels) {
+    ep_status st = check_config(cfg);
+    if (st != EP_OK) return st;
+    if (!kernels) return EP_ERR_INVALID_ARG;
+    if (cfg->T == 0) {
+        *kernels = 1;
+        return EP_OK;
+    }
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return EP_ERR_CUDA;
+    *kernels = ep::fused_would_run(*cfg) ? 2 : 3 + ep::layout_kernel_count(*cfg);
+    return EP_OK;
+}
+
 ep_status ep_route(const ep_config *cfg, const float *logits, int32_t *topk_idx, float *topk_w,
                    cudaStream_t stream) {
     ep_status st = check_config(cfg);
@@ -199,6 +226,37 @@ ep_status ep_layout(const ep_config *cfg, const int32_t *topk_idx, int32_t *expe
     }
     return from_cuda(ep::launch_layout(*cfg, W, topk_idx, expert_count, expert_offset, rank_count, rank_offset,
                                        slot, chunks, n_chunks, worker_begin, workspace, stream));
+}
+
+ep_status ep_dispatch_fused(const ep_config *cfg, const float *logits, const ep_bf16 *x, int32_t *topk_idx,
+                            float *topk_w, int32_t *expert_count, int32_t *expert_offset, int32_t *rank_count,
+                            int32_t *rank_offset, int32_t *slot, ep_chunk *chunks, int32_t chunk_capacity,
+                            int32_t *n_chunks, int32_t *worker_begin, ep_bf16 *send, int32_t *slot_meta,
+                            void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    ep_status st = check_config(cfg);
+    if (st != EP_OK) return st;
+    if ((st = check_schedule(cfg)) != EP_OK) return st;
+    if ((st = check_rows(cfg)) != EP_OK) return st;
+    if (!expert_count || !expert_offset || !rank_count || !rank_offset || !chunks || !n_chunks || !worker_begin)
+        return EP_ERR_INVALID_ARG;
+    if (cfg->T > 0 && (!logits || !x || !topk_idx || !topk_w || !slot || !send || !slot_meta))
+        return EP_ERR_INVALID_ARG;
+    if (cfg->T > 0 && (!aligned16(x) || !aligned16(send))) return EP_ERR_INVALID_ARG;
+    int32_t W = 0;
+    if ((st = resolve_workers(cfg, &W)) != EP_OK) return st;
+    if ((int64_t)chunk_capacity < 2 * (int64_t)W + cfg->R) return EP_ERR_CAPACITY;
+    const size_t need = ep::fused_workspace_bytes(*cfg);
+    if (need > 0) {
+        if (!workspace) return EP_ERR_INVALID_ARG;
+        if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return EP_ERR_INVALID_ARG;
+        if (workspace_bytes < need) return EP_ERR_CAPACITY;
+    }
+    if (cfg->T == 0)
+        return from_cuda(ep::launch_layout(*cfg, W, topk_idx, expert_count, expert_offset, rank_count, rank_offset,
+                                           slot, chunks, n_chunks, worker_begin, workspace, stream));
+    return from_cuda(ep::launch_dispatch_fused(*cfg, W, logits, x, topk_idx, topk_w, expert_count, expert_offset,
+                                               rank_count, rank_offset, slot, chunks, n_chunks, worker_begin, send,
+                                               slot_meta, workspace, stream));
 }
 
 ep_status ep_dispatch(const ep_config *cfg, const ep_bf16 *x, const int32_t *slot, ep_bf16 *send,

@@ -10,7 +10,7 @@
 
 #include <cuda_runtime.h>
 
-#include "../../include/ep.h"
+#include "ep.h"
 
 namespace ep {
 
@@ -157,6 +157,17 @@ __device__ __forceinline__ void bulk_wait() {
 // Device-side error flags (bit values), one word per translation unit that
 // can set them; ep_device_error() collects and clears them.
 constexpr int32_t kErrDispatchWait = 1;  // a dispatch CTA gave up waiting for a bulk copy
+constexpr int32_t kErrFusedWait = 2;     // a fused-dispatch CTA gave up waiting (barrier or bulk copy)
 cudaError_t dispatch_error_word(int32_t **addr);
+cudaError_t fused_error_word(int32_t **addr);
+
+// Fused route + layout + dispatch (fused.cu).
+size_t fused_workspace_bytes(const ep_config &c);
+bool fused_would_run(const ep_config &c);
+cudaError_t launch_dispatch_fused(const ep_config &c, int32_t W, const float *logits, const ep_bf16 *x,
+                                  int32_t *topk_idx, float *topk_w, int32_t *expert_count, int32_t *expert_offset,
+                                  int32_t *rank_count, int32_t *rank_offset, int32_t *slot, ep_chunk *chunks,
+                                  int32_t *n_chunks, int32_t *worker_begin, ep_bf16 *send, int32_t *meta,
+                                  void *workspace, cudaStream_t s);
 
 }  // namespace ep

@@ -1,0 +1,456 @@
+// fused.cu -- ep_dispatch_fused: route, layout and dispatch in one cooperative
+// launch (the UBEP article's "Kernel Decomposition": metadata work and token
+// movement in one kernel, with the SyncAll barriers between separate phases
+// replaced by cores that poll global memory for the metadata they need).
+//
+// Each CTA owns a contiguous tile of tokens and takes it through every step:
+//   0. lane 0 of warp 0 starts TMA bulk loads of the tile's first x rows into
+//      shared-memory stages (they land while the metadata is computed);
+//   A. route: one warp per token (route_token.cuh), picks kept in shared memory;
+//   B. rank: the tile's (token, expert) pairs are ranked per expert
+//      (cta_rank_pairs) and the tile's per-expert counts published;
+//   C. bounded grid barrier;
+//   D. column scan: CTA q scans expert q's counts over all tiles (one value per
+//      thread) and publishes each tile's base inside the expert and the total;
+//   E. bounded grid barrier;
+//   F. each CTA reads its tile's bases and the totals, scans the totals into
+//      expert offsets and writes its slots; CTA 0 writes counts and offsets and
+//      the last CTA builds the chunk schedule;
+//   G. dispatch of the CTA's own tile from the prefetched stages: lanes j < k
+//      bulk-store each row to its k send rows.
+// Every result equals what ep_route, ep_layout and ep_dispatch write.
+#include "block_common.cuh"
+#include "route_token.cuh"
+
+namespace ep {
+namespace {
+
+constexpr int kFusedWarps = 8;
+constexpr int kFusedThreads = 32 * kFusedWarps;
+constexpr int kMaxTilePairs = 2048;   // tokens per tile * k
+constexpr int kMaxFusedStages = 8;
+constexpr int kMaxFusedCTAs = 1024;
+constexpr uint32_t kFusedMaxPolls = 1u << 22;
+constexpr size_t kFusedSmemLimit = 200 * 1024;
+
+static __device__ int32_t g_fused_error;
+
+struct FusedPlan {
+    int nb = 0;       // CTAs (tiles)
+    int tb = 0;       // tokens per tile
+    int ns = 0;       // x-row stages per CTA (bulk path), 0 = vector copy
+    int row_pad = 0;  // bytes per stage
+    size_t smem = 0;
+};
+
+size_t align128(size_t b) { return (b + 127) & ~(size_t)127; }
+
+// Shared-memory carve-up, in this order (each piece 128-byte aligned):
+// stages, mbarriers, tile_e, tile_r, tile_s, cnt [8][E], group logits [8][E],
+// cand [8][32] int2, pick [8][32] int2, s_tot [E], s_eoff [E+2], s_base [E],
+// s_roff [R+1], s_P [R+2].
+struct SmemLayout {
+    size_t stages, bars, tile_e, tile_r, tile_s, cnt, glog, cand, pick, tot, eoff, base, roff, P, bytes;
+};
+
+__host__ __device__ inline SmemLayout smem_layout(int ns, int row_pad, int tb, int32_t k, int32_t E, int32_t R,
+                                                  bool groups) {
+    SmemLayout L;
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o += (bytes + 127) & ~(size_t)127;
+        return at;
+    };
+    L.stages = take((size_t)ns * row_pad);
+    L.bars = take(sizeof(uint64_t) * kMaxFusedStages);
+    L.tile_e = take(sizeof(int32_t) * (size_t)tb * k);
+    L.tile_r = take(sizeof(int32_t) * (size_t)tb * k);
+    L.tile_s = take(sizeof(int32_t) * (size_t)tb * k);
+    L.cnt = take(sizeof(int32_t) * kFusedWarps * (size_t)E);
+    L.glog = take(groups ? sizeof(float) * kFusedWarps * (size_t)E : 0);
+    L.cand = take(sizeof(int2) * kFusedWarps * 32);
+    L.pick = take(sizeof(int2) * kFusedWarps * 32);
+    L.tot = take(sizeof(int32_t) * (size_t)E);
+    L.eoff = take(sizeof(int32_t) * ((size_t)E + 2));
+    L.base = take(sizeof(int32_t) * (size_t)E);
+    L.roff = take(sizeof(int32_t) * ((size_t)R + 1));
+    L.P = take(sizeof(int32_t) * ((size_t)R + 2));
+    L.bytes = o;
+    return L;
+}
+
+struct FusedArgs {
+    const float *logits;
+    const char *x;
+    int32_t *topk_idx;
+    float *topk_w;
+    int32_t *expert_count, *expert_offset, *rank_count, *rank_offset, *slot;
+    ep_chunk *chunks;
+    int32_t *n_chunks, *worker_begin;
+    char *send;
+    int32_t *meta;
+    int32_t *counts;  // [nb][E] per-tile counts
+    int32_t *bases;   // [nb][E] per-tile base inside each expert
+    int32_t *totals;  // [E]
+    unsigned *sync;   // [2] barrier arrivals
+    int32_t *err;
+    int32_t T, H, E, R, k, n_groups, topk_groups, renormalize, W, rpn, self_rank;
+    int32_t nb, tb, ns, row_pad;
+};
+
+template <int VPL>
+__global__ void __launch_bounds__(kFusedThreads) dispatch_fused_kernel(FusedArgs a) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ int s_warp32[32];
+    const SmemLayout L = smem_layout(a.ns, a.row_pad, a.tb, a.k, a.E, a.R, a.n_groups > 1);
+    unsigned char *stages = smem + L.stages;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + L.bars);
+    int32_t *tile_e = reinterpret_cast<int32_t *>(smem + L.tile_e);
+    int32_t *tile_r = reinterpret_cast<int32_t *>(smem + L.tile_r);
+    int32_t *tile_s = reinterpret_cast<int32_t *>(smem + L.tile_s);
+    int32_t *cnt = reinterpret_cast<int32_t *>(smem + L.cnt);
+    float *glog = reinterpret_cast<float *>(smem + L.glog);
+    int2 *cand = reinterpret_cast<int2 *>(smem + L.cand);
+    int2 *pick = reinterpret_cast<int2 *>(smem + L.pick);
+    int32_t *s_tot = reinterpret_cast<int32_t *>(smem + L.tot);
+    int32_t *s_eoff = reinterpret_cast<int32_t *>(smem + L.eoff);
+    int32_t *s_base = reinterpret_cast<int32_t *>(smem + L.base);
+    int32_t *s_roff = reinterpret_cast<int32_t *>(smem + L.roff);
+    int32_t *s_P = reinterpret_cast<int32_t *>(smem + L.P);
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int b = blockIdx.x;
+    const int E = a.E, k = a.k;
+    const int64_t t0 = (int64_t)b * a.tb;
+    const int ntok = (int)((int64_t)a.T - t0 < a.tb ? (int64_t)a.T - t0 : a.tb);  // >= 1
+    const int np = ntok * k;
+    const int32_t row_bytes = a.H * 2;
+
+    // 0. start the tile's first x rows
+    if (a.ns > 0 && threadIdx.x == 0) {
+        for (int s = 0; s < a.ns; ++s) mbar_init(&bar[s], 1);
+        fence_mbar_init();
+        for (int s = 0; s < a.ns && s < ntok; ++s) {
+            mbar_arrive_expect_tx(&bar[s], (uint32_t)row_bytes);
+            bulk_g2s(stages + (size_t)s * a.row_pad, a.x + (t0 + s) * row_bytes, (uint32_t)row_bytes, &bar[s]);
+        }
+    }
+
+    // A. route the tile, one warp per token
+    for (int i = warp; i < ntok; i += kFusedWarps) {
+        const int64_t t = t0 + i;
+        int e;
+        float w;
+        route_token<VPL>(a.logits + t * E, E, k, a.n_groups, a.topk_groups, a.renormalize, lane, glog + warp * E,
+                         cand + warp * 32, pick + warp * 32, e, w);
+        if (lane < k) {
+            tile_e[i * k + lane] = e;
+            a.topk_idx[t * k + lane] = e;
+            a.topk_w[t * k + lane] = w;
+        }
+        __syncwarp();
+    }
+    __syncthreads();
+
+    // B. rank the tile's pairs; publish the tile's counts
+    const int ppw = (np + kFusedWarps - 1) / kFusedWarps;
+    cta_rank_pairs(tile_e, np, ppw, E, cnt, tile_r, a.counts + (int64_t)b * E, 1);
+
+    // C.
+    bool ok = grid_barrier(&a.sync[0], (unsigned)a.nb);
+
+    // D. column scan: expert e's counts over all tiles, one tile per thread
+    if (ok) {
+        for (int e = b; e < E; e += a.nb) {
+            const int per = (a.nb + blockDim.x - 1) / blockDim.x;
+            const int q0 = threadIdx.x * per;
+            int local = 0;
+            for (int q = q0; q < q0 + per && q < a.nb; ++q) local += __ldcg(a.counts + (int64_t)q * E + e);
+            int total;
+            int run = cta_exclusive_scan32(local, s_warp32, &total);
+            for (int q = q0; q < q0 + per && q < a.nb; ++q) {
+                const int c = __ldcg(a.counts + (int64_t)q * E + e);
+                a.bases[(int64_t)q * E + e] = run;
+                run += c;
+            }
+            if (threadIdx.x == 0) a.totals[e] = total;
+        }
+        // E.
+        ok = grid_barrier(&a.sync[1], (unsigned)a.nb);
+    }
+
+    if (ok) {
+        // F. expert offsets and this tile's slots
+        for (int e = threadIdx.x; e < E; e += blockDim.x) {
+            s_tot[e] = __ldcg(a.totals + e);
+            s_base[e] = __ldcg(a.bases + (int64_t)b * E + e);
+        }
+        __syncthreads();
+        {
+            const int per = (E + blockDim.x - 1) / blockDim.x;
+            const int e0 = threadIdx.x * per;
+            const int e1 = e0 + per < E ? e0 + per : E;
+            int local = 0;
+            for (int e = e0; e < e1; ++e) local += s_tot[e];
+            int total;
+            int run = cta_exclusive_scan32(local, s_warp32, &total);
+            for (int e = e0; e < e1; ++e) {
+                s_eoff[e] = run;
+                run += s_tot[e];
+            }
+            if (threadIdx.x == 0) s_eoff[E] = total;
+        }
+        __syncthreads();
+        for (int p = threadIdx.x; p < np; p += blockDim.x) {
+            const int e = tile_e[p];
+            const int r = tile_r[p];
+            const int sv = r < 0 ? -1 : s_eoff[e] + s_base[e] + cnt[(p / ppw) * E + e] + r;
+            tile_s[p] = sv;
+            a.slot[t0 * k + p] = sv;
+        }
+        const int32_t epr = E / a.R;
+        if (b == 0) {
+            for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+                a.expert_offset[e] = s_eoff[e];
+                if (e < E) a.expert_count[e] = s_tot[e];
+            }
+            for (int r = threadIdx.x; r < a.R; r += blockDim.x) {
+                a.rank_offset[r] = s_eoff[r * epr];
+                a.rank_count[r] = s_eoff[(r + 1) * epr] - s_eoff[r * epr];
+            }
+            if (threadIdx.x == 0) a.rank_offset[a.R] = s_eoff[E];
+        }
+        if (b == a.nb - 1) {
+            for (int r = threadIdx.x; r <= a.R; r += blockDim.x) s_roff[r] = s_eoff[r * epr];
+            __syncthreads();
+            cta_build_schedule(s_roff, a.R, a.W, a.rpn, a.self_rank, a.chunks, a.n_chunks, a.worker_begin, s_warp32,
+                               s_P);
+        }
+        __syncthreads();
+    } else if (threadIdx.x == 0) {
+        atomicOr(a.err, kErrFusedWait);
+        atomicExch(a.n_chunks, -1);
+    }
+
+    // G. dispatch the tile
+    const int64_t rows = (int64_t)a.T * k;
+    if (a.ns > 0) {
+        if (warp != 0) return;
+        int i = 0;
+        bool good = ok;
+        for (; good && i < ntok; ++i) {
+            const int s = i % a.ns;
+            if (!mbar_wait_bounded(&bar[s], (uint32_t)((i / a.ns) & 1), kFusedMaxPolls)) {
+                good = false;
+                break;
+            }
+            const unsigned char *st = stages + (size_t)s * a.row_pad;
+            if (lane < k) {
+                const int sv = tile_s[i * k + lane];
+                if (sv >= 0 && (int64_t)sv < rows) {
+                    bulk_s2g(a.send + (int64_t)sv * row_bytes, st, (uint32_t)row_bytes);
+                    a.meta[sv] = (int32_t)((t0 + i) * k + lane);
+                }
+                bulk_commit();
+            }
+            // refill the stage of row i - 1 once its stores have read it
+            if (i >= 1 && i - 1 + a.ns < ntok) {
+                if (lane < k) bulk_wait_read<1>();
+                __syncwarp();
+                if (lane == 0) {
+                    const int sp = (i - 1) % a.ns;
+                    mbar_arrive_expect_tx(&bar[sp], (uint32_t)row_bytes);
+                    bulk_g2s(stages + (size_t)sp * a.row_pad, a.x + (t0 + i - 1 + a.ns) * row_bytes,
+                             (uint32_t)row_bytes, &bar[sp]);
+                }
+            }
+        }
+        if (!good) {
+            // Let every load already issued land before the CTA goes away.
+            if (lane == 0) atomicOr(a.err, kErrFusedWait);
+            const int issued = (i >= 1 ? i - 1 + a.ns : a.ns) < ntok ? (i >= 1 ? i - 1 + a.ns : a.ns) : ntok;
+            for (int j = i; j < issued; ++j)
+                mbar_wait_bounded(&bar[j % a.ns], (uint32_t)((j / a.ns) & 1), kFusedMaxPolls);
+        }
+        if (lane < k) bulk_wait<0>();
+    } else if (ok) {
+        // rows not suited to bulk copies: 16-byte vector copy by every warp
+        const int hv = a.H / 8;
+        const uint4 *x4 = reinterpret_cast<const uint4 *>(a.x);
+        uint4 *s4 = reinterpret_cast<uint4 *>(a.send);
+        for (int i = warp; i < ntok; i += kFusedWarps) {
+            const int64_t t = t0 + i;
+            for (int v = lane; v < hv; v += 32) {
+                const uint4 val = ld_stream_v4(x4 + t * hv + v);
+                for (int j = 0; j < k; ++j) {
+                    const int sv = tile_s[i * k + j];
+                    if (sv >= 0 && (int64_t)sv < rows) st_v4(s4 + (int64_t)sv * hv + v, val);
+                }
+            }
+            if (lane < k) {
+                const int sv = tile_s[i * k + lane];
+                if (sv >= 0 && (int64_t)sv < rows) a.meta[sv] = (int32_t)(t * k + lane);
+            }
+        }
+    }
+}
+
+using FusedKernel = void (*)(FusedArgs);
+
+FusedKernel pick_kernel(int32_t E) {
+    const int vpl = (E + 31) / 32;
+    if (vpl <= 1) return dispatch_fused_kernel<1>;
+    if (vpl <= 2) return dispatch_fused_kernel<2>;
+    if (vpl <= 4) return dispatch_fused_kernel<4>;
+    if (vpl <= 8) return dispatch_fused_kernel<8>;
+    if (vpl <= 16) return dispatch_fused_kernel<16>;
+    return dispatch_fused_kernel<32>;
+}
+
+// Choose the tiling: as many CTAs as fit on the GPU at once (up to 1024),
+// every CTA holding the same number of tokens. false if the fused kernel
+// cannot run this shape (then the caller runs the three separate steps).
+bool plan_fused(const ep_config &c, FusedPlan *p) {
+    if (c.T <= 0) return false;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices_) return false;
+    const FusedKernel kern = pick_kernel(c.E);
+    static bool attr_set[kMaxDevices_][6] = {};
+    const int vi = ((c.E + 31) / 32 <= 1) ? 0 : ((c.E + 31) / 32 <= 2) ? 1 : ((c.E + 31) / 32 <= 4) ? 2
+                 : ((c.E + 31) / 32 <= 8) ? 3 : ((c.E + 31) / 32 <= 16) ? 4 : 5;
+    if (!attr_set[dev][vi]) {
+        if (cudaFuncSetAttribute(reinterpret_cast<const void *>(kern), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kFusedSmemLimit) != cudaSuccess) {
+            cudaGetLastError();
+            return false;
+        }
+        attr_set[dev][vi] = true;
+    }
+    const int32_t row_bytes = c.H * 2;
+    const bool bulk = c.k % 4 == 0 && row_bytes >= 1024 && row_bytes <= 48 * 1024;
+    const int sms = sm_count(dev);
+    // Try 2, then 1 CTA per SM (more CTAs = smaller tiles = shorter metadata phases).
+    for (int per_sm = 2; per_sm >= 1; --per_sm) {
+        int nb = sms * per_sm;
+        if (nb > kMaxFusedCTAs) nb = kMaxFusedCTAs;
+        int tb = (int)((c.T + nb - 1) / nb);
+        nb = (int)((c.T + tb - 1) / tb);
+        if ((int64_t)tb * c.k > kMaxTilePairs) return false;
+        const int row_pad = (int)align128((size_t)row_bytes);
+        const SmemLayout base = smem_layout(0, row_pad, tb, c.k, c.E, c.R, c.n_groups > 1);
+        int ns = 0;
+        if (bulk) {
+            const size_t budget = kFusedSmemLimit / per_sm - base.bytes - 2048;
+            ns = (int)(budget / row_pad);
+            if (ns > kMaxFusedStages) ns = kMaxFusedStages;
+            if (ns > tb) ns = tb;
+            if (ns < 1) continue;
+        }
+        const SmemLayout L = smem_layout(ns, row_pad, tb, c.k, c.E, c.R, c.n_groups > 1);
+        if (L.bytes > kFusedSmemLimit) continue;
+        const int occ = max_blocks_per_sm(reinterpret_cast<const void *>(kern), kFusedThreads, L.bytes);
+        if (nb > sms * occ) continue;
+        p->nb = nb;
+        p->tb = tb;
+        p->ns = ns;
+        p->row_pad = row_pad;
+        p->smem = L.bytes;
+        return true;
+    }
+    return false;
+}
+
+}  // namespace
+
+cudaError_t fused_error_word(int32_t **addr) {
+    static int32_t *cached[kMaxDevices_] = {nullptr};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices_) return cudaErrorInvalidDevice;
+    if (!cached[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_fused_error);
+        if (e != cudaSuccess) return e;
+        cached[dev] = static_cast<int32_t *>(p);
+    }
+    *addr = cached[dev];
+    return cudaSuccess;
+}
+
+size_t fused_workspace_bytes(const ep_config &c) {
+    const int64_t nb = c.T < kMaxFusedCTAs ? c.T : kMaxFusedCTAs;
+    const size_t tables = 2 * sizeof(int32_t) * (size_t)nb * (size_t)c.E;
+    const size_t fused = ((tables + sizeof(int32_t) * (size_t)c.E + 255) & ~(size_t)255) + 256;
+    const size_t sep = layout_workspace(c).bytes;
+    return c.T == 0 ? 0 : (fused > sep ? fused : sep);
+}
+
+bool fused_would_run(const ep_config &c) {
+    FusedPlan p;
+    return plan_fused(c, &p);
+}
+
+cudaError_t launch_dispatch_fused(const ep_config &c, int32_t W, const float *logits, const ep_bf16 *x,
+                                  int32_t *topk_idx, float *topk_w, int32_t *expert_count, int32_t *expert_offset,
+                                  int32_t *rank_count, int32_t *rank_offset, int32_t *slot, ep_chunk *chunks,
+                                  int32_t *n_chunks, int32_t *worker_begin, ep_bf16 *send, int32_t *meta,
+                                  void *workspace, cudaStream_t s) {
+    FusedPlan p;
+    if (!plan_fused(c, &p)) {
+        cudaError_t e = launch_route(c, logits, topk_idx, topk_w, s);
+        if (e != cudaSuccess) return e;
+        e = launch_layout(c, W, topk_idx, expert_count, expert_offset, rank_count, rank_offset, slot, chunks,
+                          n_chunks, worker_begin, workspace, s);
+        if (e != cudaSuccess) return e;
+        return launch_dispatch(c, x, slot, send, meta, s);
+    }
+    FusedArgs a;
+    a.logits = logits;
+    a.x = reinterpret_cast<const char *>(x);
+    a.topk_idx = topk_idx;
+    a.topk_w = topk_w;
+    a.expert_count = expert_count;
+    a.expert_offset = expert_offset;
+    a.rank_count = rank_count;
+    a.rank_offset = rank_offset;
+    a.slot = slot;
+    a.chunks = chunks;
+    a.n_chunks = n_chunks;
+    a.worker_begin = worker_begin;
+    a.send = reinterpret_cast<char *>(send);
+    a.meta = meta;
+    char *ws = static_cast<char *>(workspace);
+    const size_t table = sizeof(int32_t) * (size_t)p.nb * (size_t)c.E;
+    a.counts = reinterpret_cast<int32_t *>(ws);
+    a.bases = reinterpret_cast<int32_t *>(ws + table);
+    a.totals = reinterpret_cast<int32_t *>(ws + 2 * table);
+    const size_t sync_off = (2 * table + sizeof(int32_t) * (size_t)c.E + 255) & ~(size_t)255;
+    a.sync = reinterpret_cast<unsigned *>(ws + sync_off);
+    cudaError_t e = fused_error_word(&a.err);
+    if (e != cudaSuccess) return e;
+    a.T = c.T;
+    a.H = c.H;
+    a.E = c.E;
+    a.R = c.R;
+    a.k = c.k;
+    a.n_groups = c.n_groups;
+    a.topk_groups = c.topk_groups;
+    a.renormalize = c.renormalize;
+    a.W = W;
+    a.rpn = c.ranks_per_node;
+    a.self_rank = c.self_rank;
+    a.nb = p.nb;
+    a.tb = p.tb;
+    a.ns = p.ns;
+    a.row_pad = p.row_pad;
+    e = cudaMemsetAsync(a.sync, 0, 2 * sizeof(unsigned), s);
+    if (e != cudaSuccess) return e;
+    void *args[] = {&a};
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(pick_kernel(c.E)), dim3((unsigned)p.nb),
+                                       dim3(kFusedThreads), args, p.smem, s);
+}
+
+}  // namespace ep

@@ -31,7 +31,7 @@
 // per step, ~log4(n) steps), then cuts its share at rank boundaries.
 #include <climits>
 
-#include "ep_internal.cuh"
+#include "block_common.cuh"
 
 namespace ep {
 
@@ -40,7 +40,6 @@ namespace {
 constexpr int kScanThreads = 1024;
 constexpr int kFusedMaxWarps = 32;
 constexpr size_t kFusedSmemBudget = 160 * 1024;
-constexpr unsigned kBarrierSpinLimit = 1u << 22;  // polls of ~64 ns before giving up
 
 size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
 
@@ -77,300 +76,6 @@ LayoutWorkspace layout_workspace(const ep_config &c) {
 }
 
 namespace {
-
-// ---------------------------------------------------------------------------
-// shared device pieces
-// ---------------------------------------------------------------------------
-
-// Exclusive scan of one value per thread over the CTA; returns the prefix and
-// stores the CTA total in *total. Uses s_warp[32].
-__device__ __forceinline__ int64_t cta_exclusive_scan(int64_t x, int64_t *s_warp, int64_t *total) {
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    const int nwarps = blockDim.x >> 5;
-    int64_t inc = x;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const int64_t o = __shfl_up_sync(0xffffffffu, inc, d);
-        if (lane >= d) inc += o;
-    }
-    if (lane == 31) s_warp[warp] = inc;
-    __syncthreads();
-    if (warp == 0) {
-        int64_t wv = lane < nwarps ? s_warp[lane] : 0;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const int64_t o = __shfl_up_sync(0xffffffffu, wv, d);
-            if (lane >= d) wv += o;
-        }
-        if (lane < nwarps) s_warp[lane] = wv;  // inclusive warp prefix
-    }
-    __syncthreads();
-    const int64_t base = warp > 0 ? s_warp[warp - 1] : 0;
-    *total = s_warp[nwarps - 1];
-    __syncthreads();  // s_warp may be reused by the caller
-    return base + inc - x;
-}
-
-// 32-bit exclusive scan of one value per thread over the CTA (s_warp: 32 ints).
-__device__ __forceinline__ int cta_exclusive_scan32(int x, int *s_warp, int *total) {
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    const int nwarps = blockDim.x >> 5;
-    int inc = x;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, inc, d);
-        if (lane >= d) inc += o;
-    }
-    if (lane == 31) s_warp[warp] = inc;
-    __syncthreads();
-    if (warp == 0) {
-        int wv = lane < nwarps ? s_warp[lane] : 0;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const int o = __shfl_up_sync(0xffffffffu, wv, d);
-            if (lane >= d) wv += o;
-        }
-        if (lane < nwarps) s_warp[lane] = wv;
-    }
-    __syncthreads();
-    const int base = warp > 0 ? s_warp[warp - 1] : 0;
-    *total = s_warp[nwarps - 1];
-    __syncthreads();
-    return base + inc - x;
-}
-
-// Threads that share one expert's work in a CTA of nw warps: the largest power
-// of two <= min(32 nw / E, nw, 32), at least 1.
-__device__ __forceinline__ int threads_per_expert(int32_t E, int nw) {
-    int cap = (32 * nw) / E;
-    if (cap > nw) cap = nw;
-    if (cap > 32) cap = 32;
-    int t = 1;
-    while (2 * t <= cap) t <<= 1;
-    return t;
-}
-
-// Rank phase for the CTA's tokens [t_cta, t_cta + 32 nw). On return (after a
-// CTA barrier): tile_e / tile_r hold each pair's expert and its rank among the
-// same warp's earlier pairs of that expert (-1 for an id outside [0, E));
-// cnt[w][e] holds the number of pairs of expert e in warps < w; and
-// cta_count[e * stride] the CTA's total for expert e.
-//
-// A warp ranks 32 consecutive pairs (token order) per step: __match_any_sync
-// groups the lanes holding the same expert, a lane's rank inside the step is
-// the number of lower lanes in its group, and the group's highest lane
-// advances the warp's shared counter for that expert. The k experts of one
-// token are distinct, so lanes of one token never match each other.
-__device__ void cta_rank_tokens(const int32_t *__restrict__ idx, int32_t T, int32_t E, int32_t k, int64_t t_cta,
-                                int32_t *cnt, int32_t *tile_e, int32_t *tile_r, int32_t *cta_count,
-                                int64_t stride) {
-    const int nw = blockDim.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    for (int i = threadIdx.x; i < nw * E; i += blockDim.x) cnt[i] = 0;
-
-    const int64_t t0 = t_cta + (int64_t)warp * 32;
-    const int64_t left = (int64_t)T - t0;
-    const int ntok = left <= 0 ? 0 : (left >= 32 ? 32 : (int)left);
-    const int npair = ntok * k;
-    int32_t *te = tile_e + warp * 32 * k;
-    int32_t *tr = tile_r + warp * 32 * k;
-    int32_t *wc = cnt + warp * E;
-    for (int i = lane; i < npair; i += 32) te[i] = __ldg(idx + t0 * k + i);
-    __syncthreads();
-
-    const unsigned below = (1u << lane) - 1u;
-    const unsigned above = ~((2u << lane) - 1u);
-    for (int p0 = 0; p0 < npair; p0 += 32) {
-        const int p = p0 + lane;
-        const int e = p < npair ? te[p] : -1;
-        const bool valid = (unsigned)e < (unsigned)E;
-        const unsigned peers = __match_any_sync(0xffffffffu, valid ? e : E + lane);
-        const int basec = valid ? wc[e] : 0;
-        __syncwarp();
-        if (valid && (peers & above) == 0) wc[e] = basec + __popc(peers);
-        if (p < npair) tr[p] = valid ? basec + __popc(peers & below) : -1;
-        __syncwarp();
-    }
-    __syncthreads();
-
-    // Exclusive scan over the warps, per expert. tpe consecutive threads share
-    // an expert, each scanning a contiguous run of nw / tpe warps; a shuffle
-    // scan joins the runs. Rounds are uniform across the CTA (shuffles need
-    // every lane).
-    const int tpe = threads_per_expert(E, nw);
-    const int sub = (int)threadIdx.x % tpe;
-    const int runlen = nw / tpe;
-    const int per_round = blockDim.x / tpe;
-    for (int base = 0; base < E; base += per_round) {
-        const int e0 = base + (int)threadIdx.x / tpe;
-        const bool act = e0 < E;
-        int local = 0;
-        if (act)
-            for (int w = sub * runlen; w < (sub + 1) * runlen; ++w) local += cnt[w * E + e0];
-        int incl = local;
-        for (int d = 1; d < tpe; d <<= 1) {
-            const int o = __shfl_up_sync(0xffffffffu, incl, d, tpe);
-            if (sub >= d) incl += o;
-        }
-        if (act) {
-            int run = incl - local;
-            for (int w = sub * runlen; w < (sub + 1) * runlen; ++w) {
-                const int c = cnt[w * E + e0];
-                cnt[w * E + e0] = run;
-                run += c;
-            }
-            if (sub == tpe - 1) cta_count[(int64_t)e0 * stride] = incl;
-        }
-    }
-    __syncthreads();
-}
-
-// Largest i in [0, n) with P[i] <= x, for P non-decreasing with P[0] <= x.
-// 4-ary search: three independent pivot compares narrow the range 4x per step.
-__device__ __forceinline__ int32_t quaternary_search(const int32_t *P, int32_t n, int32_t x) {
-    int32_t lo = 0, hi = n;  // answer in [lo, hi), P[lo] <= x
-    while (hi - lo > 1) {
-        const int32_t len = hi - lo;
-        const int32_t q1 = lo + len / 4, q2 = lo + len / 2, q3 = lo + (3 * len) / 4;
-        const bool c1 = P[q1] <= x;
-        const bool c2 = P[q2] <= x;
-        const bool c3 = P[q3] <= x;
-        if (c3) {
-            lo = q3;
-        } else if (c2) {
-            lo = q2;
-            hi = q3;
-        } else if (c1) {
-            lo = q1;
-            hi = q2;
-        } else {
-            hi = q1;
-        }
-    }
-    return lo;
-}
-
-// floor(N w / W) for the share boundaries (32-bit whenever it cannot overflow).
-__device__ __forceinline__ int32_t share_bound(int32_t N, int32_t w, int32_t W) {
-    if ((uint64_t)(uint32_t)N * (uint32_t)W <= 0xffffffffull) return (int32_t)((uint32_t)N * (uint32_t)w / (uint32_t)W);
-    return (int32_t)((int64_t)N * w / W);
-}
-
-// The chunk schedule, built by one whole CTA from rank offsets in shared
-// memory. Class 0 (near) is ranks [n_lo, n_hi) of self_rank's node; class 1
-// (far) is [0, n_lo) followed by [n_hi, R). s_P (R + 2 ints of shared memory)
-// receives each class's prefix sums P_c[i] = rows in its first i ranks. A
-// worker finds the first and last rank its share touches by two quaternary
-// searches per class, counts the non-empty ranks in between, and after a CTA
-// scan over the counts writes its chunks.
-__device__ void cta_build_schedule(const int32_t *s_roff, int32_t R, int32_t W, int32_t ranks_per_node,
-                                   int32_t self_rank, ep_chunk *chunks, int32_t *n_chunks, int32_t *worker_begin,
-                                   int *s_warp, int32_t *s_P) {
-    const int32_t node = self_rank / ranks_per_node;
-    const int32_t n_lo = node * ranks_per_node;
-    const int32_t n_hi = n_lo + ranks_per_node < R ? n_lo + ranks_per_node : R;
-    const int32_t n0 = n_hi - n_lo, n1 = R - n0;
-    int32_t *P1 = s_P;           // far class: n1 + 1 entries
-    int32_t *P0 = s_P + n1 + 1;  // near class: n0 + 1 entries
-    for (int32_t i = threadIdx.x; i <= n1; i += blockDim.x)
-        P1[i] = i <= n_lo ? s_roff[i] : s_roff[n_lo] + (s_roff[i + n0] - s_roff[n_hi]);
-    for (int32_t i = threadIdx.x; i <= n0; i += blockDim.x) P0[i] = s_roff[n_lo + i] - s_roff[n_lo];
-    __syncthreads();
-    const int32_t N[2] = {P0[n0], P1[n1]};
-
-    int carry = 0;
-    for (int32_t wb = 0; wb < W; wb += blockDim.x) {
-        const int32_t w = wb + (int32_t)threadIdx.x;
-        int32_t first[2] = {0, 0}, last[2] = {-1, -1}, lo[2] = {0, 0}, hi[2] = {0, 0};
-        int cnt = 0;
-        if (w < W) {
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const int32_t *P = c ? P1 : P0;
-                const int32_t n = c ? n1 : n0;
-                lo[c] = share_bound(N[c], w, W);
-                hi[c] = share_bound(N[c], w + 1, W);
-                if (hi[c] > lo[c]) {
-                    first[c] = quaternary_search(P, n, lo[c]);
-                    last[c] = quaternary_search(P, n, hi[c] - 1);
-                    for (int32_t i = first[c]; i <= last[c]; ++i) cnt += P[i + 1] > P[i] ? 1 : 0;
-                }
-            }
-        }
-        int tile_total;
-        const int pos0 = carry + cta_exclusive_scan32(cnt, s_warp, &tile_total);
-        if (w < W) {
-            worker_begin[w] = pos0;
-            int pos = pos0;
-#pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                const int c = 1 - cc;  // other-node traffic first
-                const int32_t *P = c ? P1 : P0;
-                for (int32_t i = first[c]; i <= last[c]; ++i) {
-                    if (P[i + 1] == P[i]) continue;
-                    const int32_t r = c ? (i < n_lo ? i : i + n0) : n_lo + i;
-                    const int32_t a = lo[c] > P[i] ? lo[c] : P[i];
-                    const int32_t bnd = hi[c] < P[i + 1] ? hi[c] : P[i + 1];
-                    ep_chunk ch;
-                    ch.worker = w;
-                    ch.hop_class = c;
-                    ch.dst_rank = r;
-                    ch.row_begin = s_roff[r] + (a - P[i]);
-                    ch.row_count = bnd - a;
-                    chunks[pos++] = ch;
-                }
-            }
-        }
-        carry += tile_total;
-    }
-    if (threadIdx.x == 0) {
-        worker_begin[W] = carry;
-        *n_chunks = carry;
-    }
-}
-
-// ---------------------------------------------------------------------------
-// fused path
-// ---------------------------------------------------------------------------
-
-__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void red_release_gpu_add(unsigned *p, unsigned v) {
-    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// Grid barrier for co-resident CTAs: after a CTA barrier, thread 0 fences the
-// CTA's global writes, arrives with a release add and polls with acquire
-// loads. Bounded: returns false (for every thread of the CTA) if the count did
-// not arrive in time.
-__device__ bool grid_barrier(unsigned *arrivals, unsigned expected) {
-    __shared__ int s_ok;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        red_release_gpu_add(arrivals, 1u);
-        int ok = 1;
-        unsigned spins = 0;
-        while (ld_acquire_gpu(arrivals) < expected) {
-            if (++spins > kBarrierSpinLimit) {
-                ok = 0;
-                break;
-            }
-            if (spins > 64) __nanosleep(32);
-        }
-        __threadfence();
-        s_ok = ok;
-    }
-    __syncthreads();
-    return s_ok != 0;
-}
 
 __global__ void __launch_bounds__(kFusedMaxWarps * 32)
 layout_fused_kernel(const int32_t *__restrict__ idx, int32_t T, int32_t E, int32_t R, int32_t k, int32_t nb,
@@ -460,19 +165,12 @@ layout_fused_kernel(const int32_t *__restrict__ idx, int32_t T, int32_t E, int32
 
     // Final slots of this CTA's pairs.
     {
-        const int lane = threadIdx.x & 31;
-        const int warp = threadIdx.x >> 5;
-        const int64_t t0 = t_cta + (int64_t)warp * 32;
-        const int64_t left = (int64_t)T - t0;
-        const int ntok = left <= 0 ? 0 : (left >= 32 ? 32 : (int)left);
-        const int npair = ntok * k;
-        const int32_t *te = tile_e + warp * 32 * k;
-        const int32_t *tr = tile_r + warp * 32 * k;
-        const int32_t *wc = cnt + warp * E;
-        for (int i = lane; i < npair; i += 32) {
-            const int e = te[i];
-            const int r = tr[i];
-            slot[t0 * k + i] = r < 0 ? -1 : s_eoff[e] + s_pre[e] + wc[e] + r;
+        const int64_t left = (int64_t)T - t_cta;
+        const int np = (left <= 0 ? 0 : (left >= 32 * nw ? 32 * nw : (int)left)) * k;
+        for (int p = threadIdx.x; p < np; p += blockDim.x) {
+            const int e = tile_e[p];
+            const int r = tile_r[p];
+            slot[t_cta * k + p] = r < 0 ? -1 : s_eoff[e] + s_pre[e] + cnt[(p / (32 * k)) * E + e] + r;
         }
     }
 
@@ -509,19 +207,12 @@ layout_rank_kernel(const int32_t *__restrict__ idx, int32_t T, int32_t E, int32_
     const int64_t t_cta = (int64_t)blockIdx.x * kLayoutTokens;
     cta_rank_tokens(idx, T, E, k, t_cta, cnt, tile_e, tile_r, block_counts + blockIdx.x, nb);
 
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    const int64_t t0 = t_cta + (int64_t)warp * 32;
-    const int64_t left = (int64_t)T - t0;
-    const int ntok = left <= 0 ? 0 : (left >= 32 ? 32 : (int)left);
-    const int npair = ntok * k;
-    const int32_t *te = tile_e + warp * 32 * k;
-    const int32_t *tr = tile_r + warp * 32 * k;
-    const int32_t *wc = cnt + warp * E;
-    for (int i = lane; i < npair; i += 32) {
-        const int e = te[i];
-        const int r = tr[i];
-        slot[t0 * k + i] = r < 0 ? -1 : wc[e] + r;
+    const int64_t left = (int64_t)T - t_cta;
+    const int np = (left <= 0 ? 0 : (left >= kLayoutTokens ? kLayoutTokens : (int)left)) * k;
+    for (int p = threadIdx.x; p < np; p += blockDim.x) {
+        const int e = tile_e[p];
+        const int r = tile_r[p];
+        slot[t_cta * k + p] = r < 0 ? -1 : cnt[(p / (32 * k)) * E + e] + r;
     }
 }
 

@@ -6,74 +6,13 @@
 // UBEP article only says each token goes to the device of its selected expert
 // (opening section); the router itself is the plainest reading.
 //
-// One warp per token; lane l holds logits e = l + 32 i (coalesced 128-byte
-// loads). Selection compares raw fp32 logits under the total order
-// (logit desc, index asc), so the chosen experts do not depend on the exp
-// implementation. It runs in three short warp-wide steps instead of k rounds
-// of arg-max:
-//   1. tau = the k-th largest of the 32 lane maxima (a 15-step bitonic sort of
-//      one float per lane). At least k logits are >= tau, so the top k all are.
-//   2. The logits >= tau are the candidates; a warp prefix sum packs them into
-//      shared memory (usually 8-12 of them for k = 8).
-//   3. If there are at most 32, each candidate counts the candidates ordered
-//      before it; that count is its rank, and the top k are written straight
-//      to their places. Otherwise (massive ties) the kernel falls back to k
-//      rounds of a butterfly arg-max.
-//
-// Weights: with renormalisation the full softmax denominator cancels, so
-// w_j = exp(l_j - l_max) / sum_i exp(l_i - l_max) over the k picks only; pick 0
-// is the global maximum (the group holding it always survives group
-// limiting). Without it, w_j = exp(l_j - l_max) / sum over all E.
-#include <cfloat>
-#include <climits>
-
-#include "ep_internal.cuh"
+// One warp per token (route_token.cuh); 8 tokens per CTA.
+#include "route_token.cuh"
 
 namespace ep {
 namespace {
 
 constexpr int kRouteWarps = 8;  // tokens per CTA
-
-// (va, ia) ranks before (vb, ib): larger logit, or equal logit and lower index.
-// INT_MAX marks "no candidate" and never ranks before a real entry.
-__device__ __forceinline__ bool before(float va, int ia, float vb, int ib) {
-    if (ia == INT_MAX) return false;
-    if (ib == INT_MAX) return true;
-    return va > vb || (va == vb && ia < ib);
-}
-
-// Butterfly arg-max over the warp under `before`; every lane ends with the winner.
-__device__ __forceinline__ void warp_argmax(float &v, int &i) {
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, v, m);
-        const int oi = __shfl_xor_sync(0xffffffffu, i, m);
-        if (before(ov, oi, v, i)) {
-            v = ov;
-            i = oi;
-        }
-    }
-}
-
-__device__ __forceinline__ float warp_sum(float x) {
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
-    return x;
-}
-
-// Bitonic sort of one float per lane, descending in lane order.
-__device__ __forceinline__ float warp_sort_desc(float s, int lane) {
-#pragma unroll
-    for (int size = 2; size <= 32; size <<= 1) {
-#pragma unroll
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            const float o = __shfl_xor_sync(0xffffffffu, s, stride);
-            const bool keep_max = ((lane & size) == 0) == ((lane & stride) == 0);
-            s = keep_max ? fmaxf(s, o) : fminf(s, o);
-        }
-    }
-    return s;
-}
 
 template <int VPL>
 __global__ void __launch_bounds__(kRouteWarps * 32)
@@ -87,145 +26,15 @@ route_kernel(const float *__restrict__ logits, int32_t T, int32_t E, int32_t k, 
     const int warp = threadIdx.x >> 5;
     const int64_t t = (int64_t)blockIdx.x * kRouteWarps + warp;
     if (t >= T) return;  // whole warp leaves together; no CTA-wide barrier follows
-
-    const float *row = logits + t * E;
-    float v[VPL];
-    uint32_t elig = 0;  // bit i: value i may be picked
-#pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E) {
-            v[i] = __ldg(row + e);
-            elig |= 1u << i;
-        } else {
-            v[i] = -INFINITY;
-        }
-    }
-
-    if (n_groups > 1) {
-        // Group score = largest logit of the group; keep the topk_groups best.
-        float *sl = s_dyn + warp * E;
-#pragma unroll
-        for (int i = 0; i < VPL; ++i) {
-            const int e = lane + 32 * i;
-            if (e < E) sl[e] = v[i];
-        }
-        __syncwarp();
-        const int gsize = E / n_groups;
-        float gs = -INFINITY;
-        bool avail = lane < n_groups;
-        if (avail) {
-            gs = sl[lane * gsize];
-            for (int q = 1; q < gsize; ++q) {
-                const float c = sl[lane * gsize + q];
-                if (c > gs) gs = c;
-            }
-        }
-        uint32_t kept = 0;
-        for (int r = 0; r < topk_groups; ++r) {
-            float bv = gs;
-            int bi = avail ? lane : INT_MAX;
-            warp_argmax(bv, bi);
-            kept |= 1u << bi;
-            if (lane == bi) avail = false;
-        }
-#pragma unroll
-        for (int i = 0; i < VPL; ++i) {
-            const int e = lane + 32 * i;
-            if (e < E && !((kept >> (e / gsize)) & 1u)) elig &= ~(1u << i);
-        }
-    }
-
-    // 1. tau = k-th largest lane maximum.
-    float lmax = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < VPL; ++i)
-        if ((elig >> i) & 1u) lmax = fmaxf(lmax, v[i]);
-    const float tau = __shfl_sync(0xffffffffu, warp_sort_desc(lmax, lane), k - 1);
-
-    // 2. candidates (eligible logits >= tau), packed by a warp prefix sum.
-    int c = 0;
-#pragma unroll
-    for (int i = 0; i < VPL; ++i) c += (((elig >> i) & 1u) && v[i] >= tau) ? 1 : 0;
-    int incl = c;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, incl, d);
-        if (lane >= d) incl += o;
-    }
-    const int C = __shfl_sync(0xffffffffu, incl, 31);
-
-    float my_v = -INFINITY;
-    int my_e = INT_MAX;  // lane j < k ends with pick j
-    if (C <= 32) {
-        int pos = incl - c;
-#pragma unroll
-        for (int i = 0; i < VPL; ++i) {
-            if (((elig >> i) & 1u) && v[i] >= tau) {
-                s_cand[warp][pos] = make_int2(__float_as_int(v[i]), lane + 32 * i);
-                ++pos;
-            }
-        }
-        __syncwarp();
-        // 3. a candidate's rank is the number of candidates ordered before it
-        //    (unique: indices differ); the top k go straight to their place.
-        if (lane < C) {
-            const int2 me = s_cand[warp][lane];
-            const float mv = __int_as_float(me.x);
-            int rank = 0;
-            for (int j = 0; j < C; ++j) {
-                const int2 o = s_cand[warp][j];
-                const float ov = __int_as_float(o.x);
-                rank += (ov > mv || (ov == mv && o.y < me.y)) ? 1 : 0;
-            }
-            if (rank < k) s_pick[warp][rank] = me;
-        }
-        __syncwarp();
-        if (lane < k) {
-            const int2 pk = s_pick[warp][lane];
-            my_v = __int_as_float(pk.x);
-            my_e = pk.y;
-        }
-    } else {
-        // Massive ties: k rounds of arg-max.
-        uint32_t avail = elig;
-        for (int j = 0; j < k; ++j) {
-            float bv = -INFINITY;
-            int bi = INT_MAX;
-#pragma unroll
-            for (int i = 0; i < VPL; ++i) {
-                if (((avail >> i) & 1u) && (bi == INT_MAX || v[i] > bv)) {  // ascending e: strict > keeps the lower index
-                    bv = v[i];
-                    bi = lane + 32 * i;
-                }
-            }
-            warp_argmax(bv, bi);
-            if ((bi & 31) == lane) avail &= ~(1u << (bi >> 5));
-            if (lane == j) {
-                my_v = bv;
-                my_e = bi;
-            }
-        }
-    }
-
-    const float m = __shfl_sync(0xffffffffu, my_v, 0);
+    int e;
     float w;
-    if (renormalize) {
-        const float ex = lane < k ? expf(my_v - m) : 0.f;
-        w = ex / warp_sum(ex);
-    } else {
-        float part = 0.f;
-#pragma unroll
-        for (int i = 0; i < VPL; ++i)
-            if (lane + 32 * i < E) part += expf(v[i] - m);
-        w = expf(my_v - m) / warp_sum(part);
-    }
+    route_token<VPL>(logits + t * E, E, k, n_groups, topk_groups, renormalize, lane, s_dyn + warp * E,
+                     s_cand[warp], s_pick[warp], e, w);
     if (lane < k) {
-        topk_idx[t * k + lane] = my_e;
+        topk_idx[t * k + lane] = e;
         topk_w[t * k + lane] = w;
     }
 }
-
 template <int VPL>
 cudaError_t launch_vpl(const ep_config &c, const float *logits, int32_t *idx, float *w, cudaStream_t s) {
     const size_t smem = c.n_groups > 1 ? sizeof(float) * kRouteWarps * (size_t)c.E : 0;

@@ -94,6 +94,8 @@ int ep_version(void);
  * trap; a wait that runs out sets a flag here instead and the kernel returns.
  *   bit 0 (1): an ep_dispatch CTA gave up waiting for a bulk copy to land; its
  *              remaining rows were not written.
+ *   bit 1 (2): an ep_dispatch_fused CTA gave up waiting (grid barrier or bulk
+ *              copy); its slots or rows were not written.
  * (ep_layout reports its own bounded wait through *n_chunks = -1.) */
 ep_status ep_device_error(int32_t *flags);
 
@@ -111,6 +113,10 @@ ep_status ep_schedule_capacity(const ep_config *cfg, int32_t *capacity);
  * kernel when all its CTAs fit on the GPU at once, else three), for callers
  * that size CUDA graphs or count launches. */
 ep_status ep_step_kernel_count(const ep_config *cfg, int32_t *kernels);
+
+/* The same for one ep_dispatch_fused + ep_combine pass (2 when the fused
+ * kernel runs). */
+ep_status ep_fused_step_kernel_count(const ep_config *cfg, int32_t *kernels);
 
 /*
  * ep_route -- router softmax and top-k for every token.
@@ -199,6 +205,33 @@ ep_status ep_layout(const ep_config *cfg, const int32_t *topk_idx,
  */
 ep_status ep_dispatch(const ep_config *cfg, const ep_bf16 *x, const int32_t *slot, ep_bf16 *send,
                       int32_t *slot_meta, cudaStream_t stream);
+
+/*
+ * ep_dispatch_fused -- ep_route, ep_layout and ep_dispatch in one call, with
+ * identical outputs (every argument means what it means there).
+ *
+ * Follows the UBEP article's "Kernel Decomposition": instead of separate
+ * phases joined by global barriers, one cooperative kernel gives every CTA a
+ * tile of tokens to route, rank and dispatch; the CTAs exchange the per-expert
+ * counts through global memory at two bounded grid barriers (in the workspace)
+ * and each CTA's x rows are fetched with bulk copies while that metadata is
+ * being computed. Shapes the fused kernel does not cover (more than
+ * 2048 / k tokens per CTA, or not all CTAs resident at once) run the three
+ * separate steps instead, with the same results.
+ *
+ * workspace : >= ep_dispatch_fused_workspace_size bytes, 256-byte aligned.
+ * A CTA that gives up a bounded wait sets ep_device_error bit 1 (2) and
+ * *n_chunks = -1 (it cannot happen under the cooperative launch used).
+ */
+ep_status ep_dispatch_fused_workspace_size(const ep_config *cfg, size_t *bytes);
+
+ep_status ep_dispatch_fused(const ep_config *cfg, const float *logits, const ep_bf16 *x,
+                            int32_t *topk_idx, float *topk_w,
+                            int32_t *expert_count, int32_t *expert_offset,
+                            int32_t *rank_count, int32_t *rank_offset, int32_t *slot,
+                            ep_chunk *chunks, int32_t chunk_capacity, int32_t *n_chunks,
+                            int32_t *worker_begin, ep_bf16 *send, int32_t *slot_meta,
+                            void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * ep_combine -- gather the k expert-output rows of every token back to token

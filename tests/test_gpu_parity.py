@@ -353,3 +353,78 @@ def test_layout_many_ctas(ep, orc, T, E, R, k):
 def test_no_device_error_flags(ep):
     """No kernel ran out of a bounded wait during the tests above."""
     assert ep.ep_device_error() == 0
+
+
+# ---------------------------------------------------------------------------
+# ep_dispatch_fused: the same outputs as ep_route + ep_layout + ep_dispatch
+# ---------------------------------------------------------------------------
+
+FUSED = [
+    ep_synth.CONFIGS["tiny"],
+    ep_synth.CONFIGS["decode"],
+    ep_synth.CONFIGS["prefill"],
+    ep_synth.CONFIGS["mid"],
+    ep_synth.CONFIGS["prefill"].with_(name="prefill-T1000", T=1000),
+    ep_synth.CONFIGS["mid"].with_(name="mid-T300-plain", T=300, renormalize=0),
+    ep_synth.CONFIGS["tiny"].with_(name="tiny-2nodes", ranks_per_node=2, self_rank=3, num_workers=5),
+    ep_synth.Workload("k6-vector", T=777, H=1024, E=64, R=8, k=6, num_workers=20),
+    ep_synth.Workload("short-rows", T=500, H=64, E=32, R=4, k=4, num_workers=7),
+    ep_synth.Workload("E1024-k32", T=300, H=512, E=1024, R=32, k=32, n_groups=32, topk_groups=4, num_workers=152),
+    ep_synth.Workload("k12-groups", T=257, H=2048, E=96, R=6, k=12, n_groups=6, topk_groups=2, ranks_per_node=2,
+                      self_rank=5, num_workers=33),
+    ep_synth.Workload("fallback-T80000", T=80000, H=256, E=256, R=32, k=8, num_workers=152),
+] + [w for w in ep_synth.sweep_workloads() if w.T in (1, 8, 64, 512, 32768)]
+
+
+@pytest.mark.parametrize("w", FUSED, ids=lambda w: w.name)
+def test_dispatch_fused_matches_separate(ep, w):
+    logits = torch.from_numpy(ep_synth.gate_logits(w.seed, w.T, w.E, w.zipf_s)).cuda()
+    x = bf16_to_dev(ep_synth.hidden_bf16_bits(w.seed, w.T, w.H))
+    cfg = ep.EpConfig.from_workload(w)
+    a = ep.LayerBuffers.allocate(cfg)
+    f = ep.LayerBuffers.allocate(cfg)
+    for b_ in (a, f):
+        b_.logits.copy_(logits)
+        b_.x.copy_(x)
+    a.send.fill_(0)
+    f.send.view(torch.int16).fill_(0x7FC1)
+    f.slot_meta.fill_(-9)
+    a.route(); a.layout(); a.dispatch()
+    f.dispatch_fused()
+    torch.cuda.synchronize()
+    assert ep.ep_device_error() == 0
+    for name in ("topk_idx", "topk_w", "expert_count", "expert_offset", "rank_count", "rank_offset", "slot",
+                 "worker_begin", "send", "slot_meta", "n_chunks"):
+        ga, gf = getattr(a, name), getattr(f, name)
+        if name == "worker_begin":
+            W = w.num_workers
+            ga, gf = ga[:W + 1], gf[:W + 1]
+        assert torch.equal(ga.view(torch.int32) if ga.dtype == torch.float32 else ga,
+                           gf.view(torch.int32) if gf.dtype == torch.float32 else gf), f"{name} differs"
+    n = int(a.n_chunks.item())
+    assert torch.equal(a.chunks[:n], f.chunks[:n])
+
+
+def test_dispatch_fused_vs_oracle(ep, orc):
+    """The fused call against the oracle directly (prefill shape, T = 2000)."""
+    w = ep_synth.CONFIGS["prefill"].with_(T=2000)
+    logits, x = make_inputs(w)
+    cfg = ep.EpConfig.from_workload(w)
+    b = ep.LayerBuffers.allocate(cfg)
+    b.logits.copy_(torch.from_numpy(logits))
+    b.x.copy_(bf16_to_dev(x))
+    b.dispatch_fused()
+    synthetic_expert(b.send, b.expert_offset, w.E, out=b.y)
+    b.combine()
+    torch.cuda.synchronize()
+    r = run_oracle(orc, w, logits, x)
+    n = int(b.n_chunks.item())
+    g = dict(idx=b.topk_idx.cpu().numpy(), w=b.topk_w.cpu().numpy(),
+             expert_count=b.expert_count.cpu().numpy(), expert_offset=b.expert_offset.cpu().numpy(),
+             rank_count=b.rank_count.cpu().numpy(), rank_offset=b.rank_offset.cpu().numpy(),
+             slot=b.slot.cpu().numpy(), chunks=b.chunks[:n].cpu().numpy(), worker_begin=b.worker_begin.cpu().numpy())
+    assert_route(g, r, logits, w.renormalize)
+    assert_layout(g, r)
+    assert np.array_equal(bf16_from_dev(b.send), r["send"])
+    assert np.array_equal(b.slot_meta.cpu().numpy(), r["meta"])
+    assert bf16_ulp_distance(bf16_from_dev(b.out), r["out"]).max() <= 1
