@@ -47,7 +47,8 @@ KERNEL_SOURCES = {
     "route": ["route.cu", "route_token.cuh"],
     "layout": ["layout.cu", "block_common.cuh"],
     "dispatch": ["dispatch.cu"],
-    "dispatch_fused": ["fused.cu", "block_common.cuh", "route_token.cuh"],
+    # the call runs the fused kernel at small T, else route + layout + dispatch kernels
+    "dispatch_fused": ["fused.cu", "block_common.cuh", "route_token.cuh", "route.cu", "layout.cu", "dispatch.cu"],
     "combine": ["combine.cu"],
 }
 

@@ -27,7 +27,7 @@ EP_OK, EP_ERR_INVALID_ARG, EP_ERR_UNSUPPORTED, EP_ERR_CUDA, EP_ERR_CAPACITY = ra
 # Entry points declared in include/ep.h (checked by the ABI test).
 EXPORTS = ("ep_status_string", "ep_version", "ep_device_error", "ep_step_kernel_count", "ep_fused_step_kernel_count",
            "ep_layout_workspace_size", "ep_dispatch_fused_workspace_size", "ep_schedule_capacity",
-           "ep_dispatch_fused",
+           "ep_dispatch_fused", "ep_check_bounded_wait",
            "ep_route", "ep_layout", "ep_dispatch", "ep_combine", "ep_layout_static")
 # Size of the device array ep_layout_static uses instead of a workspace (include/ep.h).
 EP_LAYOUT_STATIC_SCRATCH_BYTES = 1 << 20
@@ -77,6 +77,7 @@ def _load() -> ctypes.CDLL:
     lib.ep_version.argtypes = []
     lib.ep_version.restype = ctypes.c_int
     lib.ep_device_error.argtypes = [P(ctypes.c_int32)]
+    lib.ep_check_bounded_wait.argtypes = [ctypes.c_int32, vp, vp]
     lib.ep_step_kernel_count.argtypes = [cfgp, P(ctypes.c_int32)]
     lib.ep_fused_step_kernel_count.argtypes = [cfgp, P(ctypes.c_int32)]
     lib.ep_layout_workspace_size.argtypes = [cfgp, P(ctypes.c_size_t)]
@@ -90,6 +91,7 @@ def _load() -> ctypes.CDLL:
                                       ctypes.c_size_t, vp]
     lib.ep_combine.argtypes = [cfgp, vp, vp, vp, vp, vp]
     for f in ("ep_dispatch_fused_workspace_size", "ep_dispatch_fused", "ep_fused_step_kernel_count",
+              "ep_check_bounded_wait",
               "ep_device_error", "ep_step_kernel_count", "ep_layout_workspace_size", "ep_schedule_capacity", "ep_route", "ep_layout",
               "ep_dispatch", "ep_combine", "ep_layout_static"):
         getattr(lib, f).restype = ctypes.c_int
@@ -144,6 +146,12 @@ def ep_device_error() -> int:
     v = ctypes.c_int32(0)
     _check(_lib.ep_device_error(ctypes.byref(v)), "ep_device_error")
     return int(v.value)
+
+
+def ep_check_bounded_wait(max_polls: int, gave_up, stream=None) -> None:
+    """Run the library's bounded-wait self-check; gave_up: int32 [1] CUDA tensor (ends at 2)."""
+    _check(_lib.ep_check_bounded_wait(int(max_polls), _ptr(gave_up, torch.int32, (1,), "gave_up"), _stream(stream)),
+           "ep_check_bounded_wait")
 
 
 def ep_step_kernel_count(cfg: EpConfig, fused: bool = False) -> int:

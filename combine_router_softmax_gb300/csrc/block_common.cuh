@@ -290,7 +290,7 @@ __device__ __forceinline__ void red_release_gpu_add(unsigned *p, unsigned v) {
 // CTA's global writes, arrives with a release add and polls with acquire
 // loads. Bounded: returns false (for every thread of the CTA) if the count did
 // not arrive in time.
-__device__ bool grid_barrier(unsigned *arrivals, unsigned expected) {
+__device__ bool grid_barrier(unsigned *arrivals, unsigned expected, unsigned max_polls = kBarrierSpinLimit) {
     __shared__ int s_ok;
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -299,7 +299,7 @@ __device__ bool grid_barrier(unsigned *arrivals, unsigned expected) {
         int ok = 1;
         unsigned spins = 0;
         while (ld_acquire_gpu(arrivals) < expected) {
-            if (++spins > kBarrierSpinLimit) {
+            if (++spins > max_polls) {
                 ok = 0;
                 break;
             }

@@ -97,7 +97,10 @@ cudaError_t launch_k(const ep_config &c, const ep_bf16 *x, const int32_t *slot, 
 
 // ---------------------------------------------------------------------------
 // Bulk-copy path (k % 4 == 0, rows of >= 1 KiB): one warp per CTA, several
-// CTAs per SM. Lane 0 streams token rows (and their k slots) into NS shared
+// CTAs per SM. Tokens go to CTAs in a fixed stride, or -- when the caller
+// provides a counter in device memory -- are grabbed one at a time from it,
+// so CTAs that happen to get more bandwidth take more rows (measured: with a
+// fixed stride the last CTA ends ~20 % after the median one). Lane 0 streams token rows (and their k slots) into NS shared
 // memory stages with TMA bulk loads completing on per-stage mbarriers; once a
 // stage lands, lanes j < k each issue one bulk store of the row to send row
 // slot[t, j] and write its slot_meta. The stage is refilled with the token NS
@@ -114,13 +117,16 @@ constexpr uint32_t kBulkMaxPolls = 1u << 22;  // ~0.2 s of polling before giving
 __global__ void __launch_bounds__(32)
 dispatch_bulk_kernel(const char *__restrict__ x, const int32_t *__restrict__ slot, char *__restrict__ send,
                      int32_t *__restrict__ meta, int32_t T, int32_t k, int32_t row_bytes, int32_t row_pad,
-                     int32_t stage_bytes, int32_t NS, int64_t rows, int32_t *__restrict__ err) {
+                     int32_t stage_bytes, int32_t NS, int64_t rows, int32_t *__restrict__ err,
+                     unsigned *__restrict__ ctr) {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + (size_t)NS * stage_bytes);
+    int64_t *s_tok = reinterpret_cast<int64_t *>(bar + kBulkMaxStages);  // token of each stage, -1 = none
     const int lane = threadIdx.x;
     const int64_t G = gridDim.x;
     const int64_t first = blockIdx.x;
-    const int64_t n = first < T ? (T - first + G - 1) / G : 0;  // this CTA's tokens: first + i G
+    const int64_t n = first < T ? (T - first + G - 1) / G : 0;  // static order: tokens first + i G
+    const bool dyn = ctr != nullptr;
 
     if (lane == 0) {
         for (int s = 0; s < NS; ++s) mbar_init(&bar[s], 1);
@@ -135,18 +141,30 @@ dispatch_bulk_kernel(const char *__restrict__ x, const int32_t *__restrict__ slo
         bulk_g2s(st + row_pad, slot + t * k, 4u * (uint32_t)k, &bar[s]);
     };
 
-    if (lane == 0)
-        for (int s = 0; s < NS && s < n; ++s) load(s, first + s * G);
+    // Tokens per round: static stride, or grabbed from the shared counter
+    // (NS at once for the first rounds, then one per refill, one refill ahead).
+    unsigned nxt = 0;
+    if (lane == 0) {
+        const int64_t c0 = dyn ? (int64_t)atomicAdd(ctr, (unsigned)NS) : 0;
+        for (int s = 0; s < NS; ++s) {
+            const int64_t t = dyn ? c0 + s : (s < n ? first + s * G : T);
+            s_tok[s] = t < T ? t : -1;
+            if (t < T) load(s, t);
+        }
+        if (dyn) nxt = atomicAdd(ctr, 1u);
+    }
+    __syncwarp();
 
     bool ok = true;
     int64_t i = 0;
-    for (; i < n; ++i) {
+    for (;; ++i) {
         const int s = (int)(i % NS);
+        const int64_t t = s_tok[s];
+        if (t < 0) break;
         if (!mbar_wait_bounded(&bar[s], (uint32_t)((i / NS) & 1), kBulkMaxPolls)) {
             ok = false;
             break;
         }
-        const int64_t t = first + i * G;
         const unsigned char *st = smem + (size_t)s * stage_bytes;
         if (lane < k) {
             const int sv = reinterpret_cast<const int32_t *>(st + row_pad)[lane];
@@ -156,19 +174,31 @@ dispatch_bulk_kernel(const char *__restrict__ x, const int32_t *__restrict__ slo
             }
             bulk_commit();
         }
-        // Refill the stage of token i - 1 once its stores have read it.
-        if (i >= 1 && i - 1 + NS < n) {
+        // Refill the stage of round i - 1 (with round i - 1 + NS) once its stores have read it.
+        if (i >= 1) {
             if (lane < k) bulk_wait_read<1>();
             __syncwarp();
-            if (lane == 0) load((int)((i - 1) % NS), first + (i - 1 + NS) * G);
+            if (lane == 0) {
+                const int sp = (int)((i - 1) % NS);
+                int64_t tn;
+                if (dyn) {
+                    tn = (int64_t)nxt < T ? (int64_t)nxt : -1;
+                    if (tn >= 0) nxt = atomicAdd(ctr, 1u);
+                } else {
+                    tn = (i - 1 + NS < n) ? first + (i - 1 + NS) * G : -1;
+                }
+                s_tok[sp] = tn;
+                if (tn >= 0) load(sp, tn);
+            }
+            __syncwarp();
         }
     }
     if (!ok) {
         // Record the failure, then let every load already issued land before
         // the CTA (and its shared memory) goes away.
         if (lane == 0) atomicOr(err, kErrDispatchWait);
-        for (int64_t j = i; j < n && j < i + NS; ++j)
-            mbar_wait_bounded(&bar[j % NS], (uint32_t)((j / NS) & 1), kBulkMaxPolls);
+        for (int64_t j = i; j < i + NS - 1; ++j)
+            if (s_tok[j % NS] >= 0) mbar_wait_bounded(&bar[j % NS], (uint32_t)((j / NS) & 1), kBulkMaxPolls);
     }
     if (lane < k) bulk_wait<0>();
 }
@@ -182,12 +212,12 @@ int bulk_stages(int32_t row_bytes) {
 }
 
 cudaError_t launch_bulk(const ep_config &c, const ep_bf16 *x, const int32_t *slot, ep_bf16 *send, int32_t *meta,
-                        cudaStream_t s) {
+                        cudaStream_t s, unsigned *ctr, bool ctr_zeroed) {
     const int32_t row_bytes = c.H * 2;
     const int32_t row_pad = (row_bytes + 127) & ~127;
     const int32_t stage_bytes = row_pad + 128;
     const int NS = bulk_stages(row_bytes);
-    const size_t smem = (size_t)NS * stage_bytes + kBulkMaxStages * sizeof(uint64_t);
+    const size_t smem = (size_t)NS * stage_bytes + kBulkMaxStages * (sizeof(uint64_t) + sizeof(int64_t));
     int dev = 0;
     cudaGetDevice(&dev);
     static bool attr_set[kMaxDevices_] = {false};
@@ -203,9 +233,13 @@ cudaError_t launch_bulk(const ep_config &c, const ep_bf16 *x, const int32_t *slo
     const int occ = max_blocks_per_sm(reinterpret_cast<const void *>(dispatch_bulk_kernel), 32, smem);
     int64_t grid = (int64_t)sm_count(dev) * occ;
     if (grid > c.T) grid = c.T;
+    if (ctr && !ctr_zeroed) {
+        e = cudaMemsetAsync(ctr, 0, sizeof(unsigned), s);
+        if (e != cudaSuccess) return e;
+    }
     dispatch_bulk_kernel<<<(unsigned)grid, 32, smem, s>>>(reinterpret_cast<const char *>(x), slot,
                                                           reinterpret_cast<char *>(send), meta, c.T, c.k, row_bytes,
-                                                          row_pad, stage_bytes, NS, (int64_t)c.T * c.k, err);
+                                                          row_pad, stage_bytes, NS, (int64_t)c.T * c.k, err, ctr);
     return cudaGetLastError();
 }
 
@@ -236,9 +270,9 @@ static bool use_bulk(const ep_config &c, const int32_t *slot) {
 }
 
 cudaError_t launch_dispatch(const ep_config &c, const ep_bf16 *x, const int32_t *slot, ep_bf16 *send,
-                            int32_t *meta, cudaStream_t s) {
+                            int32_t *meta, cudaStream_t s, unsigned *ctr, bool ctr_zeroed) {
     if (c.T == 0) return cudaSuccess;
-    if (use_bulk(c, slot)) return launch_bulk(c, x, slot, send, meta, s);
+    if (use_bulk(c, slot)) return launch_bulk(c, x, slot, send, meta, s, ctr, ctr_zeroed);
     switch (c.k) {
         case 1: return launch_k<1>(c, x, slot, send, meta, s);
         case 2: return launch_k<2>(c, x, slot, send, meta, s);

@@ -139,6 +139,11 @@ ep_status ep_device_error(int32_t *flags) {
     return EP_OK;
 }
 
+ep_status ep_check_bounded_wait(int32_t max_polls, int32_t *gave_up, cudaStream_t stream) {
+    if (max_polls <= 0 || !gave_up) return EP_ERR_INVALID_ARG;
+    return from_cuda(ep::launch_bounded_wait_check((uint32_t)max_polls, gave_up, stream));
+}
+
 ep_status ep_dispatch_fused_workspace_size(const ep_config *cfg, size_t *bytes) {
     ep_status st = check_config(cfg);
     if (st != EP_OK) return st;

@@ -45,18 +45,28 @@ int current_device_sm_count();
 // Resident CTAs per SM for a kernel (cached per kernel, device and launch shape).
 int max_blocks_per_sm(const void *fn, int threads, size_t smem);
 
-cudaError_t launch_route(const ep_config &c, const float *logits, int32_t *idx, float *w, cudaStream_t s);
+// za / zb: optional words (na / nb of them) the route kernel sets to zero for
+// kernels that follow it in the same call sequence.
+cudaError_t launch_route(const ep_config &c, const float *logits, int32_t *idx, float *w, cudaStream_t s,
+                         unsigned *za = nullptr, int na = 0, unsigned *zb = nullptr, int nb = 0);
 
+// sync_zeroed: the caller already zeroed the workspace's sync words (skip the memset).
 cudaError_t launch_layout(const ep_config &c, int32_t W, const int32_t *idx, int32_t *expert_count,
                           int32_t *expert_offset, int32_t *rank_count, int32_t *rank_offset, int32_t *slot,
                           ep_chunk *chunks, int32_t *n_chunks, int32_t *worker_begin, void *workspace,
-                          cudaStream_t s);
+                          cudaStream_t s, bool sync_zeroed = false);
+
+// Runs two CTAs into a grid barrier that expects three; *gave_up counts the
+// CTAs that stopped waiting after max_polls polls (2 when the bound works).
+cudaError_t launch_bounded_wait_check(uint32_t max_polls, int32_t *gave_up, cudaStream_t s);
 
 // Kernels launch_layout enqueues for c on the current device (1 fused, or 3).
 int layout_kernel_count(const ep_config &c);
 
+// ctr: optional device counter (4 bytes) for dynamic token assignment, zeroed
+// here unless ctr_zeroed.
 cudaError_t launch_dispatch(const ep_config &c, const ep_bf16 *x, const int32_t *slot, ep_bf16 *send,
-                            int32_t *meta, cudaStream_t s);
+                            int32_t *meta, cudaStream_t s, unsigned *ctr = nullptr, bool ctr_zeroed = false);
 
 cudaError_t launch_combine(const ep_config &c, const ep_bf16 *y, const int32_t *slot, const float *w,
                            ep_bf16 *out, cudaStream_t s);

@@ -3,8 +3,9 @@
 // movement in one kernel, with the SyncAll barriers between separate phases
 // replaced by cores that poll global memory for the metadata they need).
 //
-// Each CTA owns a contiguous tile of tokens and takes it through every step:
-//   0. lane 0 of warp 0 starts TMA bulk loads of the tile's first x rows into
+// Each CTA owns a contiguous tile of tokens (tiles differ by at most one
+// token, two CTAs per SM) and takes it through every step:
+//   0. one thread starts TMA bulk loads of the tile's first x rows into
 //      shared-memory stages (they land while the metadata is computed);
 //   A. route: one warp per token (route_token.cuh), picks kept in shared memory;
 //   B. rank: the tile's (token, expert) pairs are ranked per expert
@@ -37,7 +38,7 @@ static __device__ int32_t g_fused_error;
 
 struct FusedPlan {
     int nb = 0;       // CTAs (tiles)
-    int tb = 0;       // tokens per tile
+    int tb = 0;       // tokens in the largest tile
     int ns = 0;       // x-row stages per CTA (bulk path), 0 = vector copy
     int row_pad = 0;  // bytes per stage
     size_t smem = 0;
@@ -123,12 +124,13 @@ __global__ void __launch_bounds__(kFusedThreads) dispatch_fused_kernel(FusedArgs
     const int warp = threadIdx.x >> 5;
     const int b = blockIdx.x;
     const int E = a.E, k = a.k;
-    const int64_t t0 = (int64_t)b * a.tb;
-    const int ntok = (int)((int64_t)a.T - t0 < a.tb ? (int64_t)a.T - t0 : a.tb);  // >= 1
+    // tile b = tokens [floor(b T / nb), floor((b + 1) T / nb)): every CTA within one token of the others
+    const int64_t t0 = (int64_t)b * a.T / a.nb;
+    const int ntok = (int)((int64_t)(b + 1) * a.T / a.nb - t0);  // may be 0 when T < nb
     const int np = ntok * k;
     const int32_t row_bytes = a.H * 2;
 
-    // 0. start the tile's first x rows
+    // 0. start the tile's first x rows into shared memory
     if (a.ns > 0 && threadIdx.x == 0) {
         for (int s = 0; s < a.ns; ++s) mbar_init(&bar[s], 1);
         fence_mbar_init();
@@ -155,7 +157,7 @@ __global__ void __launch_bounds__(kFusedThreads) dispatch_fused_kernel(FusedArgs
     __syncthreads();
 
     // B. rank the tile's pairs; publish the tile's counts
-    const int ppw = (np + kFusedWarps - 1) / kFusedWarps;
+    const int ppw = np > 0 ? (np + kFusedWarps - 1) / kFusedWarps : 1;
     cta_rank_pairs(tile_e, np, ppw, E, cnt, tile_r, a.counts + (int64_t)b * E, 1);
 
     // C.
@@ -309,8 +311,9 @@ FusedKernel pick_kernel(int32_t E) {
     return dispatch_fused_kernel<32>;
 }
 
-// Choose the tiling: as many CTAs as fit on the GPU at once (up to 1024),
-// every CTA holding the same number of tokens. false if the fused kernel
+// Choose the tiling: as many CTAs as fit on the GPU at once (two per SM when
+// shared memory allows, at most 1024 and at most T), tiles within one token
+// of each other in size. false if the fused kernel
 // cannot run this shape (then the caller runs the three separate steps).
 bool plan_fused(const ep_config &c, FusedPlan *p) {
     if (c.T <= 0) return false;
@@ -335,9 +338,12 @@ bool plan_fused(const ep_config &c, FusedPlan *p) {
     for (int per_sm = 2; per_sm >= 1; --per_sm) {
         int nb = sms * per_sm;
         if (nb > kMaxFusedCTAs) nb = kMaxFusedCTAs;
-        int tb = (int)((c.T + nb - 1) / nb);
-        nb = (int)((c.T + tb - 1) / tb);
-        if ((int64_t)tb * c.k > kMaxTilePairs) return false;
+        if (nb > c.T) nb = c.T;
+        const int tb = (int)((c.T + nb - 1) / nb);  // largest tile
+        // Routing needs a warp per token to keep its latency hidden; when a
+        // warp would route more than one token the separate route kernel
+        // (64 warps per SM) is faster, so the fused kernel is not used.
+        if (tb > kFusedWarps || (int64_t)tb * c.k > kMaxTilePairs) return false;
         const int row_pad = (int)align128((size_t)row_bytes);
         const SmemLayout base = smem_layout(0, row_pad, tb, c.k, c.E, c.R, c.n_groups > 1);
         int ns = 0;
@@ -380,11 +386,14 @@ cudaError_t fused_error_word(int32_t **addr) {
     return cudaSuccess;
 }
 
+// The separate-step path keeps its dispatch counter right after the layout's workspace.
+size_t fused_counter_offset(const ep_config &c) { return (layout_workspace(c).bytes + 255) & ~(size_t)255; }
+
 size_t fused_workspace_bytes(const ep_config &c) {
     const int64_t nb = c.T < kMaxFusedCTAs ? c.T : kMaxFusedCTAs;
     const size_t tables = 2 * sizeof(int32_t) * (size_t)nb * (size_t)c.E;
     const size_t fused = ((tables + sizeof(int32_t) * (size_t)c.E + 255) & ~(size_t)255) + 256;
-    const size_t sep = layout_workspace(c).bytes;
+    const size_t sep = fused_counter_offset(c) + 256;
     return c.T == 0 ? 0 : (fused > sep ? fused : sep);
 }
 
@@ -400,12 +409,17 @@ cudaError_t launch_dispatch_fused(const ep_config &c, int32_t W, const float *lo
                                   void *workspace, cudaStream_t s) {
     FusedPlan p;
     if (!plan_fused(c, &p)) {
-        cudaError_t e = launch_route(c, logits, topk_idx, topk_w, s);
+        // Three kernels; the route kernel zeroes the layout's barrier words and
+        // the dispatch counter, so no memset sits between the kernels.
+        char *ws = static_cast<char *>(workspace);
+        unsigned *lsync = reinterpret_cast<unsigned *>(ws + layout_workspace(c).sync_off);
+        unsigned *ctr = reinterpret_cast<unsigned *>(ws + fused_counter_offset(c));
+        cudaError_t e = launch_route(c, logits, topk_idx, topk_w, s, lsync, 2, ctr, 1);
         if (e != cudaSuccess) return e;
         e = launch_layout(c, W, topk_idx, expert_count, expert_offset, rank_count, rank_offset, slot, chunks,
-                          n_chunks, worker_begin, workspace, s);
+                          n_chunks, worker_begin, workspace, s, true);
         if (e != cudaSuccess) return e;
-        return launch_dispatch(c, x, slot, send, meta, s);
+        return launch_dispatch(c, x, slot, send, meta, s, ctr, true);
     }
     FusedArgs a;
     a.logits = logits;

@@ -70,7 +70,7 @@ LayoutWorkspace layout_workspace(const ep_config &c) {
     const int64_t nbf = nw > 0 ? (c.T + 32 * nw - 1) / (32 * nw) : nb;
     w.sync_off = align256(sizeof(int32_t) * (size_t)nbf * (size_t)c.E);
     const size_t fallback = align256(sizeof(int32_t) * (size_t)nb * (size_t)c.E);
-    const size_t fused = nbf > 1 ? w.sync_off + 256 : w.sync_off;
+    const size_t fused = w.sync_off + 256;
     w.bytes = c.T == 0 ? 0 : (fallback > fused ? fallback : fused);
     return w;
 }
@@ -357,7 +357,7 @@ int layout_kernel_count(const ep_config &c) {
 cudaError_t launch_layout(const ep_config &c, int32_t W, const int32_t *idx, int32_t *expert_count,
                           int32_t *expert_offset, int32_t *rank_count, int32_t *rank_offset, int32_t *slot,
                           ep_chunk *chunks, int32_t *n_chunks, int32_t *worker_begin, void *workspace,
-                          cudaStream_t s) {
+                          cudaStream_t s, bool sync_zeroed) {
     int nw = 0;
     int64_t nb = 0;
     if (!layout_fused_fits(c, &nw, &nb))
@@ -367,7 +367,7 @@ cudaError_t launch_layout(const ep_config &c, int32_t W, const int32_t *idx, int
     const LayoutWorkspace ws = layout_workspace(c);
     int32_t *counts = static_cast<int32_t *>(workspace);
     unsigned *sync = reinterpret_cast<unsigned *>(static_cast<char *>(workspace) + ws.sync_off);
-    if (nb > 1) {
+    if (nb > 1 && !sync_zeroed) {
         cudaError_t e = cudaMemsetAsync(sync, 0, 2 * sizeof(unsigned), s);
         if (e != cudaSuccess) return e;
     }
@@ -378,6 +378,33 @@ cudaError_t launch_layout(const ep_config &c, int32_t W, const int32_t *idx, int
                     (void *)&chunks, (void *)&n_chunks, (void *)&worker_begin, &W, &rpn, &self};
     return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(layout_fused_kernel), dim3((unsigned)nb),
                                        dim3((unsigned)(nw * 32)), args, smem, s);
+}
+
+}  // namespace ep
+
+// ---------------------------------------------------------------------------
+// Self-check of the bounded grid barrier: two CTAs wait for three arrivals,
+// which never come; both must give up after max_polls polls and report it.
+// ---------------------------------------------------------------------------
+namespace ep {
+namespace {
+
+static __device__ unsigned g_check_arrivals;
+
+__global__ void bounded_wait_check_kernel(unsigned *arrivals, unsigned max_polls, int32_t *gave_up) {
+    if (!grid_barrier(arrivals, gridDim.x + 1, max_polls) && threadIdx.x == 0) atomicAdd(gave_up, 1);
+}
+
+}  // namespace
+
+cudaError_t launch_bounded_wait_check(uint32_t max_polls, int32_t *gave_up, cudaStream_t s) {
+    void *p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_check_arrivals);
+    if (e != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(p, 0, sizeof(unsigned), s)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(gave_up, 0, sizeof(int32_t), s)) != cudaSuccess) return e;
+    bounded_wait_check_kernel<<<2, 32, 0, s>>>(static_cast<unsigned *>(p), max_polls, gave_up);
+    return cudaGetLastError();
 }
 
 }  // namespace ep

@@ -18,8 +18,14 @@ template <int VPL>
 __global__ void __launch_bounds__(kRouteWarps * 32)
 route_kernel(const float *__restrict__ logits, int32_t T, int32_t E, int32_t k, int32_t n_groups,
              int32_t topk_groups, int32_t renormalize, int32_t *__restrict__ topk_idx,
-             float *__restrict__ topk_w) {
+             float *__restrict__ topk_w, unsigned *__restrict__ zero_a, int n_zero_a, unsigned *__restrict__ zero_b,
+             int n_zero_b) {
     extern __shared__ float s_dyn[];  // [kRouteWarps][E] logits, group-limited routing only
+    // Reset the counters that later kernels of the same call sequence start from.
+    if (blockIdx.x == 0) {
+        if ((int)threadIdx.x < n_zero_a) zero_a[threadIdx.x] = 0u;
+        if ((int)threadIdx.x < n_zero_b) zero_b[threadIdx.x] = 0u;
+    }
     __shared__ int2 s_cand[kRouteWarps][32];  // candidate (logit bits, expert)
     __shared__ int2 s_pick[kRouteWarps][32];  // the k picks in order
     const int lane = threadIdx.x & 31;
@@ -36,25 +42,27 @@ route_kernel(const float *__restrict__ logits, int32_t T, int32_t E, int32_t k, 
     }
 }
 template <int VPL>
-cudaError_t launch_vpl(const ep_config &c, const float *logits, int32_t *idx, float *w, cudaStream_t s) {
+cudaError_t launch_vpl(const ep_config &c, const float *logits, int32_t *idx, float *w, cudaStream_t s,
+                       unsigned *za, int na, unsigned *zb, int nb) {
     const size_t smem = c.n_groups > 1 ? sizeof(float) * kRouteWarps * (size_t)c.E : 0;
     const unsigned grid = (unsigned)((c.T + kRouteWarps - 1) / kRouteWarps);
     route_kernel<VPL><<<grid, kRouteWarps * 32, smem, s>>>(logits, c.T, c.E, c.k, c.n_groups, c.topk_groups,
-                                                         c.renormalize, idx, w);
+                                                         c.renormalize, idx, w, za, na, zb, nb);
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_route(const ep_config &c, const float *logits, int32_t *idx, float *w, cudaStream_t s) {
+cudaError_t launch_route(const ep_config &c, const float *logits, int32_t *idx, float *w, cudaStream_t s,
+                         unsigned *za, int na, unsigned *zb, int nb) {
     if (c.T == 0) return cudaSuccess;
     const int vpl = (c.E + 31) / 32;
-    if (vpl <= 1) return launch_vpl<1>(c, logits, idx, w, s);
-    if (vpl <= 2) return launch_vpl<2>(c, logits, idx, w, s);
-    if (vpl <= 4) return launch_vpl<4>(c, logits, idx, w, s);
-    if (vpl <= 8) return launch_vpl<8>(c, logits, idx, w, s);
-    if (vpl <= 16) return launch_vpl<16>(c, logits, idx, w, s);
-    return launch_vpl<32>(c, logits, idx, w, s);
+    if (vpl <= 1) return launch_vpl<1>(c, logits, idx, w, s, za, na, zb, nb);
+    if (vpl <= 2) return launch_vpl<2>(c, logits, idx, w, s, za, na, zb, nb);
+    if (vpl <= 4) return launch_vpl<4>(c, logits, idx, w, s, za, na, zb, nb);
+    if (vpl <= 8) return launch_vpl<8>(c, logits, idx, w, s, za, na, zb, nb);
+    if (vpl <= 16) return launch_vpl<16>(c, logits, idx, w, s, za, na, zb, nb);
+    return launch_vpl<32>(c, logits, idx, w, s, za, na, zb, nb);
 }
 
 }  // namespace ep

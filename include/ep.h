@@ -99,6 +99,14 @@ int ep_version(void);
  * (ep_layout reports its own bounded wait through *n_chunks = -1.) */
 ep_status ep_device_error(int32_t *flags);
 
+/* Diagnostics: checks that the library's device-side waits are bounded.
+ * Launches two CTAs into a grid barrier (the kind ep_layout and
+ * ep_dispatch_fused use) that expects three arrivals, so the wait can never
+ * complete; each CTA must give up after max_polls polls (> 0) and count
+ * itself in *gave_up (device int32, zeroed first). Expected result: 2. The
+ * kernel returns normally; nothing faults or hangs. */
+ep_status ep_check_bounded_wait(int32_t max_polls, int32_t *gave_up, cudaStream_t stream);
+
 /* Bytes of device scratch that ep_layout needs for `cfg` (it depends on T and
  * E only). The workspace needs no initialisation and may be reused across
  * calls on the same stream. */
@@ -215,9 +223,10 @@ ep_status ep_dispatch(const ep_config *cfg, const ep_bf16 *x, const int32_t *slo
  * tile of tokens to route, rank and dispatch; the CTAs exchange the per-expert
  * counts through global memory at two bounded grid barriers (in the workspace)
  * and each CTA's x rows are fetched with bulk copies while that metadata is
- * being computed. Shapes the fused kernel does not cover (more than
- * 2048 / k tokens per CTA, or not all CTAs resident at once) run the three
- * separate steps instead, with the same results.
+ * being computed. It pays off at small T (decode batches), where the phases
+ * are latency-bound; when a CTA would have to route more than 8 tokens (T
+ * above 8 tokens per resident CTA, about 2400 on a GB300) the call runs the
+ * three separate steps instead, with the same results.
  *
  * workspace : >= ep_dispatch_fused_workspace_size bytes, 256-byte aligned.
  * A CTA that gives up a bounded wait sets ep_device_error bit 1 (2) and

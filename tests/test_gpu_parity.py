@@ -355,6 +355,18 @@ def test_no_device_error_flags(ep):
     assert ep.ep_device_error() == 0
 
 
+@pytest.mark.parametrize("polls", [1, 1000, 100000])
+def test_bounded_wait_gives_up(ep, polls):
+    """A grid barrier that can never complete returns (both CTAs give up and say so)."""
+    gave_up = torch.full((1,), -1, dtype=torch.int32, device="cuda")
+    ep.ep_check_bounded_wait(polls, gave_up)
+    torch.cuda.synchronize()
+    assert int(gave_up.item()) == 2
+    # the context is still usable afterwards
+    z = torch.ones(4, device="cuda") * 2
+    assert float(z.sum()) == 8.0
+
+
 # ---------------------------------------------------------------------------
 # ep_dispatch_fused: the same outputs as ep_route + ep_layout + ep_dispatch
 # ---------------------------------------------------------------------------
