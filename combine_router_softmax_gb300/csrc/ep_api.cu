@@ -197,7 +197,7 @@ ep_status ep_fused_step_kernel_count(const ep_config *cfg, int32_t *kernels) {
     }
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return EP_ERR_CUDA;
-    *kernels = ep::fused_would_run(*cfg) ? 2 : 3 + ep::layout_kernel_count(*cfg);
+    *kernels = ep::fused_call_kernels(*cfg) + 1;  // + combine
     return EP_OK;
 }
 

@@ -173,7 +173,8 @@ cudaError_t fused_error_word(int32_t **addr);
 
 // Fused route + layout + dispatch (fused.cu).
 size_t fused_workspace_bytes(const ep_config &c);
-bool fused_would_run(const ep_config &c);
+// Kernels one ep_dispatch_fused call enqueues on the current device.
+int fused_call_kernels(const ep_config &c);
 cudaError_t launch_dispatch_fused(const ep_config &c, int32_t W, const float *logits, const ep_bf16 *x,
                                   int32_t *topk_idx, float *topk_w, int32_t *expert_count, int32_t *expert_offset,
                                   int32_t *rank_count, int32_t *rank_offset, int32_t *slot, ep_chunk *chunks,

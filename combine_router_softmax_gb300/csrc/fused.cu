@@ -11,8 +11,9 @@
 //   B. rank: the tile's (token, expert) pairs are ranked per expert
 //      (cta_rank_pairs) and the tile's per-expert counts published;
 //   C. bounded grid barrier;
-//   D. column scan: CTA q scans expert q's counts over all tiles (one value per
-//      thread) and publishes each tile's base inside the expert and the total;
+//   D. column scan: CTA q reads the counts of experts q, q + nb, ... over all
+//      tiles in one batch and publishes each tile's base inside each of those
+//      experts and their totals;
 //   E. bounded grid barrier;
 //   F. each CTA reads its tile's bases and the totals, scans the totals into
 //      expert offsets and writes its slots; CTA 0 writes counts and offsets and
@@ -49,9 +50,9 @@ size_t align128(size_t b) { return (b + 127) & ~(size_t)127; }
 // Shared-memory carve-up, in this order (each piece 128-byte aligned):
 // stages, mbarriers, tile_e, tile_r, tile_s, cnt [8][E], group logits [8][E],
 // cand [8][32] int2, pick [8][32] int2, s_tot [E], s_eoff [E+2], s_base [E],
-// s_roff [R+1], s_P [R+2].
+// s_roff [R+1], s_P [R+2], s_col [E + 1024] (the column scan's counts).
 struct SmemLayout {
-    size_t stages, bars, tile_e, tile_r, tile_s, cnt, glog, cand, pick, tot, eoff, base, roff, P, bytes;
+    size_t stages, bars, tile_e, tile_r, tile_s, cnt, glog, cand, pick, tot, eoff, base, roff, P, col, bytes;
 };
 
 __host__ __device__ inline SmemLayout smem_layout(int ns, int row_pad, int tb, int32_t k, int32_t E, int32_t R,
@@ -77,6 +78,7 @@ __host__ __device__ inline SmemLayout smem_layout(int ns, int row_pad, int tb, i
     L.base = take(sizeof(int32_t) * (size_t)E);
     L.roff = take(sizeof(int32_t) * ((size_t)R + 1));
     L.P = take(sizeof(int32_t) * ((size_t)R + 2));
+    L.col = take(sizeof(int32_t) * ((size_t)E + kMaxFusedCTAs));  // my experts x tiles <= E + nb
     L.bytes = o;
     return L;
 }
@@ -119,6 +121,7 @@ __global__ void __launch_bounds__(kFusedThreads) dispatch_fused_kernel(FusedArgs
     int32_t *s_base = reinterpret_cast<int32_t *>(smem + L.base);
     int32_t *s_roff = reinterpret_cast<int32_t *>(smem + L.roff);
     int32_t *s_P = reinterpret_cast<int32_t *>(smem + L.P);
+    int32_t *s_col = reinterpret_cast<int32_t *>(smem + L.col);
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -163,21 +166,45 @@ __global__ void __launch_bounds__(kFusedThreads) dispatch_fused_kernel(FusedArgs
     // C.
     bool ok = grid_barrier(&a.sync[0], (unsigned)a.nb);
 
-    // D. column scan: expert e's counts over all tiles, one tile per thread
+    // D. column scan: CTA b owns experts b, b + nb, ...; all their counts over
+    // every tile are read in one batch, then scanned over the tiles.
     if (ok) {
-        for (int e = b; e < E; e += a.nb) {
-            const int per = (a.nb + blockDim.x - 1) / blockDim.x;
-            const int q0 = threadIdx.x * per;
-            int local = 0;
-            for (int q = q0; q < q0 + per && q < a.nb; ++q) local += __ldcg(a.counts + (int64_t)q * E + e);
-            int total;
-            int run = cta_exclusive_scan32(local, s_warp32, &total);
-            for (int q = q0; q < q0 + per && q < a.nb; ++q) {
-                const int c = __ldcg(a.counts + (int64_t)q * E + e);
-                a.bases[(int64_t)q * E + e] = run;
-                run += c;
+        const int nb = a.nb;
+        const int my_n = b < E ? (E - b + nb - 1) / nb : 0;
+        const int nv = my_n * nb;
+        for (int v = threadIdx.x; v < nv; v += blockDim.x) {
+            const int q = v % nb;
+            const int e = b + (v / nb) * nb;
+            s_col[v] = __ldcg(a.counts + (int64_t)q * E + e);
+        }
+        __syncthreads();
+        if (nb <= 64) {
+            // many experts, few tiles: one thread walks each expert's tiles
+            for (int j = threadIdx.x; j < my_n; j += blockDim.x) {
+                const int e = b + j * nb;
+                int run = 0;
+                for (int q = 0; q < nb; ++q) {
+                    a.bases[(int64_t)q * E + e] = run;
+                    run += s_col[j * nb + q];
+                }
+                a.totals[e] = run;
             }
-            if (threadIdx.x == 0) a.totals[e] = total;
+        } else {
+            // few experts, many tiles: the CTA scans one expert's tiles at a time
+            for (int j = 0; j < my_n; ++j) {
+                const int e = b + j * nb;
+                const int per = (nb + blockDim.x - 1) / blockDim.x;
+                const int q0 = threadIdx.x * per;
+                int local = 0;
+                for (int q = q0; q < q0 + per && q < nb; ++q) local += s_col[j * nb + q];
+                int total;
+                int run = cta_exclusive_scan32(local, s_warp32, &total);
+                for (int q = q0; q < q0 + per && q < nb; ++q) {
+                    a.bases[(int64_t)q * E + e] = run;
+                    run += s_col[j * nb + q];
+                }
+                if (threadIdx.x == 0) a.totals[e] = total;
+            }
         }
         // E.
         ok = grid_barrier(&a.sync[1], (unsigned)a.nb);
@@ -342,7 +369,10 @@ bool plan_fused(const ep_config &c, FusedPlan *p) {
         const int tb = (int)((c.T + nb - 1) / nb);  // largest tile
         // Routing needs a warp per token to keep its latency hidden; when a
         // warp would route more than one token the separate route kernel
-        // (64 warps per SM) is faster, so the fused kernel is not used.
+        // (64 warps per SM) is faster, so the fused kernel is not used. (A
+        // variant that stopped after the slots, with up to 1024 small CTAs
+        // and the dispatch kernel after it, measured 6 us slower than the
+        // separate kernels at T = 4096 and equal at T = 16384.)
         if (tb > kFusedWarps || (int64_t)tb * c.k > kMaxTilePairs) return false;
         const int row_pad = (int)align128((size_t)row_bytes);
         const SmemLayout base = smem_layout(0, row_pad, tb, c.k, c.E, c.R, c.n_groups > 1);
@@ -386,20 +416,29 @@ cudaError_t fused_error_word(int32_t **addr) {
     return cudaSuccess;
 }
 
-// The separate-step path keeps its dispatch counter right after the layout's workspace.
-size_t fused_counter_offset(const ep_config &c) { return (layout_workspace(c).bytes + 255) & ~(size_t)255; }
+size_t fused_tables_bytes(const ep_config &c);
 
-size_t fused_workspace_bytes(const ep_config &c) {
-    const int64_t nb = c.T < kMaxFusedCTAs ? c.T : kMaxFusedCTAs;
-    const size_t tables = 2 * sizeof(int32_t) * (size_t)nb * (size_t)c.E;
-    const size_t fused = ((tables + sizeof(int32_t) * (size_t)c.E + 255) & ~(size_t)255) + 256;
-    const size_t sep = fused_counter_offset(c) + 256;
-    return c.T == 0 ? 0 : (fused > sep ? fused : sep);
+// The dispatch counter sits after both the layout's workspace and the fused tables.
+size_t fused_counter_offset(const ep_config &c) {
+    const size_t lw = layout_workspace(c).bytes, ft = fused_tables_bytes(c);
+    return ((lw > ft ? lw : ft) + 255) & ~(size_t)255;
 }
 
-bool fused_would_run(const ep_config &c) {
+// Fused tables (counts, bases, totals, barrier words), then the dispatch counter.
+size_t fused_tables_bytes(const ep_config &c) {
+    const int64_t nb = c.T < kMaxFusedCTAs ? c.T : kMaxFusedCTAs;
+    const size_t tables = 2 * sizeof(int32_t) * (size_t)nb * (size_t)c.E;
+    return ((tables + sizeof(int32_t) * (size_t)c.E + 255) & ~(size_t)255) + 256;
+}
+
+size_t fused_workspace_bytes(const ep_config &c) {
+    return c.T == 0 ? 0 : fused_counter_offset(c) + 256;
+}
+
+int fused_call_kernels(const ep_config &c) {
     FusedPlan p;
-    return plan_fused(c, &p);
+    if (!plan_fused(c, &p)) return 2 + layout_kernel_count(c);  // route, layout, dispatch
+    return 1;
 }
 
 cudaError_t launch_dispatch_fused(const ep_config &c, int32_t W, const float *logits, const ep_bf16 *x,

@@ -123,7 +123,7 @@ ep_status ep_schedule_capacity(const ep_config *cfg, int32_t *capacity);
 ep_status ep_step_kernel_count(const ep_config *cfg, int32_t *kernels);
 
 /* The same for one ep_dispatch_fused + ep_combine pass (2 when the fused
- * kernel runs). */
+ * kernel runs, else 4 or 6). */
 ep_status ep_fused_step_kernel_count(const ep_config *cfg, int32_t *kernels);
 
 /*
@@ -226,7 +226,9 @@ ep_status ep_dispatch(const ep_config *cfg, const ep_bf16 *x, const int32_t *slo
  * being computed. It pays off at small T (decode batches), where the phases
  * are latency-bound; when a CTA would have to route more than 8 tokens (T
  * above 8 tokens per resident CTA, about 2400 on a GB300) the call runs the
- * three separate steps instead, with the same results.
+ * three separate steps instead (the route kernel zeroing the layout's and
+ * dispatch's counters, the dispatch taking tokens dynamically), with the same
+ * results.
  *
  * workspace : >= ep_dispatch_fused_workspace_size bytes, 256-byte aligned.
  * A CTA that gives up a bounded wait sets ep_device_error bit 1 (2) and
