@@ -333,4 +333,24 @@ def pin_bf16_rounding(o):
         assert np.float32(o.bf16_to_f32(b)).view(np.uint32) == np.uint32(b) << np.uint32(16)
 
 
+def pin_expert_scale(o):
+    """The harness expert: row s belongs to the expert e with offset[e] <= s <
+    offset[e + 1] (found here by brute force over all experts, empty ones
+    included) and y = bf16(float(send) * fp32((e + 1) / E)), rounded by torch."""
+    g = _rng(14)
+    E, H = 9, 24
+    counts = g.integers(0, 6, size=E)
+    counts[[0, 4, 8]] = 0  # empty experts at both ends and inside
+    offset = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    rows = int(offset[-1])
+    send = ep_synth.random_rows_bf16_bits(6, rows, H)
+    y = o.expert(send, offset, E)
+    owner = np.array([[e for e in range(E) if offset[e] <= s < offset[e + 1]][0] for s in range(rows)])
+    scale = (np.float32(1) + owner.astype(np.float32)) / np.float32(E)
+    prod = (ep_synth.bf16_bits_to_f32(send) * scale[:, None].astype(np.float32)).astype(np.float32)
+    ref = torch.from_numpy(prod).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(y, ref)
+    assert np.array_equal(o.expert(send, offset, E, identity=True), send)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
