@@ -65,6 +65,9 @@ def parse_args(argv=None):
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
     p.add_argument("--no-graph", action="store_true", help="time the per-step launches only (no CUDA graph)")
+    p.add_argument("--data-as-flag", action="store_true",
+                   help="also time dispatch + expert as two kernels (bulk-synchronous) and as one "
+                        "sentinel-polling kernel (Data-as-Flag)")
     p.add_argument("--separate", action="store_true",
                    help="step = ep_route, ep_layout, ep_dispatch, ep_combine (default: ep_dispatch_fused, ep_combine)")
     return p.parse_args(argv)
@@ -331,6 +334,77 @@ def call_bytes(w, name: str) -> int:
     return kb[name]
 
 
+def data_as_flag_leg(ep, buf, w, device, flush_l2, K: int) -> dict:
+    """dispatch -> expert handed over two ways, each captured in a CUDA graph and
+    replayed K times with L2 flushed in between:
+      bsp: ep_dispatch, then ep_expert_scale (kernel boundary as the barrier);
+      sp:  ep_dispatch_expert_sp (rows handed over by sentinel polling; each
+           call re-arms send for the next)."""
+    import numpy as np
+    import torch
+
+    row = w.H * 2
+    if w.k % 4 != 0 or not 1024 <= row <= 48 * 1024:
+        return {"unsupported": "needs k % 4 == 0 and rows of 1..48 KiB"}
+    scale = torch.from_numpy((np.arange(w.E, dtype=np.float32) + np.float32(1)) / np.float32(w.E)).to(device)
+    cap = torch.cuda.Stream(device)
+    cap.wait_stream(torch.cuda.current_stream(device))
+
+    def bsp():
+        buf.dispatch(cap)
+        buf.expert_scale(scale, cap)
+
+    def sp():
+        buf.dispatch_expert_sp(scale, cap)
+
+    graphs = {}
+    with torch.cuda.stream(cap):
+        buf.layout(cap)
+        bsp()
+        bsp()
+        y_bsp = buf.y.clone()
+        buf.sentinel_arm(cap)
+        sp()
+        sp()
+    cap.synchronize()
+    same = bool(torch.equal(y_bsp, buf.y))
+    for name, fn in (("bsp", bsp), ("sp", sp)):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            fn()
+        graphs[name] = g
+    torch.cuda.synchronize()
+    out = {}
+    stream = torch.cuda.current_stream(device)
+    for name in ("bsp", "sp"):
+        if name == "sp":
+            buf.sentinel_arm(stream)
+        for _ in range(3):
+            flush_l2()
+            graphs[name].replay()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for a, b_ in ev:
+            flush_l2()
+            a.record(stream)
+            graphs[name].replay()
+            b_.record(stream)
+        torch.cuda.synchronize()
+        out[name + "_us"] = round(1e3 * sum(a.elapsed_time(b_) for a, b_ in ev) / K, 2)
+    err = ep.ep_device_error()
+    rows_b = w.T * w.k * row
+    kb = w.algorithmic_bytes()
+    out.update({
+        "bsp_kernels": 2, "sp_kernels": 1,
+        "bsp_bytes": kb["dispatch"] + 2 * rows_b,
+        "sp_bytes": kb["dispatch"] + 3 * rows_b,
+        "same_output": same and err == 0,
+        "device_error": err,
+        "steps": K,
+    })
+    out["sp_speedup"] = round(out["bsp_us"] / out["sp_us"], 3)
+    return out
+
+
 def run_gb300(args):
     import numpy as np
     import torch
@@ -518,6 +592,8 @@ def run_gb300(args):
         "clocks": clk,
         "wall_s": round(wall, 3),
     }
+    if args.data_as_flag:
+        line["data_as_flag"] = data_as_flag_leg(ep, buf, w, device, flush_l2, min(K, 500))
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w0, args.cpu_seconds)
     if rank == 0:

@@ -27,7 +27,8 @@ EP_OK, EP_ERR_INVALID_ARG, EP_ERR_UNSUPPORTED, EP_ERR_CUDA, EP_ERR_CAPACITY = ra
 # Entry points declared in include/ep.h (checked by the ABI test).
 EXPORTS = ("ep_status_string", "ep_version", "ep_device_error", "ep_step_kernel_count", "ep_fused_step_kernel_count",
            "ep_layout_workspace_size", "ep_dispatch_fused_workspace_size", "ep_schedule_capacity",
-           "ep_dispatch_fused", "ep_check_bounded_wait",
+           "ep_dispatch_fused", "ep_check_bounded_wait", "ep_sentinel_arm", "ep_expert_scale",
+           "ep_dispatch_expert_sp",
            "ep_route", "ep_layout", "ep_dispatch", "ep_combine", "ep_layout_static")
 # Size of the device array ep_layout_static uses instead of a workspace (include/ep.h).
 EP_LAYOUT_STATIC_SCRATCH_BYTES = 1 << 20
@@ -78,6 +79,9 @@ def _load() -> ctypes.CDLL:
     lib.ep_version.restype = ctypes.c_int
     lib.ep_device_error.argtypes = [P(ctypes.c_int32)]
     lib.ep_check_bounded_wait.argtypes = [ctypes.c_int32, vp, vp]
+    lib.ep_sentinel_arm.argtypes = [cfgp, vp, vp]
+    lib.ep_expert_scale.argtypes = [cfgp, vp, vp, vp, vp, vp]
+    lib.ep_dispatch_expert_sp.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.ep_step_kernel_count.argtypes = [cfgp, P(ctypes.c_int32)]
     lib.ep_fused_step_kernel_count.argtypes = [cfgp, P(ctypes.c_int32)]
     lib.ep_layout_workspace_size.argtypes = [cfgp, P(ctypes.c_size_t)]
@@ -91,7 +95,7 @@ def _load() -> ctypes.CDLL:
                                       ctypes.c_size_t, vp]
     lib.ep_combine.argtypes = [cfgp, vp, vp, vp, vp, vp]
     for f in ("ep_dispatch_fused_workspace_size", "ep_dispatch_fused", "ep_fused_step_kernel_count",
-              "ep_check_bounded_wait",
+              "ep_check_bounded_wait", "ep_sentinel_arm", "ep_expert_scale", "ep_dispatch_expert_sp",
               "ep_device_error", "ep_step_kernel_count", "ep_layout_workspace_size", "ep_schedule_capacity", "ep_route", "ep_layout",
               "ep_dispatch", "ep_combine", "ep_layout_static"):
         getattr(lib, f).restype = ctypes.c_int
@@ -269,6 +273,41 @@ def ep_dispatch_fused(cfg: EpConfig, logits, x, topk_idx, topk_w, expert_count, 
                                   _stream(stream)), "ep_dispatch_fused")
 
 
+EP_SENTINEL_BF16 = 0xFFFF
+
+
+def ep_sentinel_arm(cfg: EpConfig, send, stream=None) -> None:
+    """Fill send [T*k, H] with the bf16 sentinel 0xFFFF."""
+    _check(_lib.ep_sentinel_arm(ctypes.byref(cfg), _ptr(send, torch.bfloat16, (cfg.T * cfg.k, cfg.H), "send"),
+                                _stream(stream)), "ep_sentinel_arm")
+
+
+def ep_expert_scale(cfg: EpConfig, send, expert_offset, expert_scale, y, stream=None) -> None:
+    """y[s] = bf16(send[s] * expert_scale[e(s)])."""
+    T, H, E, k = cfg.T, cfg.H, cfg.E, cfg.k
+    _check(_lib.ep_expert_scale(ctypes.byref(cfg), _ptr(send, torch.bfloat16, (T * k, H), "send"),
+                                _ptr(expert_offset, torch.int32, (E + 1,), "expert_offset"),
+                                _ptr(expert_scale, torch.float32, (E,), "expert_scale"),
+                                _ptr(y, torch.bfloat16, (T * k, H), "y"), _stream(stream)), "ep_expert_scale")
+
+
+def ep_dispatch_expert_sp(cfg: EpConfig, x, slot, expert_offset, expert_scale, chunks, n_chunks, worker_begin,
+                          send, slot_meta, y, stream=None) -> None:
+    """Dispatch + scale expert in one kernel, rows handed over by sentinel polling."""
+    T, H, E, k = cfg.T, cfg.H, cfg.E, cfg.k
+    _check(_lib.ep_dispatch_expert_sp(ctypes.byref(cfg), _ptr(x, torch.bfloat16, (T, H), "x"),
+                                      _ptr(slot, torch.int32, (T, k), "slot"),
+                                      _ptr(expert_offset, torch.int32, (E + 1,), "expert_offset"),
+                                      _ptr(expert_scale, torch.float32, (E,), "expert_scale"),
+                                      _ptr(chunks, torch.int32, None, "chunks"),
+                                      _ptr(n_chunks, torch.int32, (1,), "n_chunks"),
+                                      _ptr(worker_begin, torch.int32, None, "worker_begin"),
+                                      _ptr(send, torch.bfloat16, (T * k, H), "send"),
+                                      _ptr(slot_meta, torch.int32, (T * k,), "slot_meta"),
+                                      _ptr(y, torch.bfloat16, (T * k, H), "y"), _stream(stream)),
+           "ep_dispatch_expert_sp")
+
+
 def ep_dispatch(cfg: EpConfig, x, slot, send, slot_meta, stream=None) -> None:
     """x bf16 [T, H] -> send bf16 [T*k, H], slot_meta int32 [T*k]."""
     T, H, k = cfg.T, cfg.H, cfg.k
@@ -357,6 +396,17 @@ class LayerBuffers:
         ep_dispatch_fused(self.cfg, self.logits, self.x, self.topk_idx, self.topk_w, self.expert_count,
                           self.expert_offset, self.rank_count, self.rank_offset, self.slot, self.chunks,
                           self.n_chunks, self.worker_begin, self.send, self.slot_meta, self.workspace, stream)
+
+    def sentinel_arm(self, stream=None):
+        ep_sentinel_arm(self.cfg, self.send, stream)
+
+    def expert_scale(self, expert_scale, stream=None):
+        ep_expert_scale(self.cfg, self.send, self.expert_offset, expert_scale, self.y, stream)
+
+    def dispatch_expert_sp(self, expert_scale, stream=None):
+        """dispatch + per-expert scale in one kernel; send must be armed."""
+        ep_dispatch_expert_sp(self.cfg, self.x, self.slot, self.expert_offset, expert_scale, self.chunks,
+                              self.n_chunks, self.worker_begin, self.send, self.slot_meta, self.y, stream)
 
     def bind(self, stream=None) -> "BoundLayer":
         """Pre-marshalled C calls on this layer's buffers (same entry points,

@@ -125,9 +125,10 @@ int ep_version(void) { return 100; }
 
 ep_status ep_device_error(int32_t *flags) {
     if (!flags) return EP_ERR_INVALID_ARG;
-    int32_t *words[2] = {nullptr, nullptr};
+    int32_t *words[3] = {nullptr, nullptr, nullptr};
     if (ep::dispatch_error_word(&words[0]) != cudaSuccess) return EP_ERR_CUDA;
     if (ep::fused_error_word(&words[1]) != cudaSuccess) return EP_ERR_CUDA;
+    if (ep::sp_error_word(&words[2]) != cudaSuccess) return EP_ERR_CUDA;
     int32_t all = 0;
     for (int32_t *word : words) {
         int32_t v = 0;
@@ -262,6 +263,49 @@ ep_status ep_dispatch_fused(const ep_config *cfg, const float *logits, const ep_
     return from_cuda(ep::launch_dispatch_fused(*cfg, W, logits, x, topk_idx, topk_w, expert_count, expert_offset,
                                                rank_count, rank_offset, slot, chunks, n_chunks, worker_begin, send,
                                                slot_meta, workspace, stream));
+}
+
+ep_status ep_sentinel_arm(const ep_config *cfg, ep_bf16 *send, cudaStream_t stream) {
+    ep_status st = check_config(cfg);
+    if (st != EP_OK) return st;
+    if ((st = check_rows(cfg)) != EP_OK) return st;
+    if (cfg->T == 0) return EP_OK;
+    if (!send || !aligned16(send)) return EP_ERR_INVALID_ARG;
+    return from_cuda(ep::launch_sentinel_arm(*cfg, send, stream));
+}
+
+ep_status ep_expert_scale(const ep_config *cfg, const ep_bf16 *send, const int32_t *expert_offset,
+                          const float *expert_scale, ep_bf16 *y, cudaStream_t stream) {
+    ep_status st = check_config(cfg);
+    if (st != EP_OK) return st;
+    if ((st = check_rows(cfg)) != EP_OK) return st;
+    if (cfg->T == 0) return EP_OK;
+    if (!send || !expert_offset || !expert_scale || !y) return EP_ERR_INVALID_ARG;
+    if (!aligned16(send) || !aligned16(y)) return EP_ERR_INVALID_ARG;
+    return from_cuda(ep::launch_expert_scale(*cfg, send, expert_offset, expert_scale, y, stream));
+}
+
+ep_status ep_dispatch_expert_sp(const ep_config *cfg, const ep_bf16 *x, const int32_t *slot,
+                                const int32_t *expert_offset, const float *expert_scale, const ep_chunk *chunks,
+                                const int32_t *n_chunks, const int32_t *worker_begin, ep_bf16 *send,
+                                int32_t *slot_meta, ep_bf16 *y, cudaStream_t stream) {
+    ep_status st = check_config(cfg);
+    if (st != EP_OK) return st;
+    if ((st = check_rows(cfg)) != EP_OK) return st;
+    if ((st = check_schedule(cfg)) != EP_OK) return st;
+    if (cfg->T == 0) return EP_OK;
+    if (!x || !slot || !expert_offset || !expert_scale || !chunks || !n_chunks || !worker_begin || !send ||
+        !slot_meta || !y)
+        return EP_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(send) || !aligned16(y) || (reinterpret_cast<uintptr_t>(slot) & 15u))
+        return EP_ERR_INVALID_ARG;
+    if (cfg->k % 4 != 0 || cfg->H * 2 < 1024 || cfg->H * 2 > 48 * 1024) return EP_ERR_UNSUPPORTED;
+    int32_t W = 0;
+    if ((st = resolve_workers(cfg, &W)) != EP_OK) return st;
+    const cudaError_t e = ep::launch_dispatch_expert_sp(*cfg, W, x, slot, expert_offset, expert_scale, chunks,
+                                                        n_chunks, worker_begin, send, slot_meta, y, stream);
+    if (e == cudaErrorNotSupported) return EP_ERR_UNSUPPORTED;
+    return from_cuda(e);
 }
 
 ep_status ep_dispatch(const ep_config *cfg, const ep_bf16 *x, const int32_t *slot, ep_bf16 *send,

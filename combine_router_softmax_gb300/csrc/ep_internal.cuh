@@ -168,8 +168,19 @@ __device__ __forceinline__ void bulk_wait() {
 // can set them; ep_device_error() collects and clears them.
 constexpr int32_t kErrDispatchWait = 1;  // a dispatch CTA gave up waiting for a bulk copy
 constexpr int32_t kErrFusedWait = 2;     // a fused-dispatch CTA gave up waiting (barrier or bulk copy)
+constexpr int32_t kErrSpWait = 4;        // a sentinel-polling CTA gave up waiting
 cudaError_t dispatch_error_word(int32_t **addr);
 cudaError_t fused_error_word(int32_t **addr);
+cudaError_t sp_error_word(int32_t **addr);
+
+// Data-as-Flag by sentinel polling (sp.cu).
+cudaError_t launch_sentinel_arm(const ep_config &c, ep_bf16 *send, cudaStream_t s);
+cudaError_t launch_expert_scale(const ep_config &c, const ep_bf16 *send, const int32_t *expert_offset,
+                                const float *scale, ep_bf16 *y, cudaStream_t s);
+cudaError_t launch_dispatch_expert_sp(const ep_config &c, int32_t W, const ep_bf16 *x, const int32_t *slot,
+                                      const int32_t *expert_offset, const float *scale, const ep_chunk *chunks,
+                                      const int32_t *n_chunks, const int32_t *worker_begin, ep_bf16 *send,
+                                      int32_t *meta, ep_bf16 *y, cudaStream_t s);
 
 // Fused route + layout + dispatch (fused.cu).
 size_t fused_workspace_bytes(const ep_config &c);

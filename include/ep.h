@@ -96,6 +96,8 @@ int ep_version(void);
  *              remaining rows were not written.
  *   bit 1 (2): an ep_dispatch_fused CTA gave up waiting (grid barrier or bulk
  *              copy); its slots or rows were not written.
+ *   bit 2 (4): an ep_dispatch_expert_sp CTA gave up waiting (a row that never
+ *              arrived, or a bulk copy); its rows were not all written.
  * (ep_layout reports its own bounded wait through *n_chunks = -1.) */
 ep_status ep_device_error(int32_t *flags);
 
@@ -243,6 +245,46 @@ ep_status ep_dispatch_fused(const ep_config *cfg, const float *logits, const ep_
                             ep_chunk *chunks, int32_t chunk_capacity, int32_t *n_chunks,
                             int32_t *worker_begin, ep_bf16 *send, int32_t *slot_meta,
                             void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Data-as-Flag by Sentinel Polling (the UBEP article, "Data-as-Flag" / SP).
+ *
+ * The receiver fills its buffer with a sentinel no payload can take, the
+ * sender writes raw payload only, and the receiver polls until the sentinel
+ * is gone: no flag and no control message. Sentinel: the bf16 bit pattern
+ * 0xFFFF (a NaN); finite activations never take it, so x must hold no such
+ * value (a row that kept it would be waited on until the bound runs out).
+ *
+ * ep_sentinel_arm  : fills send [T k, H] with the sentinel (done once; every
+ *                    ep_dispatch_expert_sp call leaves it armed again).
+ * ep_expert_scale  : the bulk-synchronous counterpart of the consumer below:
+ *                    y[s, :] = bf16_rne(float(send[s, :]) * expert_scale[e]),
+ *                    e the expert that owns row s (expert_offset, E + 1).
+ * ep_dispatch_expert_sp : one cooperative kernel. Producer CTAs dispatch x as
+ *                    ep_dispatch does (send, slot_meta); one consumer CTA per
+ *                    chunk-schedule worker (chunks / n_chunks / worker_begin,
+ *                    all device pointers, from ep_layout on the same cfg)
+ *                    polls the rows of its chunks,
+ *                    writes y as ep_expert_scale would and writes the
+ *                    sentinel back into send. On return y equals
+ *                    ep_dispatch + ep_expert_scale, slot_meta equals
+ *                    ep_dispatch's, and send is armed again (its payload is
+ *                    consumed). Needs k % 4 == 0 and rows of 1..48 KiB
+ *                    (EP_ERR_UNSUPPORTED otherwise); slot 16-byte aligned. A
+ *                    CTA that gives up a bounded wait sets ep_device_error
+ *                    bit 2 (4).
+ */
+#define EP_SENTINEL_BF16 0xFFFFu
+
+ep_status ep_sentinel_arm(const ep_config *cfg, ep_bf16 *send, cudaStream_t stream);
+
+ep_status ep_expert_scale(const ep_config *cfg, const ep_bf16 *send, const int32_t *expert_offset,
+                          const float *expert_scale, ep_bf16 *y, cudaStream_t stream);
+
+ep_status ep_dispatch_expert_sp(const ep_config *cfg, const ep_bf16 *x, const int32_t *slot,
+                                const int32_t *expert_offset, const float *expert_scale,
+                                const ep_chunk *chunks, const int32_t *n_chunks, const int32_t *worker_begin,
+                                ep_bf16 *send, int32_t *slot_meta, ep_bf16 *y, cudaStream_t stream);
 
 /*
  * ep_combine -- gather the k expert-output rows of every token back to token
