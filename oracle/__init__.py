@@ -72,7 +72,7 @@ class Oracle:
         L = self.lib
         L.orc_route.argtypes = [i64, i32, i32, i32, i32, i32, P(ctypes.c_float), P(i32), P(ctypes.c_double)]
         L.orc_layout.argtypes = [i64, i32, i32, i32, P(i32), P(i32), P(i32), P(i32), P(i32), P(i32)]
-        L.orc_schedule.argtypes = [i32, i32, i32, i32, P(i32), P(i32), i32, P(i32), P(i32)]
+        L.orc_schedule.argtypes = [i32, i32, i32, i32, i32, P(i32), P(i32), i32, P(i32), P(i32)]
         L.orc_dispatch.argtypes = [i64, i32, i32, P(ctypes.c_uint16), P(i32), P(ctypes.c_uint16), P(i32)]
         L.orc_combine.argtypes = [i64, i32, i32, P(ctypes.c_uint16), P(i32), P(ctypes.c_float), P(ctypes.c_uint16)]
         L.orc_expert_scale.argtypes = [i64, i32, i32, P(i32), i32, P(ctypes.c_uint16), P(ctypes.c_uint16)]
@@ -117,15 +117,17 @@ class Oracle:
         return out
 
     # -- schedule (orc_schedule) -------------------------------------------
-    def schedule(self, rank_offset: np.ndarray, ranks_per_node: int, self_rank: int, W: int):
+    def schedule(self, rank_offset: np.ndarray, ranks_per_node: int, self_rank: int, W: int,
+                 ranks_per_pod: int = 0):
         """(chunks int32 [n, 5], worker_begin int32 [W + 1])."""
         rank_offset = np.ascontiguousarray(rank_offset, dtype=np.int32)
         R = rank_offset.shape[0] - 1
-        cap = 2 * W + R
+        cap = 3 * W + R
         chunks = np.zeros((cap, 5), np.int32)
         wb = np.zeros(W + 1, np.int32)
         n = ctypes.c_int32(0)
-        self._check(self.lib.orc_schedule(R, ranks_per_node, self_rank, W, _ptr(rank_offset, ctypes.c_int32),
+        self._check(self.lib.orc_schedule(R, ranks_per_node, ranks_per_pod, self_rank, W,
+                                          _ptr(rank_offset, ctypes.c_int32),
                                           _ptr(chunks, ctypes.c_int32), cap, ctypes.byref(n),
                                           _ptr(wb, ctypes.c_int32)), "orc_schedule")
         return chunks[:n.value].copy(), wb
@@ -175,11 +177,11 @@ class Oracle:
 
     # -- the whole path on one workload ------------------------------------
     def run_path(self, logits, x_bits, *, E, R, k, n_groups=1, topk_groups=1, renormalize=1,
-                 ranks_per_node=16, self_rank=0, W=152, identity_expert=False) -> dict:
+                 ranks_per_node=16, self_rank=0, W=152, identity_expert=False, ranks_per_pod=0) -> dict:
         """route -> layout -> schedule -> dispatch -> expert -> combine, all on the CPU."""
         idx, w = self.route(logits, k, n_groups, topk_groups, renormalize)
         lay = self.layout(idx, E, R)
-        chunks, wb = self.schedule(lay["rank_offset"], ranks_per_node, self_rank, W)
+        chunks, wb = self.schedule(lay["rank_offset"], ranks_per_node, self_rank, W, ranks_per_pod)
         send, meta = self.dispatch(x_bits, lay["slot"])
         y = self.expert(send, lay["expert_offset"], E, identity=identity_expert)
         w32 = w.astype(np.float32)

@@ -233,12 +233,19 @@ int orc_layout(int64_t T, int32_t E, int32_t R, int32_t k, const int32_t *idx,
 /*
  * "Hierarchical Token-Level Scheduling" / "Latency Homogenization" (UBEP
  * article): tokens are classed by network hop count and every worker gets a
- * balanced mixture of the latency classes. The pages give the goal, not the
+ * balanced mixture of the latency classes; the same section says the scheme
+ * extends to fabrics with more switch tiers. The pages give the goal, not the
  * heuristic; the plainest closed form is used:
  *
  *   hop_class(r) = 0 if r / ranks_per_node == self_rank / ranks_per_node
- *                  (same node, self included), else 1 (another node: the
- *                  two-hop access of "Topology-Agnostic Scheduling").
+ *                  (same node, self included);
+ *                  2 if ranks_per_pod > 0 and
+ *                  r / ranks_per_pod != self_rank / ranks_per_pod (another
+ *                  pod: one more switch tier);
+ *                  1 otherwise (another node: the two-hop access of
+ *                  "Topology-Agnostic Scheduling").
+ *                  ranks_per_pod = 0 means no pod tier (classes 0 and 1 only);
+ *                  else it is a multiple of ranks_per_node.
  *   S_c          = the rank segments [rank_offset[r], rank_offset[r+1]) of
  *                  class c concatenated in ascending r; N_c rows in all.
  *   worker w     takes positions [floor(N_c w / W), floor(N_c (w+1) / W)) of
@@ -247,32 +254,39 @@ int orc_layout(int64_t T, int32_t E, int32_t R, int32_t k, const int32_t *idx,
  *
  * A share cut at rank boundaries gives chunks {worker, hop_class, dst_rank,
  * row_begin, row_count}; empty chunks are omitted. Table order: worker
- * ascending, then class descending (two-hop traffic first), then rank
+ * ascending, then class descending (the farthest traffic first), then rank
  * ascending. worker_begin[w] is the index of worker w's first chunk and
  * worker_begin[W] the number of chunks. chunks holds 5 int32 per record.
  */
-int orc_schedule(int32_t R, int32_t ranks_per_node, int32_t self_rank, int32_t W,
+static int orc_hop_class(int32_t r, int32_t ranks_per_node, int32_t ranks_per_pod, int32_t self_rank)
+{
+    if (r / ranks_per_node == self_rank / ranks_per_node) return 0;
+    if (ranks_per_pod > 0 && r / ranks_per_pod != self_rank / ranks_per_pod) return 2;
+    return 1;
+}
+
+int orc_schedule(int32_t R, int32_t ranks_per_node, int32_t ranks_per_pod, int32_t self_rank, int32_t W,
                  const int32_t *rank_offset, int32_t *chunks, int32_t capacity,
                  int32_t *n_chunks, int32_t *worker_begin)
 {
     if (R <= 0 || ranks_per_node <= 0 || self_rank < 0 || self_rank >= R || W <= 0 || capacity < 0)
         return ORC_EINVAL;
-    const int32_t self_node = self_rank / ranks_per_node;
-    int64_t N[2] = {0, 0};
-    for (int32_t r = 0; r < R; ++r) {
-        int c = (r / ranks_per_node == self_node) ? 0 : 1;
-        N[c] += (int64_t)rank_offset[r + 1] - rank_offset[r];
-    }
+    if (ranks_per_pod < 0 || (ranks_per_pod > 0 && ranks_per_pod % ranks_per_node != 0))
+        return ORC_EINVAL;
+    int64_t N[3] = {0, 0, 0};
+    for (int32_t r = 0; r < R; ++r)
+        N[orc_hop_class(r, ranks_per_node, ranks_per_pod, self_rank)] +=
+            (int64_t)rank_offset[r + 1] - rank_offset[r];
 
     int32_t n = 0;
     for (int32_t w = 0; w < W; ++w) {
         worker_begin[w] = n;
-        for (int c = 1; c >= 0; --c) {
+        for (int c = 2; c >= 0; --c) {
             int64_t lo = N[c] * w / W;
             int64_t hi = N[c] * (w + 1) / W;
             int64_t pos = 0; /* start of the current rank's segment inside S_c */
             for (int32_t r = 0; r < R; ++r) {
-                if (((r / ranks_per_node == self_node) ? 0 : 1) != c) continue;
+                if (orc_hop_class(r, ranks_per_node, ranks_per_pod, self_rank) != c) continue;
                 int64_t seg_lo = pos;
                 int64_t seg_hi = pos + ((int64_t)rank_offset[r + 1] - rank_offset[r]);
                 pos = seg_hi;

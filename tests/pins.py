@@ -216,28 +216,38 @@ def pin_layout_golden(o):
 def pin_schedule_golden(o):
     d = json.loads((GOLDEN / "schedule_small.json").read_text())
     for c in d["cases"]:
-        ch, wb = o.schedule(np.array(c["rank_offset"], np.int32), c["ranks_per_node"], c["self_rank"], c["W"])
+        ch, wb = o.schedule(np.array(c["rank_offset"], np.int32), c["ranks_per_node"], c["self_rank"], c["W"],
+                            c.get("ranks_per_pod", 0))
         assert ch.tolist() == c["chunks"], c["name"]
         assert wb.tolist() == c["worker_begin"], c["name"]
 
 
-def check_schedule_invariants(chunks, wb, rank_offset, rpn, self_rank, W):
+def hop_class(r, rpn, self_rank, rpp=0):
+    """0: the sending rank's node; 2: another pod (when pods are given); 1: another node."""
+    if r // rpn == self_rank // rpn:
+        return 0
+    if rpp > 0 and r // rpp != self_rank // rpp:
+        return 2
+    return 1
+
+
+def check_schedule_invariants(chunks, wb, rank_offset, rpn, self_rank, W, rpp=0):
     """Tiling, balance and order of a chunk table (also used on GPU output)."""
     R = len(rank_offset) - 1
     total = int(rank_offset[-1])
-    assert len(chunks) <= 2 * W + R
+    n_classes = 3 if rpp > 0 else 2
+    assert len(chunks) <= n_classes * W + R
     assert wb[0] == 0 and wb[-1] == len(chunks) and (np.diff(wb) >= 0).all()
     cover = np.zeros(total, np.int32)
-    share = np.zeros((W, 2), np.int64)
-    node = self_rank // rpn
+    share = np.zeros((W, 3), np.int64)
     for i, (w, c, r, b, n) in enumerate(chunks):
         assert wb[w] <= i < wb[w + 1]
-        assert n > 0 and c == (0 if r // rpn == node else 1)
+        assert n > 0 and c == hop_class(r, rpn, self_rank, rpp)
         assert rank_offset[r] <= b and b + n <= rank_offset[r + 1]
         cover[b:b + n] += 1
         share[w, c] += n
     assert (cover == 1).all(), "rows not covered exactly once"
-    for c in (0, 1):
+    for c in range(3):
         assert share[:, c].max() - share[:, c].min() <= 1, "class shares unbalanced"
     for w in range(W):
         rows = [tuple(chunks[i]) for i in range(wb[w], wb[w + 1])]
@@ -247,12 +257,25 @@ def check_schedule_invariants(chunks, wb, rank_offset, rpn, self_rank, W):
 
 def pin_schedule_invariants(o):
     g = _rng(9)
-    for R, rpn, self_rank, W in ((64, 16, 0, 152), (32, 16, 17, 7), (16, 16, 3, 40), (8, 1, 5, 3), (5, 2, 4, 11)):
+    for R, rpn, self_rank, W, rpp in ((64, 16, 0, 152, 0), (32, 16, 17, 7, 0), (16, 16, 3, 40, 0), (8, 1, 5, 3, 0),
+                                      (5, 2, 4, 11, 0), (64, 4, 37, 19, 16), (64, 1, 0, 152, 8), (30, 2, 29, 7, 6),
+                                      (12, 3, 5, 1, 6)):
         counts = g.integers(0, 30, size=R)
         counts[g.integers(0, R)] = 0
         ro = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
-        ch, wb = o.schedule(ro, rpn, self_rank, W)
-        check_schedule_invariants(ch, wb, ro, rpn, self_rank, W)
+        ch, wb = o.schedule(ro, rpn, self_rank, W, rpp)
+        check_schedule_invariants(ch, wb, ro, rpn, self_rank, W, rpp)
+
+
+def pin_schedule_one_pod_is_two_tiers(o):
+    """A pod that holds every rank adds no tier: the table equals the two-tier one."""
+    g = _rng(15)
+    for R, rpn, self_rank, W in ((16, 4, 6, 9), (64, 16, 40, 152)):
+        ro = np.concatenate([[0], np.cumsum(g.integers(0, 40, size=R))]).astype(np.int32)
+        two = o.schedule(ro, rpn, self_rank, W)
+        for rpp in (R, 2 * R):
+            three = o.schedule(ro, rpn, self_rank, W, rpp)
+            assert np.array_equal(two[0], three[0]) and np.array_equal(two[1], three[1])
 
 
 # ---------------------------------------------------------------------------

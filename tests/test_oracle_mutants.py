@@ -36,13 +36,18 @@ MUTANTS = [
      "    for (int64_t t = 0; t < T; ++t)\n        for (int32_t j = 0; j < k; ++j) {\n            int32_t e = idx[t * k + j];\n            slot[t * k + j] = cursor[e];",
      "    for (int64_t t = T - 1; t >= 0; --t)\n        for (int32_t j = 0; j < k; ++j) {\n            int32_t e = idx[t * k + j];\n            slot[t * k + j] = cursor[e];"),
     ("near traffic scheduled first",
-     "for (int c = 1; c >= 0; --c) {", "for (int c = 0; c <= 1; ++c) {"),
+     "for (int c = 2; c >= 0; --c) {", "for (int c = 0; c <= 2; ++c) {"),
     ("chunk row_begin missing the rank base",
      "rec[3] = (int32_t)(rank_offset[r] + (a - seg_lo));", "rec[3] = (int32_t)(a - seg_lo);"),
     ("worker share rounded up",
      "int64_t hi = N[c] * (w + 1) / W;", "int64_t hi = (N[c] * (w + 1) + W - 1) / W;"),
     ("hop class from the rank, not the node",
-     "int c = (r / ranks_per_node == self_node) ? 0 : 1;", "int c = (r == self_rank) ? 0 : 1;"),
+     "if (r / ranks_per_node == self_rank / ranks_per_node) return 0;", "if (r == self_rank) return 0;"),
+    ("pod tier tested with the node size",
+     "r / ranks_per_pod != self_rank / ranks_per_pod) return 2;",
+     "r / ranks_per_node != self_rank / ranks_per_pod) return 2;"),
+    ("pod tier folded into the node tier",
+     "self_rank / ranks_per_pod) return 2;", "self_rank / ranks_per_pod) return 1;"),
     ("meta transposed",
      "meta[s] = (int32_t)(t * k + j);", "meta[s] = (int32_t)(j * T + t);"),
     ("combine weight operand transposed",
