@@ -44,18 +44,23 @@ class EpConfig(ctypes.Structure):
     """``ep_config`` of include/ep.h."""
     _fields_ = [(n, ctypes.c_int32) for n in (
         "T", "H", "E", "R", "k", "n_groups", "topk_groups", "renormalize",
-        "ranks_per_node", "self_rank", "num_workers")]
+        "ranks_per_node", "self_rank", "num_workers", "ranks_per_pod")]
 
     @classmethod
     def make(cls, *, T, H, E, R, k, n_groups=1, topk_groups=1, renormalize=1, ranks_per_node=16,
-             self_rank=0, num_workers=0) -> "EpConfig":
-        return cls(T, H, E, R, k, n_groups, topk_groups, renormalize, ranks_per_node, self_rank, num_workers)
+             self_rank=0, num_workers=0, ranks_per_pod=0) -> "EpConfig":
+        return cls(T, H, E, R, k, n_groups, topk_groups, renormalize, ranks_per_node, self_rank, num_workers,
+                   ranks_per_pod)
+
+    @property
+    def hop_classes(self) -> int:
+        return 3 if self.ranks_per_pod > 0 else 2
 
     @classmethod
     def from_workload(cls, w, **over) -> "EpConfig":
         kw = dict(T=w.T, H=w.H, E=w.E, R=w.R, k=w.k, n_groups=w.n_groups, topk_groups=w.topk_groups,
                   renormalize=w.renormalize, ranks_per_node=w.ranks_per_node, self_rank=w.self_rank,
-                  num_workers=w.num_workers)
+                  num_workers=w.num_workers, ranks_per_pod=w.ranks_per_pod)
         kw.update(over)
         return cls.make(**kw)
 
@@ -194,7 +199,7 @@ def ep_layout(cfg: EpConfig, topk_idx, expert_count, expert_offset, rank_count, 
     T, E, R, k = cfg.T, cfg.E, cfg.R, cfg.k
     if chunks.dim() != 2 or chunks.shape[1] != 5:
         raise ValueError("chunks: expected int32 [capacity, 5]")
-    W = (ep_schedule_capacity(cfg) - R) // 2
+    W = (ep_schedule_capacity(cfg) - R) // cfg.hop_classes
     if worker_begin.dim() != 1 or worker_begin.numel() < W + 1:
         raise ValueError(f"worker_begin: expected int32 [>= {W + 1}]")
     if workspace is not None and workspace.dtype != torch.uint8:
@@ -221,7 +226,7 @@ def ep_layout_static(cfg: EpConfig, topk_idx, expert_count, expert_offset, rank_
     T, E, R, k = cfg.T, cfg.E, cfg.R, cfg.k
     if chunks.dim() != 2 or chunks.shape[1] != 5:
         raise ValueError("chunks: expected int32 [capacity, 5]")
-    W = (ep_schedule_capacity(cfg) - R) // 2
+    W = (ep_schedule_capacity(cfg) - R) // cfg.hop_classes
     if worker_begin.dim() != 1 or worker_begin.numel() < W + 1:
         raise ValueError(f"worker_begin: expected int32 [>= {W + 1}]")
     _check(_lib.ep_layout_static(ctypes.byref(cfg), _ptr(topk_idx, torch.int32, (T, k), "topk_idx"),
@@ -250,7 +255,7 @@ def ep_dispatch_fused(cfg: EpConfig, logits, x, topk_idx, topk_w, expert_count, 
     T, H, E, R, k = cfg.T, cfg.H, cfg.E, cfg.R, cfg.k
     if chunks.dim() != 2 or chunks.shape[1] != 5:
         raise ValueError("chunks: expected int32 [capacity, 5]")
-    W = (ep_schedule_capacity(cfg) - R) // 2
+    W = (ep_schedule_capacity(cfg) - R) // cfg.hop_classes
     if worker_begin.dim() != 1 or worker_begin.numel() < W + 1:
         raise ValueError(f"worker_begin: expected int32 [>= {W + 1}]")
     if workspace.dtype != torch.uint8:
@@ -352,7 +357,7 @@ class LayerBuffers:
     def allocate(cls, cfg: EpConfig, device="cuda", y_is_send: bool = False) -> "LayerBuffers":
         T, H, E, R, k = cfg.T, cfg.H, cfg.E, cfg.R, cfg.k
         cap = ep_schedule_capacity(cfg)
-        W = (cap - R) // 2
+        W = (cap - R) // cfg.hop_classes
         i32 = dict(dtype=torch.int32, device=device)
         send = torch.empty((T * k, H), dtype=torch.bfloat16, device=device)
         return cls(
@@ -437,7 +442,7 @@ class BoundLayer:
         self._keep = (b, cfg)
         st = _stream(stream)
         cap = ep_schedule_capacity(cfg)
-        W = (cap - R) // 2
+        W = (cap - R) // cfg.hop_classes
         if b.chunks.shape[0] < cap or b.worker_begin.numel() < W + 1:
             raise ValueError("chunk table or worker_begin too small")
         self._route = (self._cfg, _ptr(b.logits, torch.float32, (T, E), "logits"),

@@ -199,44 +199,75 @@ __device__ __forceinline__ int32_t share_bound(int32_t N, int32_t w, int32_t W) 
     return (int32_t)((int64_t)N * w / W);
 }
 
+// The ranks of one hop class: at most two runs of consecutive ranks,
+// [a0, a0 + n0) then [a1, a1 + n - n0), in ascending order.
+struct ClassRuns {
+    int32_t a0, n0, a1, n;
+    __device__ __forceinline__ int32_t rank(int32_t i) const { return i < n0 ? a0 + i : a1 + (i - n0); }
+};
+
+// Class c's runs for the sending rank's node [nl, nh) inside its pod [pl, ph)
+// (the pod is [0, R) when there is no pod tier): class 0 = the node, class 1
+// = the pod around it, class 2 = everything outside the pod.
+__device__ __forceinline__ ClassRuns class_runs(int c, int32_t R, int32_t nl, int32_t nh, int32_t pl, int32_t ph) {
+    ClassRuns q;
+    if (c == 0) {
+        q.a0 = nl; q.n0 = nh - nl; q.a1 = nh; q.n = nh - nl;
+    } else if (c == 1) {
+        q.a0 = pl; q.n0 = nl - pl; q.a1 = nh; q.n = (nl - pl) + (ph - nh);
+    } else {
+        q.a0 = 0; q.n0 = pl; q.a1 = ph; q.n = pl + (R - ph);
+    }
+    return q;
+}
+
 // The chunk schedule, built by one whole CTA from rank offsets in shared
-// memory. Class 0 (near) is ranks [n_lo, n_hi) of self_rank's node; class 1
-// (far) is [0, n_lo) followed by [n_hi, R). s_P (R + 2 ints of shared memory)
-// receives each class's prefix sums P_c[i] = rows in its first i ranks. A
-// worker finds the first and last rank its share touches by two quaternary
-// searches per class, counts the non-empty ranks in between, and after a CTA
-// scan over the counts writes its chunks.
-__device__ void cta_build_schedule(const int32_t *s_roff, int32_t R, int32_t W, int32_t ranks_per_node,
-                                   int32_t self_rank, ep_chunk *chunks, int32_t *n_chunks, int32_t *worker_begin,
-                                   int *s_warp, int32_t *s_P) {
-    const int32_t node = self_rank / ranks_per_node;
-    const int32_t n_lo = node * ranks_per_node;
-    const int32_t n_hi = n_lo + ranks_per_node < R ? n_lo + ranks_per_node : R;
-    const int32_t n0 = n_hi - n_lo, n1 = R - n0;
-    int32_t *P1 = s_P;           // far class: n1 + 1 entries
-    int32_t *P0 = s_P + n1 + 1;  // near class: n0 + 1 entries
-    for (int32_t i = threadIdx.x; i <= n1; i += blockDim.x)
-        P1[i] = i <= n_lo ? s_roff[i] : s_roff[n_lo] + (s_roff[i + n0] - s_roff[n_hi]);
-    for (int32_t i = threadIdx.x; i <= n0; i += blockDim.x) P0[i] = s_roff[n_lo + i] - s_roff[n_lo];
+// memory. s_P (R + 3 ints of shared memory) receives each class's prefix sums
+// P_c[i] = rows in the class's first i ranks. A worker finds the first and
+// last rank its share of each class touches by two quaternary searches,
+// counts the non-empty ranks in between, and after a CTA scan over the counts
+// writes its chunks, farthest class first.
+__device__ void cta_build_schedule(const int32_t *s_roff, int32_t R, int32_t W, HopTiers h, ep_chunk *chunks,
+                                   int32_t *n_chunks, int32_t *worker_begin, int *s_warp, int32_t *s_P) {
+    const int32_t nl = h.self_rank / h.ranks_per_node * h.ranks_per_node;
+    const int32_t nh = nl + h.ranks_per_node < R ? nl + h.ranks_per_node : R;
+    const int32_t pl = h.ranks_per_pod > 0 ? h.self_rank / h.ranks_per_pod * h.ranks_per_pod : 0;
+    const int32_t ph = h.ranks_per_pod > 0 ? (pl + h.ranks_per_pod < R ? pl + h.ranks_per_pod : R) : R;
+    ClassRuns q[3];
+    int32_t *P[3];
+    int32_t base = 0;
+#pragma unroll
+    for (int c = 0; c < 3; ++c) {
+        q[c] = class_runs(c, R, nl, nh, pl, ph);
+        P[c] = s_P + base;
+        base += q[c].n + 1;
+    }
+#pragma unroll
+    for (int c = 0; c < 3; ++c) {
+        const ClassRuns qc = q[c];
+        for (int32_t i = threadIdx.x; i <= qc.n; i += blockDim.x)
+            P[c][i] = i <= qc.n0 ? s_roff[qc.a0 + i] - s_roff[qc.a0]
+                                 : (s_roff[qc.a0 + qc.n0] - s_roff[qc.a0]) + (s_roff[qc.a1 + (i - qc.n0)] - s_roff[qc.a1]);
+    }
     __syncthreads();
-    const int32_t N[2] = {P0[n0], P1[n1]};
+    int32_t N[3];
+#pragma unroll
+    for (int c = 0; c < 3; ++c) N[c] = P[c][q[c].n];
 
     int carry = 0;
     for (int32_t wb = 0; wb < W; wb += blockDim.x) {
         const int32_t w = wb + (int32_t)threadIdx.x;
-        int32_t first[2] = {0, 0}, last[2] = {-1, -1}, lo[2] = {0, 0}, hi[2] = {0, 0};
+        int32_t first[3] = {0, 0, 0}, last[3] = {-1, -1, -1}, lo[3] = {0, 0, 0}, hi[3] = {0, 0, 0};
         int cnt = 0;
         if (w < W) {
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                const int32_t *P = c ? P1 : P0;
-                const int32_t n = c ? n1 : n0;
+            for (int c = 0; c < 3; ++c) {
                 lo[c] = share_bound(N[c], w, W);
                 hi[c] = share_bound(N[c], w + 1, W);
                 if (hi[c] > lo[c]) {
-                    first[c] = quaternary_search(P, n, lo[c]);
-                    last[c] = quaternary_search(P, n, hi[c] - 1);
-                    for (int32_t i = first[c]; i <= last[c]; ++i) cnt += P[i + 1] > P[i] ? 1 : 0;
+                    first[c] = quaternary_search(P[c], q[c].n, lo[c]);
+                    last[c] = quaternary_search(P[c], q[c].n, hi[c] - 1);
+                    for (int32_t i = first[c]; i <= last[c]; ++i) cnt += P[c][i + 1] > P[c][i] ? 1 : 0;
                 }
             }
         }
@@ -246,19 +277,18 @@ __device__ void cta_build_schedule(const int32_t *s_roff, int32_t R, int32_t W, 
             worker_begin[w] = pos0;
             int pos = pos0;
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                const int c = 1 - cc;  // other-node traffic first
-                const int32_t *P = c ? P1 : P0;
+            for (int c = 2; c >= 0; --c) {
+                const int32_t *Pc = P[c];
                 for (int32_t i = first[c]; i <= last[c]; ++i) {
-                    if (P[i + 1] == P[i]) continue;
-                    const int32_t r = c ? (i < n_lo ? i : i + n0) : n_lo + i;
-                    const int32_t a = lo[c] > P[i] ? lo[c] : P[i];
-                    const int32_t bnd = hi[c] < P[i + 1] ? hi[c] : P[i + 1];
+                    if (Pc[i + 1] == Pc[i]) continue;
+                    const int32_t r = q[c].rank(i);
+                    const int32_t a = lo[c] > Pc[i] ? lo[c] : Pc[i];
+                    const int32_t bnd = hi[c] < Pc[i + 1] ? hi[c] : Pc[i + 1];
                     ep_chunk ch;
                     ch.worker = w;
                     ch.hop_class = c;
                     ch.dst_rank = r;
-                    ch.row_begin = s_roff[r] + (a - P[i]);
+                    ch.row_begin = s_roff[r] + (a - Pc[i]);
                     ch.row_count = bnd - a;
                     chunks[pos++] = ch;
                 }

@@ -90,6 +90,8 @@ ep_status check_rows(const ep_config *c) {
 ep_status check_schedule(const ep_config *c) {
     if (c->ranks_per_node <= 0 || c->self_rank < 0 || c->self_rank >= c->R || c->num_workers < 0)
         return EP_ERR_INVALID_ARG;
+    if (c->ranks_per_pod < 0 || (c->ranks_per_pod > 0 && c->ranks_per_pod % c->ranks_per_node != 0))
+        return EP_ERR_INVALID_ARG;
     return EP_OK;
 }
 
@@ -168,7 +170,7 @@ ep_status ep_schedule_capacity(const ep_config *cfg, int32_t *capacity) {
     if (!capacity) return EP_ERR_INVALID_ARG;
     int32_t W = 0;
     if ((st = resolve_workers(cfg, &W)) != EP_OK) return st;
-    const int64_t cap = 2 * (int64_t)W + cfg->R;
+    const int64_t cap = (int64_t)ep::hop_classes(*cfg) * W + cfg->R;
     if (cap > INT32_MAX) return EP_ERR_INVALID_ARG;
     *capacity = (int32_t)cap;
     return EP_OK;
@@ -223,7 +225,7 @@ ep_status ep_layout(const ep_config *cfg, const int32_t *topk_idx, int32_t *expe
     if (cfg->T > 0 && (!topk_idx || !slot)) return EP_ERR_INVALID_ARG;
     int32_t W = 0;
     if ((st = resolve_workers(cfg, &W)) != EP_OK) return st;
-    if ((int64_t)chunk_capacity < 2 * (int64_t)W + cfg->R) return EP_ERR_CAPACITY;
+    if ((int64_t)chunk_capacity < (int64_t)ep::hop_classes(*cfg) * W + cfg->R) return EP_ERR_CAPACITY;
     const size_t need = ep::layout_workspace(*cfg).bytes;
     if (need > 0) {
         if (!workspace) return EP_ERR_INVALID_ARG;
@@ -250,7 +252,7 @@ ep_status ep_dispatch_fused(const ep_config *cfg, const float *logits, const ep_
     if (cfg->T > 0 && (!aligned16(x) || !aligned16(send))) return EP_ERR_INVALID_ARG;
     int32_t W = 0;
     if ((st = resolve_workers(cfg, &W)) != EP_OK) return st;
-    if ((int64_t)chunk_capacity < 2 * (int64_t)W + cfg->R) return EP_ERR_CAPACITY;
+    if ((int64_t)chunk_capacity < (int64_t)ep::hop_classes(*cfg) * W + cfg->R) return EP_ERR_CAPACITY;
     const size_t need = ep::fused_workspace_bytes(*cfg);
     if (need > 0) {
         if (!workspace) return EP_ERR_INVALID_ARG;
@@ -383,7 +385,7 @@ extern "C" ep_status ep_layout_static(const ep_config *cfg, const int32_t *topk_
     if (ep::layout_workspace(*cfg).bytes > (size_t)EP_LAYOUT_STATIC_SCRATCH_BYTES) return EP_ERR_CAPACITY;
     int32_t W = 0;
     if ((st = resolve_workers(cfg, &W)) != EP_OK) return st;
-    if ((int64_t)chunk_capacity < 2 * (int64_t)W + cfg->R) return EP_ERR_CAPACITY;
+    if ((int64_t)chunk_capacity < (int64_t)ep::hop_classes(*cfg) * W + cfg->R) return EP_ERR_CAPACITY;
     void *scratch = nullptr;
     if ((st = static_scratch_address(&scratch)) != EP_OK) return st;
     return from_cuda(ep::launch_layout(*cfg, W, topk_idx, expert_count, expert_offset, rank_count, rank_offset,

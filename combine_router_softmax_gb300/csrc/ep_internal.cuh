@@ -14,6 +14,13 @@
 
 namespace ep {
 
+// The hop tiers the chunk schedule classes ranks by (ep_config fields).
+struct HopTiers {
+    int32_t ranks_per_node, ranks_per_pod, self_rank;
+};
+inline HopTiers hop_tiers(const ep_config &c) { return HopTiers{c.ranks_per_node, c.ranks_per_pod, c.self_rank}; }
+inline int hop_classes(const ep_config &c) { return c.ranks_per_pod > 0 ? 3 : 2; }
+
 constexpr int kFullMask = -1;  // all 32 lanes (as unsigned in shuffles)
 
 // Layout tiling: a layout CTA owns kLayoutTokens consecutive tokens, 32 per warp.

@@ -50,7 +50,7 @@ size_t align128(size_t b) { return (b + 127) & ~(size_t)127; }
 // Shared-memory carve-up, in this order (each piece 128-byte aligned):
 // stages, mbarriers, tile_e, tile_r, tile_s, cnt [8][E], group logits [8][E],
 // cand [8][32] int2, pick [8][32] int2, s_tot [E], s_eoff [E+2], s_base [E],
-// s_roff [R+1], s_P [R+2], s_col [E + 1024] (the column scan's counts).
+// s_roff [R+1], s_P [R+3], s_col [E + 1024] (the column scan's counts).
 struct SmemLayout {
     size_t stages, bars, tile_e, tile_r, tile_s, cnt, glog, cand, pick, tot, eoff, base, roff, P, col, bytes;
 };
@@ -77,7 +77,7 @@ __host__ __device__ inline SmemLayout smem_layout(int ns, int row_pad, int tb, i
     L.eoff = take(sizeof(int32_t) * ((size_t)E + 2));
     L.base = take(sizeof(int32_t) * (size_t)E);
     L.roff = take(sizeof(int32_t) * ((size_t)R + 1));
-    L.P = take(sizeof(int32_t) * ((size_t)R + 2));
+    L.P = take(sizeof(int32_t) * ((size_t)R + 3));
     L.col = take(sizeof(int32_t) * ((size_t)E + kMaxFusedCTAs));  // my experts x tiles <= E + nb
     L.bytes = o;
     return L;
@@ -98,7 +98,8 @@ struct FusedArgs {
     int32_t *totals;  // [E]
     unsigned *sync;   // [2] barrier arrivals
     int32_t *err;
-    int32_t T, H, E, R, k, n_groups, topk_groups, renormalize, W, rpn, self_rank;
+    int32_t T, H, E, R, k, n_groups, topk_groups, renormalize, W;
+    HopTiers tiers;
     int32_t nb, tb, ns, row_pad;
 };
 
@@ -254,8 +255,7 @@ __global__ void __launch_bounds__(kFusedThreads) dispatch_fused_kernel(FusedArgs
         if (b == a.nb - 1) {
             for (int r = threadIdx.x; r <= a.R; r += blockDim.x) s_roff[r] = s_eoff[r * epr];
             __syncthreads();
-            cta_build_schedule(s_roff, a.R, a.W, a.rpn, a.self_rank, a.chunks, a.n_chunks, a.worker_begin, s_warp32,
-                               s_P);
+            cta_build_schedule(s_roff, a.R, a.W, a.tiers, a.chunks, a.n_chunks, a.worker_begin, s_warp32, s_P);
         }
         __syncthreads();
     } else if (threadIdx.x == 0) {
@@ -493,8 +493,7 @@ cudaError_t launch_dispatch_fused(const ep_config &c, int32_t W, const float *lo
     a.topk_groups = c.topk_groups;
     a.renormalize = c.renormalize;
     a.W = W;
-    a.rpn = c.ranks_per_node;
-    a.self_rank = c.self_rank;
+    a.tiers = hop_tiers(c);
     a.nb = p.nb;
     a.tb = p.tb;
     a.ns = p.ns;

@@ -45,7 +45,7 @@ size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
 
 // Shared memory of the fused kernel for nw warps.
 size_t fused_smem_bytes(int nw, int32_t E, int32_t R, int32_t k) {
-    return sizeof(int32_t) * ((size_t)nw * E + 2 * (size_t)nw * 32 * k + 3 * (size_t)E + 2 + 2 * (size_t)R + 3);
+    return sizeof(int32_t) * ((size_t)nw * E + 2 * (size_t)nw * 32 * k + 3 * (size_t)E + 2 + 2 * (size_t)R + 4);
 }
 
 // Warps per fused CTA (8, 16 or 32): the fewest that keep the grid at <= 32
@@ -83,7 +83,7 @@ layout_fused_kernel(const int32_t *__restrict__ idx, int32_t T, int32_t E, int32
                     int32_t *__restrict__ expert_offset, int32_t *__restrict__ rank_count,
                     int32_t *__restrict__ rank_offset, int32_t *__restrict__ slot, ep_chunk *__restrict__ chunks,
                     int32_t *__restrict__ n_chunks, int32_t *__restrict__ worker_begin, int32_t W,
-                    int32_t ranks_per_node, int32_t self_rank) {
+                    HopTiers tiers) {
     extern __shared__ int32_t sm[];
     const int nw = blockDim.x >> 5;
     int32_t *cnt = sm;                         // [nw][E]
@@ -93,7 +93,7 @@ layout_fused_kernel(const int32_t *__restrict__ idx, int32_t T, int32_t E, int32
     int32_t *s_pre = s_tot + E;                // [E]   pairs of expert e in CTAs before this one
     int32_t *s_eoff = s_pre + E;               // [E+2] expert offsets (+ total)
     int32_t *s_roff = s_eoff + E + 2;          // [R+1] rank offsets
-    int32_t *s_P = s_roff + R + 1;             // [R+2] class prefix sums (schedule)
+    int32_t *s_P = s_roff + R + 1;             // [R+3] class prefix sums (schedule)
     __shared__ int s_warp32[32];
 
     const int b = blockIdx.x;
@@ -189,7 +189,7 @@ layout_fused_kernel(const int32_t *__restrict__ idx, int32_t T, int32_t E, int32
     if (b == nb - 1) {
         for (int r = threadIdx.x; r <= R; r += blockDim.x) s_roff[r] = s_eoff[r * epr];
         __syncthreads();
-        cta_build_schedule(s_roff, R, W, ranks_per_node, self_rank, chunks, n_chunks, worker_begin, s_warp32, s_P);
+        cta_build_schedule(s_roff, R, W, tiers, chunks, n_chunks, worker_begin, s_warp32, s_P);
     }
 }
 
@@ -221,7 +221,7 @@ layout_scan_kernel(int32_t *__restrict__ block_counts, int32_t nb, int32_t E, in
                    int32_t *__restrict__ expert_count, int32_t *__restrict__ expert_offset,
                    int32_t *__restrict__ rank_count, int32_t *__restrict__ rank_offset,
                    ep_chunk *__restrict__ chunks, int32_t *__restrict__ n_chunks,
-                   int32_t *__restrict__ worker_begin, int32_t W, int32_t ranks_per_node, int32_t self_rank) {
+                   int32_t *__restrict__ worker_begin, int32_t W, HopTiers tiers) {
     __shared__ int64_t s_warp[32];
     __shared__ int32_t s_eoff[kMaxE + 1];
     __shared__ int32_t s_roff[kMaxE + 1];
@@ -264,8 +264,8 @@ layout_scan_kernel(int32_t *__restrict__ block_counts, int32_t nb, int32_t E, in
 
     // (c) chunk schedule.
     __shared__ int s_warp32[32];
-    __shared__ int32_t s_P[kMaxE + 2];
-    cta_build_schedule(s_roff, R, W, ranks_per_node, self_rank, chunks, n_chunks, worker_begin, s_warp32, s_P);
+    __shared__ int32_t s_P[kMaxE + 3];
+    cta_build_schedule(s_roff, R, W, tiers, chunks, n_chunks, worker_begin, s_warp32, s_P);
 }
 
 __global__ void __launch_bounds__(256)
@@ -306,7 +306,7 @@ cudaError_t launch_fallback(const ep_config &c, int32_t W, const int32_t *idx, i
     }
     layout_scan_kernel<<<1, kScanThreads, 0, s>>>(block_counts, (int32_t)nb, c.E, c.R, expert_count, expert_offset,
                                                   rank_count, rank_offset, chunks, n_chunks, worker_begin, W,
-                                                  c.ranks_per_node, c.self_rank);
+                                                  hop_tiers(c));
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (nb > 0) {
@@ -372,10 +372,11 @@ cudaError_t launch_layout(const ep_config &c, int32_t W, const int32_t *idx, int
         if (e != cudaSuccess) return e;
     }
     const size_t smem = fused_smem_bytes(nw, c.E, c.R, c.k);
-    int32_t T = c.T, E = c.E, R = c.R, k = c.k, nbi = (int32_t)nb, rpn = c.ranks_per_node, self = c.self_rank;
+    int32_t T = c.T, E = c.E, R = c.R, k = c.k, nbi = (int32_t)nb;
+    HopTiers tiers = hop_tiers(c);
     void *args[] = {(void *)&idx, &T, &E, &R, &k, &nbi, (void *)&counts, (void *)&sync, (void *)&expert_count,
                     (void *)&expert_offset, (void *)&rank_count, (void *)&rank_offset, (void *)&slot,
-                    (void *)&chunks, (void *)&n_chunks, (void *)&worker_begin, &W, &rpn, &self};
+                    (void *)&chunks, (void *)&n_chunks, (void *)&worker_begin, &W, &tiers};
     return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(layout_fused_kernel), dim3((unsigned)nb),
                                        dim3((unsigned)(nw * 32)), args, smem, s);
 }

@@ -30,6 +30,7 @@ class Workload:
     ranks_per_node: int = 16
     self_rank: int = 0
     num_workers: int = 152
+    ranks_per_pod: int = 0   # 0: no pod tier (two hop classes)
     note: str = ""
 
     def with_(self, **kw) -> "Workload":

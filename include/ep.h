@@ -68,11 +68,15 @@ typedef struct ep_config {
     int32_t ranks_per_node; /* ranks sharing one node: defines the hop classes (>= 1)     */
     int32_t self_rank;      /* the sending rank whose view the schedule models [0, R)     */
     int32_t num_workers;    /* W, workers of the chunk schedule; 0 = the device SM count  */
+    int32_t ranks_per_pod;  /* ranks sharing one pod (a second switch tier): 0 = no pod
+                               tier (hop classes 0 and 1); else a multiple of
+                               ranks_per_node, and ranks in another pod form class 2   */
 } ep_config;
 
 /* One record of the chunk schedule: rows [row_begin, row_begin + row_count)
  * of the send buffer, all bound for dst_rank, handled by `worker`.
- * hop_class 0 = a rank on the sender's node, 1 = a rank on another node. */
+ * hop_class 0 = a rank on the sender's node, 1 = a rank on another node (of
+ * the same pod, when pods are given), 2 = a rank in another pod. */
 typedef struct ep_chunk {
     int32_t worker;
     int32_t hop_class;
@@ -114,8 +118,9 @@ ep_status ep_check_bounded_wait(int32_t max_polls, int32_t *gave_up, cudaStream_
  * calls on the same stream. */
 ep_status ep_layout_workspace_size(const ep_config *cfg, size_t *bytes);
 
-/* Number of ep_chunk records ep_layout may write for `cfg`: 2 W + R
- * (W = num_workers, or the current device's SM count when num_workers = 0). */
+/* Number of ep_chunk records ep_layout may write for `cfg`: C W + R, with C
+ * the number of hop classes (2, or 3 when ranks_per_pod > 0) and W =
+ * num_workers, or the current device's SM count when num_workers = 0. */
 ep_status ep_schedule_capacity(const ep_config *cfg, int32_t *capacity);
 
 /* Number of kernels one ep_route + ep_layout + ep_dispatch + ep_combine pass
@@ -161,14 +166,16 @@ ep_status ep_route(const ep_config *cfg, const float *logits, int32_t *topk_idx,
  *   slot[t, j]       = expert_offset[e] + #{t' < t : e in topk_idx[t', :]}, e = topk_idx[t, j]
  * i.e. send rows are ordered by (destination rank, expert, source token).
  *
- * Chunk schedule (Latency Homogenization): hop_class(r) = 0 if rank r is on
- * the node of self_rank (r / ranks_per_node == self_rank / ranks_per_node),
+ * Chunk schedule (Latency Homogenization; the same section extends it to
+ * more switch tiers): hop_class(r) = 0 if rank r is on the node of self_rank
+ * (r / ranks_per_node == self_rank / ranks_per_node); else 2 if
+ * ranks_per_pod > 0 and r / ranks_per_pod != self_rank / ranks_per_pod;
  * else 1. For each class c, the class's rank segments concatenated in
  * ascending rank hold N_c rows; worker w takes positions
  * [floor(N_c w / W), floor(N_c (w + 1) / W)) of each class, cut at rank
  * boundaries into non-empty chunks. The table is ordered by worker, then
- * class descending (other-node traffic first), then rank; worker_begin[w] is
- * the index of worker w's first chunk and worker_begin[W] = *n_chunks.
+ * class descending (the farthest traffic first), then rank; worker_begin[w]
+ * is the index of worker w's first chunk and worker_begin[W] = *n_chunks.
  *
  * topk_idx      : const int32 [T, k]; each row holds k distinct experts in
  *                 [0, E) (as ep_route writes). An id outside [0, E) gets
@@ -179,7 +186,7 @@ ep_status ep_route(const ep_config *cfg, const float *logits, int32_t *topk_idx,
  * rank_count    : int32 [R]      output
  * rank_offset   : int32 [R + 1]  output
  * slot          : int32 [T, k]   output
- * chunks        : ep_chunk [chunk_capacity] output; chunk_capacity >= 2 W + R
+ * chunks        : ep_chunk [chunk_capacity] output; chunk_capacity >= C W + R
  *                 (ep_schedule_capacity), else EP_ERR_CAPACITY
  * n_chunks      : int32 [1]      output (device memory)
  * worker_begin  : int32 [W + 1]  output

@@ -43,7 +43,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_struct_layout(lib):
-    assert ctypes.sizeof(lib.EpConfig) == 11 * 4
+    assert ctypes.sizeof(lib.EpConfig) == 12 * 4
     assert ctypes.sizeof(lib.EpChunk) == 5 * 4
 
 
@@ -92,6 +92,17 @@ def test_null_and_shape_errors(lib):
     assert L.ep_dispatch(ctypes.byref(cfg), ctypes.c_void_p(0x10008), FAKE, FAKE, FAKE, None) == lib.EP_ERR_INVALID_ARG
     assert L.ep_combine(ctypes.byref(cfg), FAKE, FAKE, FAKE, ctypes.c_void_p(0x10004), None) == lib.EP_ERR_INVALID_ARG
     assert L.ep_combine(ctypes.byref(cfg), FAKE, None, FAKE, FAKE, None) == lib.EP_ERR_INVALID_ARG
+
+
+def test_pod_tier_capacity_and_validation(lib):
+    """With a pod tier the schedule has three hop classes: capacity 3 W + R;
+    ranks_per_pod must be a non-negative multiple of ranks_per_node."""
+    assert lib.ep_schedule_capacity(_cfg(lib, ranks_per_node=2, ranks_per_pod=4)) == 3 * 8 + 4
+    assert lib.ep_schedule_capacity(_cfg(lib, ranks_per_node=2, ranks_per_pod=0)) == 2 * 8 + 4
+    n = ctypes.c_int32(0)
+    for bad in (dict(ranks_per_node=2, ranks_per_pod=3), dict(ranks_per_pod=-16)):
+        rc = lib._lib.ep_schedule_capacity(ctypes.byref(_cfg(lib, **bad)), ctypes.byref(n))
+        assert rc == lib.EP_ERR_INVALID_ARG
 
 
 def test_layout_capacity_and_workspace_errors(lib):

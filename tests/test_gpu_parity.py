@@ -73,7 +73,7 @@ def run_gpu(ep, w, logits, x_bits, identity=False):
 def run_oracle(orc, w, logits, x_bits, identity=False):
     return orc.run_path(logits, x_bits, E=w.E, R=w.R, k=w.k, n_groups=w.n_groups, topk_groups=w.topk_groups,
                         renormalize=w.renormalize, ranks_per_node=w.ranks_per_node, self_rank=w.self_rank,
-                        W=w.num_workers, identity_expert=identity)
+                        W=w.num_workers, identity_expert=identity, ranks_per_pod=w.ranks_per_pod)
 
 
 def assert_route(g, r, logits, renormalize):
@@ -103,6 +103,9 @@ SMALL = [
     ep_synth.CONFIGS["tiny"].with_(name="tiny-plain-softmax", renormalize=0),
     ep_synth.CONFIGS["mid"].with_(name="mid-T300-plain", T=300, renormalize=0),
     ep_synth.CONFIGS["tiny"].with_(name="tiny-2nodes", ranks_per_node=2, self_rank=3, num_workers=5),
+    ep_synth.CONFIGS["tiny"].with_(name="tiny-3tiers", ranks_per_node=1, ranks_per_pod=2, self_rank=2, num_workers=5),
+    ep_synth.CONFIGS["prefill"].with_(name="prefill-T1000-pods", T=1000, ranks_per_node=4, ranks_per_pod=16,
+                                      self_rank=21),
 ] + [w for w in ep_synth.sweep_workloads() if w.T <= 512]
 
 
@@ -186,7 +189,7 @@ def _route_layout(ep, orc, w, logits):
              slot=b.slot.cpu().numpy(), chunks=b.chunks[:n].cpu().numpy(), worker_begin=b.worker_begin.cpu().numpy())
     idx, w64 = orc.route(logits, w.k, w.n_groups, w.topk_groups, w.renormalize)
     lay = orc.layout(idx, w.E, w.R)
-    ch, wb = orc.schedule(lay["rank_offset"], w.ranks_per_node, w.self_rank, w.num_workers)
+    ch, wb = orc.schedule(lay["rank_offset"], w.ranks_per_node, w.self_rank, w.num_workers, w.ranks_per_pod)
     r = dict(idx=idx, w=w64, chunks=ch, worker_begin=wb, **lay)
     return g, r
 
@@ -207,6 +210,13 @@ EDGE = [
     ("W5000-rpn1", ep_synth.CONFIGS["decode"].with_(T=200, num_workers=5000, ranks_per_node=1, self_rank=63), None),
     ("rpn-ge-R", ep_synth.CONFIGS["decode"].with_(T=200, ranks_per_node=100, self_rank=10), None),
     ("zipf-empty-experts", ep_synth.CONFIGS["prefill"].with_(T=40, zipf_s=3.0), None),
+    ("pods-W5000", ep_synth.CONFIGS["decode"].with_(T=200, num_workers=5000, ranks_per_node=2, ranks_per_pod=8,
+                                                    self_rank=63), None),
+    ("pods-W1", ep_synth.CONFIGS["prefill"].with_(T=300, num_workers=1, ranks_per_node=1, ranks_per_pod=4,
+                                                  self_rank=6), None),
+    ("pod-ge-R", ep_synth.CONFIGS["decode"].with_(T=200, ranks_per_node=4, ranks_per_pod=128, self_rank=10), None),
+    ("pods-E1024", ep_synth.Workload("maxp", T=300, H=64, E=1024, R=1024, k=32, ranks_per_node=8, ranks_per_pod=64,
+                                     self_rank=1000, num_workers=152), None),
 ]
 
 
@@ -221,7 +231,7 @@ def test_route_layout_edges(ep, orc, name, w, mode):
     assert_route(g, r, logits, w.renormalize)
     assert_layout(g, r)
     check_schedule_invariants(g["chunks"], g["worker_begin"], g["rank_offset"], w.ranks_per_node, w.self_rank,
-                              w.num_workers)
+                              w.num_workers, w.ranks_per_pod)
 
 
 def test_layout_T0(ep):
@@ -327,22 +337,22 @@ def test_route_unaligned_logits(ep, orc):
     assert_route(dict(idx=idx.cpu().numpy(), w=w.cpu().numpy()), dict(idx=r_idx, w=r_w), logits, 1)
 
 
-@pytest.mark.parametrize("T,E,R,k", [(400_000, 256, 32, 8), (160_000, 1024, 64, 32)])
-def test_layout_many_ctas(ep, orc, T, E, R, k):
+@pytest.mark.parametrize("T,E,R,k,rpp", [(400_000, 256, 32, 8, 0), (160_000, 1024, 64, 32, 32)])
+def test_layout_many_ctas(ep, orc, T, E, R, k, rpp):
     """T beyond one co-resident grid: the three-kernel layout path."""
     rng = np.random.default_rng(T)
     base = rng.integers(0, E, size=(T, 1))
     step = rng.integers(1, E // k + 1, size=(T, 1))
     idx = ((base + step * np.arange(k)[None, :]) % E).astype(np.int32)  # k distinct experts per token
     assert (np.sort(idx, axis=1)[:, 1:] != np.sort(idx, axis=1)[:, :-1]).all()
-    w = ep_synth.Workload("many", T=T, H=8, E=E, R=R, k=k, num_workers=152)
+    w = ep_synth.Workload("many", T=T, H=8, E=E, R=R, k=k, num_workers=152, ranks_per_pod=rpp, self_rank=R - 1)
     cfg = ep.EpConfig.from_workload(w)
     b = ep.LayerBuffers.allocate(cfg)
     b.topk_idx.copy_(torch.from_numpy(idx))
     b.layout()
     torch.cuda.synchronize()
     lay = orc.layout(idx, E, R)
-    ch, wb = orc.schedule(lay["rank_offset"], w.ranks_per_node, w.self_rank, w.num_workers)
+    ch, wb = orc.schedule(lay["rank_offset"], w.ranks_per_node, w.self_rank, w.num_workers, w.ranks_per_pod)
     n = int(b.n_chunks.item())
     g = dict(expert_count=b.expert_count.cpu().numpy(), expert_offset=b.expert_offset.cpu().numpy(),
              rank_count=b.rank_count.cpu().numpy(), rank_offset=b.rank_offset.cpu().numpy(),
@@ -385,6 +395,10 @@ FUSED = [
     ep_synth.Workload("k12-groups", T=257, H=2048, E=96, R=6, k=12, n_groups=6, topk_groups=2, ranks_per_node=2,
                       self_rank=5, num_workers=33),
     ep_synth.Workload("fallback-T80000", T=80000, H=256, E=256, R=32, k=8, num_workers=152),
+    ep_synth.Workload("pods-T64", T=64, H=7168, E=256, R=64, k=8, ranks_per_node=4, ranks_per_pod=16, self_rank=33,
+                      num_workers=152),
+    ep_synth.Workload("pods-T4096", T=4096, H=1024, E=256, R=64, k=8, ranks_per_node=4, ranks_per_pod=16,
+                      self_rank=5, num_workers=152),
 ] + [w for w in ep_synth.sweep_workloads() if w.T in (1, 8, 64, 512, 32768)]
 
 
