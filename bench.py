@@ -68,6 +68,9 @@ def parse_args(argv=None):
     p.add_argument("--data-as-flag", action="store_true",
                    help="also time dispatch + expert as two kernels (bulk-synchronous) and as one "
                         "sentinel-polling kernel (Data-as-Flag)")
+    p.add_argument("--schedule-ablation", action="store_true",
+                   help="also time the dispatch pulled by the chunk schedule under three tables (latency-"
+                        "homogenized, one class, whole ranks per worker) beside the token-major dispatch")
     p.add_argument("--separate", action="store_true",
                    help="step = ep_route, ep_layout, ep_dispatch, ep_combine (default: ep_dispatch_fused, ep_combine)")
     return p.parse_args(argv)
@@ -405,6 +408,125 @@ def data_as_flag_leg(ep, buf, w, device, flush_l2, K: int) -> dict:
     return out
 
 
+def rank_static_table(rank_offset, W: int):
+    """Ablation table: worker r mod W takes the whole send segment of rank r
+    (no balancing)."""
+    per = [[] for _ in range(W)]
+    for r in range(len(rank_offset) - 1):
+        n = int(rank_offset[r + 1] - rank_offset[r])
+        if n:
+            per[r % W].append([r % W, 0, r, int(rank_offset[r]), n])
+    rows, wb = [], [0]
+    for p in per:
+        rows += p
+        wb.append(len(rows))
+    return rows, wb
+
+
+def schedule_ablation_leg(ep, buf, w, device, flush_l2, K: int) -> dict:
+    """The dispatch pulled by the chunk schedule (ep_dispatch_scheduled) under
+    three tables over the same rows, beside the token-major ep_dispatch:
+      homogenized : ep_layout's table (every worker an equal share of each hop class);
+      one_class   : ep_layout's table with every rank in the sender's node (equal row
+                    shares, classes ignored: the token-count-only split);
+      rank_static : whole destination ranks per worker, no balancing.
+    Each is timed as a CUDA graph replayed K times with L2 flushed in between; one
+    more eager call records %globaltimer per CTA, from which the per-worker end
+    times (max over a worker's CTAs, relative to the earliest CTA start) give the
+    peak (the slowest worker) and its ratio to the mean."""
+    import numpy as np
+    import torch
+
+    row = w.H * 2
+    if row > 48 * 1024:
+        return {"unsupported": "rows above 48 KiB"}
+    cap = torch.cuda.Stream(device)
+    cap.wait_stream(torch.cuda.current_stream(device))
+    W = (ep.ep_schedule_capacity(buf.cfg) - w.R) // buf.cfg.hop_classes
+    tables = {}
+    with torch.cuda.stream(cap):
+        buf.layout(cap)
+    cap.synchronize()
+    n = int(buf.n_chunks.item())
+    tables["homogenized"] = (buf.chunks[:n].clone(), buf.worker_begin[:W + 1].clone())
+    one = ep.EpConfig.from_workload(w, ranks_per_node=w.R, ranks_per_pod=0, self_rank=0)
+    b1 = ep.LayerBuffers.allocate(one, device=device)
+    b1.topk_idx.copy_(buf.topk_idx)
+    with torch.cuda.stream(cap):
+        b1.layout(cap)
+    cap.synchronize()
+    n1 = int(b1.n_chunks.item())
+    tables["one_class"] = (b1.chunks[:n1].clone(), b1.worker_begin[:W + 1].clone())
+    del b1
+    rows, wb = rank_static_table(buf.rank_offset.cpu().numpy(), W)
+    tables["rank_static"] = (torch.tensor(rows, dtype=torch.int32, device=device).reshape(-1, 5),
+                             torch.tensor(wb, dtype=torch.int32, device=device))
+    chunks = torch.zeros((max(t[0].shape[0] for t in tables.values()) + 1, 5), dtype=torch.int32, device=device)
+    worker_begin = torch.zeros((W + 1,), dtype=torch.int32, device=device)
+    n_chunks = torch.zeros((1,), dtype=torch.int32, device=device)
+    ref_send = torch.empty_like(buf.send)
+    with torch.cuda.stream(cap):
+        buf.dispatch(cap)
+    cap.synchronize()
+    ref_send.copy_(buf.send)
+    n_ctas = ep.ep_dispatch_scheduled_ctas(buf.cfg)
+    ns = torch.zeros((n_ctas, 2), dtype=torch.int64, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def time_graph(fn):
+        with torch.cuda.stream(cap):
+            fn()
+            fn()
+        cap.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            fn()
+        torch.cuda.synchronize()
+        for _ in range(3):
+            flush_l2()
+            g.replay()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for a, b_ in ev:
+            flush_l2()
+            a.record(stream)
+            g.replay()
+            b_.record(stream)
+        torch.cuda.synchronize()
+        return round(1e3 * sum(a.elapsed_time(b_) for a, b_ in ev) / K, 2)
+
+    out = {"scatter_us": time_graph(lambda: ep.ep_dispatch(buf.cfg, buf.x, buf.slot, buf.send, buf.slot_meta, cap)),
+           "workers": W, "ctas": n_ctas, "steps": K}
+    for name, (ch, wbt) in tables.items():
+        chunks.zero_()
+        chunks[:ch.shape[0]].copy_(ch)
+        worker_begin.copy_(wbt)
+        n_chunks.fill_(ch.shape[0])
+
+        def fn(ns_arg=None):
+            ep.ep_dispatch_scheduled(buf.cfg, buf.x, buf.slot, chunks, n_chunks, worker_begin, buf.send,
+                                     buf.slot_meta, ns_arg, cap)
+
+        us = time_graph(fn)
+        flush_l2()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(cap):
+            fn(ns)
+        cap.synchronize()
+        same = bool(torch.equal(buf.send, ref_send))
+        t = ns.cpu().numpy().astype(np.int64)
+        t0 = t[:, 0].min()
+        end = np.zeros(W, np.int64)
+        for c in range(n_ctas):
+            end[c % W] = max(end[c % W], t[c, 1] - t0)
+        end_us = end / 1e3
+        rows_w = np.diff(wbt.cpu().numpy())  # chunks per worker (not rows)
+        out[name] = {"us": us, "peak_us": round(float(end_us.max()), 2), "mean_us": round(float(end_us.mean()), 2),
+                     "peak_over_mean": round(float(end_us.max() / max(end_us.mean(), 1e-9)), 3),
+                     "idle_workers": int((rows_w == 0).sum()), "same_send": same}
+    out["device_error"] = ep.ep_device_error()
+    return out
+
+
 def run_gb300(args):
     import numpy as np
     import torch
@@ -592,6 +714,8 @@ def run_gb300(args):
         "clocks": clk,
         "wall_s": round(wall, 3),
     }
+    if args.schedule_ablation:
+        line["schedule_ablation"] = schedule_ablation_leg(ep, buf, w, device, flush_l2, min(K, 500))
     if args.data_as_flag:
         line["data_as_flag"] = data_as_flag_leg(ep, buf, w, device, flush_l2, min(K, 500))
     if rank == 0 and not args.no_cpu_baseline:

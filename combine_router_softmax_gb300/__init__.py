@@ -28,7 +28,7 @@ EP_OK, EP_ERR_INVALID_ARG, EP_ERR_UNSUPPORTED, EP_ERR_CUDA, EP_ERR_CAPACITY = ra
 EXPORTS = ("ep_status_string", "ep_version", "ep_device_error", "ep_step_kernel_count", "ep_fused_step_kernel_count",
            "ep_layout_workspace_size", "ep_dispatch_fused_workspace_size", "ep_schedule_capacity",
            "ep_dispatch_fused", "ep_check_bounded_wait", "ep_sentinel_arm", "ep_expert_scale",
-           "ep_dispatch_expert_sp",
+           "ep_dispatch_expert_sp", "ep_dispatch_scheduled_ctas", "ep_dispatch_scheduled",
            "ep_route", "ep_layout", "ep_dispatch", "ep_combine", "ep_layout_static")
 # Size of the device array ep_layout_static uses instead of a workspace (include/ep.h).
 EP_LAYOUT_STATIC_SCRATCH_BYTES = 1 << 20
@@ -87,6 +87,8 @@ def _load() -> ctypes.CDLL:
     lib.ep_sentinel_arm.argtypes = [cfgp, vp, vp]
     lib.ep_expert_scale.argtypes = [cfgp, vp, vp, vp, vp, vp]
     lib.ep_dispatch_expert_sp.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.ep_dispatch_scheduled_ctas.argtypes = [cfgp, P(ctypes.c_int32)]
+    lib.ep_dispatch_scheduled.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.ep_step_kernel_count.argtypes = [cfgp, P(ctypes.c_int32)]
     lib.ep_fused_step_kernel_count.argtypes = [cfgp, P(ctypes.c_int32)]
     lib.ep_layout_workspace_size.argtypes = [cfgp, P(ctypes.c_size_t)]
@@ -101,6 +103,7 @@ def _load() -> ctypes.CDLL:
     lib.ep_combine.argtypes = [cfgp, vp, vp, vp, vp, vp]
     for f in ("ep_dispatch_fused_workspace_size", "ep_dispatch_fused", "ep_fused_step_kernel_count",
               "ep_check_bounded_wait", "ep_sentinel_arm", "ep_expert_scale", "ep_dispatch_expert_sp",
+              "ep_dispatch_scheduled_ctas", "ep_dispatch_scheduled",
               "ep_device_error", "ep_step_kernel_count", "ep_layout_workspace_size", "ep_schedule_capacity", "ep_route", "ep_layout",
               "ep_dispatch", "ep_combine", "ep_layout_static"):
         getattr(lib, f).restype = ctypes.c_int
@@ -278,6 +281,30 @@ def ep_dispatch_fused(cfg: EpConfig, logits, x, topk_idx, topk_w, expert_count, 
                                   _stream(stream)), "ep_dispatch_fused")
 
 
+def ep_dispatch_scheduled_ctas(cfg: EpConfig) -> int:
+    """CTAs of ep_dispatch_scheduled (rows of its optional cta_ns output)."""
+    n = ctypes.c_int32(0)
+    _check(_lib.ep_dispatch_scheduled_ctas(ctypes.byref(cfg), ctypes.byref(n)), "ep_dispatch_scheduled_ctas")
+    return n.value
+
+
+def ep_dispatch_scheduled(cfg: EpConfig, x, slot, chunks, n_chunks, worker_begin, send, slot_meta, cta_ns=None,
+                          stream=None) -> None:
+    """Dispatch pulled by the chunk schedule (same send / slot_meta as ep_dispatch)."""
+    T, H, k = cfg.T, cfg.H, cfg.k
+    ns = None
+    if cta_ns is not None:
+        ns = _ptr(cta_ns, torch.int64, (ep_dispatch_scheduled_ctas(cfg), 2), "cta_ns")
+    _check(_lib.ep_dispatch_scheduled(ctypes.byref(cfg), _ptr(x, torch.bfloat16, (T, H), "x"),
+                                      _ptr(slot, torch.int32, (T, k), "slot"),
+                                      _ptr(chunks, torch.int32, None, "chunks"),
+                                      _ptr(n_chunks, torch.int32, (1,), "n_chunks"),
+                                      _ptr(worker_begin, torch.int32, None, "worker_begin"),
+                                      _ptr(send, torch.bfloat16, (T * k, H), "send"),
+                                      _ptr(slot_meta, torch.int32, (T * k,), "slot_meta"), ns, _stream(stream)),
+           "ep_dispatch_scheduled")
+
+
 EP_SENTINEL_BF16 = 0xFFFF
 
 
@@ -401,6 +428,10 @@ class LayerBuffers:
         ep_dispatch_fused(self.cfg, self.logits, self.x, self.topk_idx, self.topk_w, self.expert_count,
                           self.expert_offset, self.rank_count, self.rank_offset, self.slot, self.chunks,
                           self.n_chunks, self.worker_begin, self.send, self.slot_meta, self.workspace, stream)
+
+    def dispatch_scheduled(self, cta_ns=None, stream=None):
+        ep_dispatch_scheduled(self.cfg, self.x, self.slot, self.chunks, self.n_chunks, self.worker_begin, self.send,
+                              self.slot_meta, cta_ns, stream)
 
     def sentinel_arm(self, stream=None):
         ep_sentinel_arm(self.cfg, self.send, stream)

@@ -267,6 +267,38 @@ ep_status ep_dispatch_fused(const ep_config *cfg, const float *logits, const ep_
                                                slot_meta, workspace, stream));
 }
 
+ep_status ep_dispatch_scheduled_ctas(const ep_config *cfg, int32_t *ctas) {
+    ep_status st = check_config(cfg);
+    if (st != EP_OK) return st;
+    if ((st = check_schedule(cfg)) != EP_OK) return st;
+    if (!ctas) return EP_ERR_INVALID_ARG;
+    int32_t W = 0;
+    if ((st = resolve_workers(cfg, &W)) != EP_OK) return st;
+    const int64_t n = ep::gather_ctas(*cfg, W);
+    if (n > INT32_MAX) return EP_ERR_INVALID_ARG;
+    *ctas = (int32_t)n;
+    return EP_OK;
+}
+
+ep_status ep_dispatch_scheduled(const ep_config *cfg, const ep_bf16 *x, const int32_t *slot, const ep_chunk *chunks,
+                                const int32_t *n_chunks, const int32_t *worker_begin, ep_bf16 *send,
+                                int32_t *slot_meta, int64_t *cta_ns, cudaStream_t stream) {
+    ep_status st = check_config(cfg);
+    if (st != EP_OK) return st;
+    if ((st = check_rows(cfg)) != EP_OK) return st;
+    if ((st = check_schedule(cfg)) != EP_OK) return st;
+    if (cfg->T == 0) return EP_OK;
+    if (!x || !slot || !chunks || !n_chunks || !worker_begin || !send || !slot_meta) return EP_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(send) || (reinterpret_cast<uintptr_t>(cta_ns) & 7u)) return EP_ERR_INVALID_ARG;
+    if (cfg->H * 2 > 48 * 1024) return EP_ERR_UNSUPPORTED;
+    int32_t W = 0;
+    if ((st = resolve_workers(cfg, &W)) != EP_OK) return st;
+    const cudaError_t e = ep::launch_dispatch_scheduled(*cfg, W, x, slot, chunks, n_chunks, worker_begin, send,
+                                                        slot_meta, cta_ns, stream);
+    if (e == cudaErrorNotSupported) return EP_ERR_UNSUPPORTED;
+    return from_cuda(e);
+}
+
 ep_status ep_sentinel_arm(const ep_config *cfg, ep_bf16 *send, cudaStream_t stream) {
     ep_status st = check_config(cfg);
     if (st != EP_OK) return st;

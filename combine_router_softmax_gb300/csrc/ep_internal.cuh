@@ -176,9 +176,16 @@ __device__ __forceinline__ void bulk_wait() {
 constexpr int32_t kErrDispatchWait = 1;  // a dispatch CTA gave up waiting for a bulk copy
 constexpr int32_t kErrFusedWait = 2;     // a fused-dispatch CTA gave up waiting (barrier or bulk copy)
 constexpr int32_t kErrSpWait = 4;        // a sentinel-polling CTA gave up waiting
+constexpr int32_t kErrGatherWait = 8;    // a schedule-driven dispatch CTA gave up waiting (or a bad table)
 cudaError_t dispatch_error_word(int32_t **addr);
 cudaError_t fused_error_word(int32_t **addr);
 cudaError_t sp_error_word(int32_t **addr);
+
+// Schedule-driven dispatch (gather.cu).
+int64_t gather_ctas(const ep_config &c, int32_t W);
+cudaError_t launch_dispatch_scheduled(const ep_config &c, int32_t W, const ep_bf16 *x, const int32_t *slot,
+                                      const ep_chunk *chunks, const int32_t *n_chunks, const int32_t *worker_begin,
+                                      ep_bf16 *send, int32_t *meta, int64_t *cta_ns, cudaStream_t s);
 
 // Data-as-Flag by sentinel polling (sp.cu).
 cudaError_t launch_sentinel_arm(const ep_config &c, ep_bf16 *send, cudaStream_t s);

@@ -102,6 +102,8 @@ int ep_version(void);
  *              copy); its slots or rows were not written.
  *   bit 2 (4): an ep_dispatch_expert_sp CTA gave up waiting (a row that never
  *              arrived, or a bulk copy); its rows were not all written.
+ *   bit 3 (8): an ep_dispatch_scheduled CTA gave up waiting on a bulk copy,
+ *              or its chunk table named rows outside the send buffer.
  * (ep_layout reports its own bounded wait through *n_chunks = -1.) */
 ep_status ep_device_error(int32_t *flags);
 
@@ -252,6 +254,37 @@ ep_status ep_dispatch_fused(const ep_config *cfg, const float *logits, const ep_
                             ep_chunk *chunks, int32_t chunk_capacity, int32_t *n_chunks,
                             int32_t *worker_begin, ep_bf16 *send, int32_t *slot_meta,
                             void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * ep_dispatch_scheduled -- the dispatch driven by the chunk schedule
+ * (the UBEP article, "Hierarchical Token-Level Scheduling": each worker moves
+ * the rows of its own chunk list).
+ *
+ * Writes the same send and slot_meta as ep_dispatch, by pulling rows: first
+ * slot_meta[slot[t, j]] = t k + j for every valid slot, then CTA c serves
+ * worker w = c mod W and copies send[s, :] = x[slot_meta[s] / k, :] for the
+ * rows s of worker w's chunks (CTA c takes the part c / W of each chunk, in
+ * ep_dispatch_scheduled_ctas / W parts). chunks / n_chunks / worker_begin are
+ * device pointers from ep_layout on the same cfg (or any table of the same
+ * form whose chunks tile the rows once); rows outside every chunk are not
+ * written. Each x row is read k times (from L2 when x fits there).
+ *
+ * x          : const bf16 [T, H], 16-byte aligned; rows of at most 48 KiB
+ *              (EP_ERR_UNSUPPORTED otherwise)
+ * slot       : const int32 [T, k] (ep_layout)
+ * send       : bf16 [T k, H] output, 16-byte aligned
+ * slot_meta  : int32 [T k] output
+ * cta_ns     : optional int64 [ep_dispatch_scheduled_ctas][2] output (or
+ *              NULL): %globaltimer (ns) when CTA c started and when its last
+ *              store had landed, for per-worker timing.
+ * A CTA that gives up a bounded wait, or meets a chunk outside [0, T k),
+ * sets ep_device_error bit 3 (8).
+ */
+ep_status ep_dispatch_scheduled_ctas(const ep_config *cfg, int32_t *ctas);
+
+ep_status ep_dispatch_scheduled(const ep_config *cfg, const ep_bf16 *x, const int32_t *slot,
+                                const ep_chunk *chunks, const int32_t *n_chunks, const int32_t *worker_begin,
+                                ep_bf16 *send, int32_t *slot_meta, int64_t *cta_ns, cudaStream_t stream);
 
 /*
  * Data-as-Flag by Sentinel Polling (the UBEP article, "Data-as-Flag" / SP).
