@@ -338,11 +338,13 @@ def call_bytes(w, name: str) -> int:
 
 
 def data_as_flag_leg(ep, buf, w, device, flush_l2, K: int) -> dict:
-    """dispatch -> expert handed over two ways, each captured in a CUDA graph and
+    """dispatch -> expert handed over three ways, each captured in a CUDA graph and
     replayed K times with L2 flushed in between:
       bsp: ep_dispatch, then ep_expert_scale (kernel boundary as the barrier);
       sp:  ep_dispatch_expert_sp (rows handed over by sentinel polling; each
-           call re-arms send for the next)."""
+           call re-arms send for the next);
+      sw:  ep_dispatch_expert_sw (stop-and-wait: a per-row flag released after
+           the row lands; two graphs with epochs 1 and 2 replayed in turn)."""
     import numpy as np
     import torch
 
@@ -360,6 +362,14 @@ def data_as_flag_leg(ep, buf, w, device, flush_l2, K: int) -> dict:
     def sp():
         buf.dispatch_expert_sp(scale, cap)
 
+    flag = torch.zeros(w.T * w.k, dtype=torch.int32, device=device)
+
+    def sw1():
+        buf.dispatch_expert_sw(scale, flag, 1, cap)
+
+    def sw2():
+        buf.dispatch_expert_sw(scale, flag, 2, cap)
+
     graphs = {}
     with torch.cuda.stream(cap):
         buf.layout(cap)
@@ -371,7 +381,13 @@ def data_as_flag_leg(ep, buf, w, device, flush_l2, K: int) -> dict:
         sp()
     cap.synchronize()
     same = bool(torch.equal(y_bsp, buf.y))
-    for name, fn in (("bsp", bsp), ("sp", sp)):
+    with torch.cuda.stream(cap):
+        buf.y.zero_()
+        sw1()
+        sw2()
+    cap.synchronize()
+    same = same and bool(torch.equal(y_bsp, buf.y))
+    for name, fn in (("bsp", bsp), ("sp", sp), ("sw1", sw1), ("sw2", sw2)):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=cap):
             fn()
@@ -379,17 +395,20 @@ def data_as_flag_leg(ep, buf, w, device, flush_l2, K: int) -> dict:
     torch.cuda.synchronize()
     out = {}
     stream = torch.cuda.current_stream(device)
-    for name in ("bsp", "sp"):
+    for name in ("bsp", "sp", "sw"):
         if name == "sp":
             buf.sentinel_arm(stream)
-        for _ in range(3):
+        # stop-and-wait alternates two graphs (epochs 1 and 2) so that every
+        # replay finds the other epoch in the flags
+        seq = [graphs["sw1"], graphs["sw2"]] if name == "sw" else [graphs[name]]
+        for i in range(4):
             flush_l2()
-            graphs[name].replay()
+            seq[i % len(seq)].replay()
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-        for a, b_ in ev:
+        for i, (a, b_) in enumerate(ev):
             flush_l2()
             a.record(stream)
-            graphs[name].replay()
+            seq[i % len(seq)].replay()
             b_.record(stream)
         torch.cuda.synchronize()
         out[name + "_us"] = round(1e3 * sum(a.elapsed_time(b_) for a, b_ in ev) / K, 2)
@@ -397,7 +416,8 @@ def data_as_flag_leg(ep, buf, w, device, flush_l2, K: int) -> dict:
     rows_b = w.T * w.k * row
     kb = w.algorithmic_bytes()
     out.update({
-        "bsp_kernels": 2, "sp_kernels": 1,
+        "bsp_kernels": 2, "sp_kernels": 1, "sw_kernels": 1,
+        "sw_bytes": kb["dispatch"] + 2 * rows_b + 2 * w.T * w.k * 4,
         "bsp_bytes": kb["dispatch"] + 2 * rows_b,
         "sp_bytes": kb["dispatch"] + 3 * rows_b,
         "same_output": same and err == 0,
@@ -405,6 +425,7 @@ def data_as_flag_leg(ep, buf, w, device, flush_l2, K: int) -> dict:
         "steps": K,
     })
     out["sp_speedup"] = round(out["bsp_us"] / out["sp_us"], 3)
+    out["sp_vs_sw_latency_cut"] = round(1.0 - out["sp_us"] / out["sw_us"], 3)
     return out
 
 

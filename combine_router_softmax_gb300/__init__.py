@@ -28,7 +28,7 @@ EP_OK, EP_ERR_INVALID_ARG, EP_ERR_UNSUPPORTED, EP_ERR_CUDA, EP_ERR_CAPACITY = ra
 EXPORTS = ("ep_status_string", "ep_version", "ep_device_error", "ep_step_kernel_count", "ep_fused_step_kernel_count",
            "ep_layout_workspace_size", "ep_dispatch_fused_workspace_size", "ep_schedule_capacity",
            "ep_dispatch_fused", "ep_check_bounded_wait", "ep_sentinel_arm", "ep_expert_scale",
-           "ep_dispatch_expert_sp", "ep_dispatch_scheduled_ctas", "ep_dispatch_scheduled",
+           "ep_dispatch_expert_sp", "ep_dispatch_expert_sw", "ep_dispatch_scheduled_ctas", "ep_dispatch_scheduled",
            "ep_route", "ep_layout", "ep_dispatch", "ep_combine", "ep_layout_static")
 # Size of the device array ep_layout_static uses instead of a workspace (include/ep.h).
 EP_LAYOUT_STATIC_SCRATCH_BYTES = 1 << 20
@@ -87,6 +87,7 @@ def _load() -> ctypes.CDLL:
     lib.ep_sentinel_arm.argtypes = [cfgp, vp, vp]
     lib.ep_expert_scale.argtypes = [cfgp, vp, vp, vp, vp, vp]
     lib.ep_dispatch_expert_sp.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.ep_dispatch_expert_sw.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_uint32, vp]
     lib.ep_dispatch_scheduled_ctas.argtypes = [cfgp, P(ctypes.c_int32)]
     lib.ep_dispatch_scheduled.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.ep_step_kernel_count.argtypes = [cfgp, P(ctypes.c_int32)]
@@ -103,7 +104,7 @@ def _load() -> ctypes.CDLL:
     lib.ep_combine.argtypes = [cfgp, vp, vp, vp, vp, vp]
     for f in ("ep_dispatch_fused_workspace_size", "ep_dispatch_fused", "ep_fused_step_kernel_count",
               "ep_check_bounded_wait", "ep_sentinel_arm", "ep_expert_scale", "ep_dispatch_expert_sp",
-              "ep_dispatch_scheduled_ctas", "ep_dispatch_scheduled",
+              "ep_dispatch_scheduled_ctas", "ep_dispatch_scheduled", "ep_dispatch_expert_sw",
               "ep_device_error", "ep_step_kernel_count", "ep_layout_workspace_size", "ep_schedule_capacity", "ep_route", "ep_layout",
               "ep_dispatch", "ep_combine", "ep_layout_static"):
         getattr(lib, f).restype = ctypes.c_int
@@ -340,6 +341,24 @@ def ep_dispatch_expert_sp(cfg: EpConfig, x, slot, expert_offset, expert_scale, c
            "ep_dispatch_expert_sp")
 
 
+def ep_dispatch_expert_sw(cfg: EpConfig, x, slot, expert_offset, expert_scale, chunks, n_chunks, worker_begin,
+                          send, slot_meta, y, row_flag, epoch: int, stream=None) -> None:
+    """Stop-and-wait handoff: per-row flag released after the row lands (row_flag int32 [T*k])."""
+    T, H, E, k = cfg.T, cfg.H, cfg.E, cfg.k
+    _check(_lib.ep_dispatch_expert_sw(ctypes.byref(cfg), _ptr(x, torch.bfloat16, (T, H), "x"),
+                                      _ptr(slot, torch.int32, (T, k), "slot"),
+                                      _ptr(expert_offset, torch.int32, (E + 1,), "expert_offset"),
+                                      _ptr(expert_scale, torch.float32, (E,), "expert_scale"),
+                                      _ptr(chunks, torch.int32, None, "chunks"),
+                                      _ptr(n_chunks, torch.int32, (1,), "n_chunks"),
+                                      _ptr(worker_begin, torch.int32, None, "worker_begin"),
+                                      _ptr(send, torch.bfloat16, (T * k, H), "send"),
+                                      _ptr(slot_meta, torch.int32, (T * k,), "slot_meta"),
+                                      _ptr(y, torch.bfloat16, (T * k, H), "y"),
+                                      _ptr(row_flag, torch.int32, (T * k,), "row_flag"),
+                                      ctypes.c_uint32(epoch & 0xFFFFFFFF), _stream(stream)), "ep_dispatch_expert_sw")
+
+
 def ep_dispatch(cfg: EpConfig, x, slot, send, slot_meta, stream=None) -> None:
     """x bf16 [T, H] -> send bf16 [T*k, H], slot_meta int32 [T*k]."""
     T, H, k = cfg.T, cfg.H, cfg.k
@@ -443,6 +462,12 @@ class LayerBuffers:
         """dispatch + per-expert scale in one kernel; send must be armed."""
         ep_dispatch_expert_sp(self.cfg, self.x, self.slot, self.expert_offset, expert_scale, self.chunks,
                               self.n_chunks, self.worker_begin, self.send, self.slot_meta, self.y, stream)
+
+    def dispatch_expert_sw(self, expert_scale, row_flag, epoch: int, stream=None):
+        """dispatch + per-expert scale in one kernel, rows handed over by per-row flags."""
+        ep_dispatch_expert_sw(self.cfg, self.x, self.slot, self.expert_offset, expert_scale, self.chunks,
+                              self.n_chunks, self.worker_begin, self.send, self.slot_meta, self.y, row_flag, epoch,
+                              stream)
 
     def bind(self, stream=None) -> "BoundLayer":
         """Pre-marshalled C calls on this layer's buffers (same entry points,

@@ -342,6 +342,32 @@ ep_status ep_dispatch_expert_sp(const ep_config *cfg, const ep_bf16 *x, const in
     return from_cuda(e);
 }
 
+ep_status ep_dispatch_expert_sw(const ep_config *cfg, const ep_bf16 *x, const int32_t *slot,
+                                const int32_t *expert_offset, const float *expert_scale, const ep_chunk *chunks,
+                                const int32_t *n_chunks, const int32_t *worker_begin, ep_bf16 *send,
+                                int32_t *slot_meta, ep_bf16 *y, uint32_t *row_flag, uint32_t epoch,
+                                cudaStream_t stream) {
+    ep_status st = check_config(cfg);
+    if (st != EP_OK) return st;
+    if ((st = check_rows(cfg)) != EP_OK) return st;
+    if ((st = check_schedule(cfg)) != EP_OK) return st;
+    if (cfg->T == 0) return EP_OK;
+    if (!x || !slot || !expert_offset || !expert_scale || !chunks || !n_chunks || !worker_begin || !send ||
+        !slot_meta || !y || !row_flag)
+        return EP_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(send) || !aligned16(y) || (reinterpret_cast<uintptr_t>(slot) & 15u) ||
+        (reinterpret_cast<uintptr_t>(row_flag) & 3u))
+        return EP_ERR_INVALID_ARG;
+    if (cfg->k % 4 != 0 || cfg->H * 2 < 1024 || cfg->H * 2 > 48 * 1024) return EP_ERR_UNSUPPORTED;
+    int32_t W = 0;
+    if ((st = resolve_workers(cfg, &W)) != EP_OK) return st;
+    const cudaError_t e = ep::launch_dispatch_expert_sw(*cfg, W, x, slot, expert_offset, expert_scale, chunks,
+                                                        n_chunks, worker_begin, send, slot_meta, y, row_flag, epoch,
+                                                        stream);
+    if (e == cudaErrorNotSupported) return EP_ERR_UNSUPPORTED;
+    return from_cuda(e);
+}
+
 ep_status ep_dispatch(const ep_config *cfg, const ep_bf16 *x, const int32_t *slot, ep_bf16 *send,
                       int32_t *slot_meta, cudaStream_t stream) {
     ep_status st = check_config(cfg);

@@ -195,6 +195,11 @@ cudaError_t launch_dispatch_expert_sp(const ep_config &c, int32_t W, const ep_bf
                                       const int32_t *expert_offset, const float *scale, const ep_chunk *chunks,
                                       const int32_t *n_chunks, const int32_t *worker_begin, ep_bf16 *send,
                                       int32_t *meta, ep_bf16 *y, cudaStream_t s);
+cudaError_t launch_dispatch_expert_sw(const ep_config &c, int32_t W, const ep_bf16 *x, const int32_t *slot,
+                                      const int32_t *expert_offset, const float *scale, const ep_chunk *chunks,
+                                      const int32_t *n_chunks, const int32_t *worker_begin, ep_bf16 *send,
+                                      int32_t *meta, ep_bf16 *y, unsigned *row_flag, unsigned epoch,
+                                      cudaStream_t s);
 
 // Fused route + layout + dispatch (fused.cu).
 size_t fused_workspace_bytes(const ep_config &c);

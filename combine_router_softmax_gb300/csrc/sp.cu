@@ -105,9 +105,21 @@ struct SpArgs {
     char *send;
     int32_t *meta;
     char *y;
+    unsigned *row_flag;  // stop-and-wait only: [T k] epoch of each row's flag
     int32_t *err;
     int32_t T, H, E, k, W, row_pad;
+    unsigned epoch;
 };
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_u32(unsigned *p, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 
 // Expert that owns row s: the e with eoff[e] <= s < eoff[e + 1] (empty experts skipped).
 __device__ __forceinline__ int owner_expert(const int32_t *eoff, int32_t E, int64_t s) {
@@ -125,6 +137,11 @@ __device__ __forceinline__ int owner_expert(const int32_t *eoff, int32_t E, int6
 // concatenated chunk rows round-robin, so each worker's rows are polled by
 // many warps at once and each warp walks its rows in the order they arrive
 // (token order inside an expert's segment).
+// kSW = false: Data-as-Flag by sentinel polling. kSW = true: the stop-and-wait
+// baseline of the same section -- the producer lane waits until its row has
+// landed, then releases the row's flag (the epoch); the consumer acquires the
+// flag, then reads the row; nothing is re-armed.
+template <bool kSW>
 __global__ void __launch_bounds__(kSpThreads, 4) dispatch_expert_sp_kernel(SpArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     const int lane = threadIdx.x & 31;
@@ -163,11 +180,19 @@ __global__ void __launch_bounds__(kSpThreads, 4) dispatch_expert_sp_kernel(SpArg
             const unsigned char *st = smem + (size_t)s * stage_bytes;
             if (lane < a.k) {
                 const int sv = reinterpret_cast<const int32_t *>(st + a.row_pad)[lane];
-                if (sv >= 0 && (int64_t)sv < rows) {
+                const bool valid = sv >= 0 && (int64_t)sv < rows;
+                if (valid) {
                     bulk_s2g(a.send + (int64_t)sv * row_bytes, st, (uint32_t)row_bytes);
                     a.meta[sv] = (int32_t)(t * a.k + lane);
                 }
                 bulk_commit();
+                if (kSW && valid) {
+                    // the row has landed (writes done), is ordered before this
+                    // thread's generic accesses, and only then is flagged
+                    bulk_wait<0>();
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                    st_release_u32(a.row_flag + sv, a.epoch);
+                }
             }
             if (i >= 1 && i - 1 + kSpStages < n) {
                 if (lane < a.k) bulk_wait_read<1>();
@@ -223,6 +248,30 @@ __global__ void __launch_bounds__(kSpThreads, 4) dispatch_expert_sp_kernel(SpArg
             const int64_t s = rb + (p - acc);
             const float sc = __ldg(a.scale + owner_expert(s_eoff, a.E, s));
             const uint4 *src = send4 + s * hv;
+            if (kSW) {
+                bool got = false;
+                for (uint32_t polls = 0; polls <= kSpMaxPolls; ++polls) {
+                    if (ld_acquire_u32(a.row_flag + s) == a.epoch) {
+                        got = true;
+                        break;
+                    }
+                    __nanosleep(64);
+                }
+                if (__all_sync(0xffffffffu, got)) {
+                    for (int v0 = lane; v0 < hv; v0 += kSpUnroll * 32) {
+                        uint4 val[kSpUnroll];
+#pragma unroll
+                        for (int u = 0; u < kSpUnroll; ++u)
+                            if (v0 + 32 * u < hv) val[u] = ld_relaxed_v4(src + v0 + 32 * u);
+#pragma unroll
+                        for (int u = 0; u < kSpUnroll; ++u)
+                            if (v0 + 32 * u < hv) st_v4(y4 + s * hv + v0 + 32 * u, scale8(val[u], sc));
+                    }
+                } else {
+                    ok = false;
+                }
+                continue;
+            }
             // Probe one vector (the row's last, which the bulk store writes
             // last or near it) until the payload shows: early polls then touch
             // one sector instead of pulling the whole sentinel row from HBM,
@@ -308,11 +357,15 @@ cudaError_t launch_expert_scale(const ep_config &c, const ep_bf16 *send, const i
     return cudaGetLastError();
 }
 
+namespace {
+
 // EP_ERR_UNSUPPORTED-style refusal is signalled by cudaErrorNotSupported.
-cudaError_t launch_dispatch_expert_sp(const ep_config &c, int32_t W, const ep_bf16 *x, const int32_t *slot,
-                                      const int32_t *expert_offset, const float *scale, const ep_chunk *chunks,
-                                      const int32_t *n_chunks, const int32_t *worker_begin, ep_bf16 *send,
-                                      int32_t *meta, ep_bf16 *y, cudaStream_t s) {
+
+template <bool kSW>
+cudaError_t launch_handoff(const ep_config &c, int32_t W, const ep_bf16 *x, const int32_t *slot,
+                           const int32_t *expert_offset, const float *scale, const ep_chunk *chunks,
+                           const int32_t *n_chunks, const int32_t *worker_begin, ep_bf16 *send, int32_t *meta,
+                           ep_bf16 *y, unsigned *row_flag, unsigned epoch, cudaStream_t s) {
     if (c.T == 0) return cudaSuccess;
     const int32_t row_bytes = c.H * 2;
     if (c.k % 4 != 0 || row_bytes < 1024 || row_bytes > 48 * 1024) return cudaErrorNotSupported;
@@ -321,14 +374,15 @@ cudaError_t launch_dispatch_expert_sp(const ep_config &c, int32_t W, const ep_bf
     if (e != cudaSuccess) return e;
     static bool attr_set[kMaxDevices_] = {false};
     if (!attr_set[dev]) {
-        if ((e = cudaFuncSetAttribute(dispatch_expert_sp_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if ((e = cudaFuncSetAttribute(dispatch_expert_sp_kernel<kSW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       110 * 1024)) != cudaSuccess)
             return e;
         attr_set[dev] = true;
     }
     const int row_pad = (row_bytes + 127) & ~127;
     const size_t smem = sp_smem(row_pad, c.E);
-    const int occ = max_blocks_per_sm(reinterpret_cast<const void *>(dispatch_expert_sp_kernel), kSpThreads, smem);
+    const int occ =
+        max_blocks_per_sm(reinterpret_cast<const void *>(dispatch_expert_sp_kernel<kSW>), kSpThreads, smem);
     const int64_t G = (int64_t)sm_count(dev) * occ;  // all co-resident: consumers wait on producers
     if (G < 1 || G * kSpConsumerWarps < W) return cudaErrorNotSupported;
     SpArgs a;
@@ -342,6 +396,8 @@ cudaError_t launch_dispatch_expert_sp(const ep_config &c, int32_t W, const ep_bf
     a.send = reinterpret_cast<char *>(send);
     a.meta = meta;
     a.y = reinterpret_cast<char *>(y);
+    a.row_flag = row_flag;
+    a.epoch = epoch;
     if ((e = sp_error_word(&a.err)) != cudaSuccess) return e;
     a.T = c.T;
     a.H = c.H;
@@ -350,8 +406,27 @@ cudaError_t launch_dispatch_expert_sp(const ep_config &c, int32_t W, const ep_bf
     a.W = W;
     a.row_pad = row_pad;
     void *args[] = {&a};
-    return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(dispatch_expert_sp_kernel),
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(dispatch_expert_sp_kernel<kSW>),
                                        dim3((unsigned)G), dim3(kSpThreads), args, smem, s);
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch_expert_sp(const ep_config &c, int32_t W, const ep_bf16 *x, const int32_t *slot,
+                                      const int32_t *expert_offset, const float *scale, const ep_chunk *chunks,
+                                      const int32_t *n_chunks, const int32_t *worker_begin, ep_bf16 *send,
+                                      int32_t *meta, ep_bf16 *y, cudaStream_t s) {
+    return launch_handoff<false>(c, W, x, slot, expert_offset, scale, chunks, n_chunks, worker_begin, send, meta, y,
+                                 nullptr, 0u, s);
+}
+
+cudaError_t launch_dispatch_expert_sw(const ep_config &c, int32_t W, const ep_bf16 *x, const int32_t *slot,
+                                      const int32_t *expert_offset, const float *scale, const ep_chunk *chunks,
+                                      const int32_t *n_chunks, const int32_t *worker_begin, ep_bf16 *send,
+                                      int32_t *meta, ep_bf16 *y, unsigned *row_flag, unsigned epoch,
+                                      cudaStream_t s) {
+    return launch_handoff<true>(c, W, x, slot, expert_offset, scale, chunks, n_chunks, worker_begin, send, meta, y,
+                                row_flag, epoch, s);
 }
 
 }  // namespace ep

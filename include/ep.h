@@ -316,6 +316,26 @@ ep_status ep_dispatch_scheduled(const ep_config *cfg, const ep_bf16 *x, const in
  */
 #define EP_SENTINEL_BF16 0xFFFFu
 
+/*
+ * ep_dispatch_expert_sw -- the stop-and-wait baseline the same section
+ * measures Data-as-Flag against (write data, then a completion flag; the
+ * receiver polls the flag, then consumes the data), in the same
+ * producer/consumer kernel as ep_dispatch_expert_sp: a producer lane waits
+ * until its row has landed, then release-stores `epoch` into row_flag[s]; a
+ * consumer acquire-polls row_flag[s] == epoch and then reads the row. send is
+ * left holding the payload (nothing to re-arm). Outputs and requirements are
+ * those of ep_dispatch_expert_sp; additionally
+ *   row_flag : uint32 [T k] device, 4-byte aligned, holding no `epoch` on
+ *              entry (e.g. zero-filled once, epoch = 1, 2, ... per call);
+ *              holds `epoch` for every row on return.
+ * A CTA that gives up a bounded wait sets ep_device_error bit 2 (4).
+ */
+ep_status ep_dispatch_expert_sw(const ep_config *cfg, const ep_bf16 *x, const int32_t *slot,
+                                const int32_t *expert_offset, const float *expert_scale,
+                                const ep_chunk *chunks, const int32_t *n_chunks, const int32_t *worker_begin,
+                                ep_bf16 *send, int32_t *slot_meta, ep_bf16 *y, uint32_t *row_flag,
+                                uint32_t epoch, cudaStream_t stream);
+
 ep_status ep_sentinel_arm(const ep_config *cfg, ep_bf16 *send, cudaStream_t stream);
 
 ep_status ep_expert_scale(const ep_config *cfg, const ep_bf16 *send, const int32_t *expert_offset,

@@ -148,3 +148,60 @@ def test_sentinel_polling_unsupported_shapes(ep):
         assert ei.value.status == ep.EP_ERR_UNSUPPORTED
     torch.cuda.synchronize()
     assert ep.ep_device_error() == 0
+
+
+# ---------------------------------------------------------------------------
+# stop-and-wait baseline (per-row flags)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("w", SP, ids=lambda w: w.name)
+def test_stop_and_wait_vs_oracle(ep, orc, w):
+    b, r = setup_layer(ep, orc, w)
+    rows = w.T * w.k
+    flag = torch.zeros(rows, dtype=torch.int32, device="cuda")
+    b.slot_meta.fill_(-7)
+    b.y.fill_(0)
+    b.send.fill_(0)
+    b.dispatch_expert_sw(expert_scales(w.E), flag, 1)
+    torch.cuda.synchronize()
+    assert ep.ep_device_error() == 0
+    assert np.array_equal(bf16_from_dev(b.y), r["y"]), "expert output differs"
+    assert np.array_equal(bf16_from_dev(b.send), r["send"]), "send differs"
+    assert np.array_equal(b.slot_meta.cpu().numpy(), r["meta"][:rows])
+    assert (flag.cpu().numpy() == 1).all()
+
+
+def test_stop_and_wait_epochs_and_graphs(ep, orc):
+    """New inputs under new epochs; two captured graphs with alternating
+    epochs replayed in turn, as the benchmark runs them."""
+    w = ep_synth.CONFIGS["decode"].with_(name="decode-T64", T=64)
+    b, _ = setup_layer(ep, orc, w)
+    scale = expert_scales(w.E)
+    flag = torch.zeros(w.T * w.k, dtype=torch.int32, device="cuda")
+    offs = b.expert_offset.cpu().numpy()
+    for epoch in (1, 2, 0xFFFFFFFF):
+        x = ep_synth.hidden_bf16_bits(w.seed + epoch % 97, w.T, w.H)
+        b.x.copy_(bf16_to_dev(x))
+        b.dispatch_expert_sw(scale, flag, epoch)
+        torch.cuda.synchronize()
+        assert ep.ep_device_error() == 0
+        send_ref, _ = orc.dispatch(x, b.slot.cpu().numpy())
+        assert np.array_equal(bf16_from_dev(b.y), orc.expert(send_ref, offs, w.E)), f"epoch {epoch}"
+    s = torch.cuda.Stream()
+    graphs = []
+    for epoch in (1, 2):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                b.dispatch_expert_sw(scale, flag, epoch, stream=s)
+        graphs.append(g)
+    send_ref, _ = orc.dispatch(ep_synth.hidden_bf16_bits(w.seed + 2, w.T, w.H), b.slot.cpu().numpy())
+    y_ref = orc.expert(send_ref, offs, w.E)
+    b.x.copy_(bf16_to_dev(ep_synth.hidden_bf16_bits(w.seed + 2, w.T, w.H)))
+    for i in range(6):
+        b.y.fill_(0)
+        graphs[i % 2].replay()
+        torch.cuda.synchronize()
+        assert ep.ep_device_error() == 0
+        assert np.array_equal(bf16_from_dev(b.y), y_ref)
+        assert (flag.cpu().numpy() == (1 if i % 2 == 0 else 2)).all()
