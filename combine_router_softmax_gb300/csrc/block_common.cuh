@@ -75,6 +75,53 @@ __device__ __forceinline__ int cta_exclusive_scan32(int x, int *s_warp, int *tot
     return base + inc - x;
 }
 
+// A set of whole warps of one CTA that works as a unit: thread tid of nthr
+// (warp-aligned, tid = threadIdx.x - first thread), synchronised by named
+// barrier BAR (0: the whole CTA with __syncthreads). The barrier id is a
+// compile-time constant so that a kernel reserves only the barriers it uses.
+template <int BAR>
+struct ThreadGroup {
+    int tid, nthr;
+    __device__ __forceinline__ void sync() const {
+        if (BAR == 0)
+            __syncthreads();
+        else
+            asm volatile("bar.sync %0, %1;" ::"n"(BAR), "r"(nthr) : "memory");
+    }
+};
+
+__device__ __forceinline__ ThreadGroup<0> whole_cta() { return ThreadGroup<0>{(int)threadIdx.x, (int)blockDim.x}; }
+
+// cta_exclusive_scan32 over a ThreadGroup.
+template <int BAR>
+__device__ __forceinline__ int group_exclusive_scan32(int x, int *s_warp, int *total, const ThreadGroup<BAR> &g) {
+    const int lane = g.tid & 31;
+    const int warp = g.tid >> 5;
+    const int nwarps = g.nthr >> 5;
+    int inc = x;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, inc, d);
+        if (lane >= d) inc += o;
+    }
+    if (lane == 31) s_warp[warp] = inc;
+    g.sync();
+    if (warp == 0) {
+        int wv = lane < nwarps ? s_warp[lane] : 0;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, wv, d);
+            if (lane >= d) wv += o;
+        }
+        if (lane < nwarps) s_warp[lane] = wv;
+    }
+    g.sync();
+    const int base = warp > 0 ? s_warp[warp - 1] : 0;
+    *total = s_warp[nwarps - 1];
+    g.sync();
+    return base + inc - x;
+}
+
 // Threads that share one expert's work in a CTA of nw warps: the largest power
 // of two <= min(32 nw / E, nw, 32), at least 1.
 __device__ __forceinline__ int threads_per_expert(int32_t E, int nw) {
@@ -199,6 +246,79 @@ __device__ __forceinline__ int32_t share_bound(int32_t N, int32_t w, int32_t W) 
     return (int32_t)((int64_t)N * w / W);
 }
 
+// The two-class chunk schedule (no pod tier), built by one whole CTA from rank
+// offsets in shared memory. Class 0 (near) is ranks [n_lo, n_hi) of
+// self_rank's node; class 1 (far) is [0, n_lo) followed by [n_hi, R). s_P (R + 2 ints of shared memory)
+// receives each class's prefix sums P_c[i] = rows in its first i ranks. A
+// worker finds the first and last rank its share touches by two quaternary
+// searches per class, counts the non-empty ranks in between, and after a CTA
+// scan over the counts writes its chunks.
+__device__ void build_schedule_two_tiers(const int32_t *s_roff, int32_t R, int32_t W, int32_t ranks_per_node,
+                                         int32_t self_rank, ep_chunk *chunks, int32_t *n_chunks,
+                                         int32_t *worker_begin, int *s_warp, int32_t *s_P) {
+    const int32_t node = self_rank / ranks_per_node;
+    const int32_t n_lo = node * ranks_per_node;
+    const int32_t n_hi = n_lo + ranks_per_node < R ? n_lo + ranks_per_node : R;
+    const int32_t n0 = n_hi - n_lo, n1 = R - n0;
+    int32_t *P1 = s_P;           // far class: n1 + 1 entries
+    int32_t *P0 = s_P + n1 + 1;  // near class: n0 + 1 entries
+    for (int32_t i = threadIdx.x; i <= n1; i += blockDim.x)
+        P1[i] = i <= n_lo ? s_roff[i] : s_roff[n_lo] + (s_roff[i + n0] - s_roff[n_hi]);
+    for (int32_t i = threadIdx.x; i <= n0; i += blockDim.x) P0[i] = s_roff[n_lo + i] - s_roff[n_lo];
+    __syncthreads();
+    const int32_t N[2] = {P0[n0], P1[n1]};
+
+    int carry = 0;
+    for (int32_t wb = 0; wb < W; wb += blockDim.x) {
+        const int32_t w = wb + (int32_t)threadIdx.x;
+        int32_t first[2] = {0, 0}, last[2] = {-1, -1}, lo[2] = {0, 0}, hi[2] = {0, 0};
+        int cnt = 0;
+        if (w < W) {
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                const int32_t *P = c ? P1 : P0;
+                const int32_t n = c ? n1 : n0;
+                lo[c] = share_bound(N[c], w, W);
+                hi[c] = share_bound(N[c], w + 1, W);
+                if (hi[c] > lo[c]) {
+                    first[c] = quaternary_search(P, n, lo[c]);
+                    last[c] = quaternary_search(P, n, hi[c] - 1);
+                    for (int32_t i = first[c]; i <= last[c]; ++i) cnt += P[i + 1] > P[i] ? 1 : 0;
+                }
+            }
+        }
+        int tile_total;
+        const int pos0 = carry + cta_exclusive_scan32(cnt, s_warp, &tile_total);
+        if (w < W) {
+            worker_begin[w] = pos0;
+            int pos = pos0;
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c = 1 - cc;  // other-node traffic first
+                const int32_t *P = c ? P1 : P0;
+                for (int32_t i = first[c]; i <= last[c]; ++i) {
+                    if (P[i + 1] == P[i]) continue;
+                    const int32_t r = c ? (i < n_lo ? i : i + n0) : n_lo + i;
+                    const int32_t a = lo[c] > P[i] ? lo[c] : P[i];
+                    const int32_t bnd = hi[c] < P[i + 1] ? hi[c] : P[i + 1];
+                    ep_chunk ch;
+                    ch.worker = w;
+                    ch.hop_class = c;
+                    ch.dst_rank = r;
+                    ch.row_begin = s_roff[r] + (a - P[i]);
+                    ch.row_count = bnd - a;
+                    chunks[pos++] = ch;
+                }
+            }
+        }
+        carry += tile_total;
+    }
+    if (threadIdx.x == 0) {
+        worker_begin[W] = carry;
+        *n_chunks = carry;
+    }
+}
+
 // The ranks of one hop class: at most two runs of consecutive ranks,
 // [a0, a0 + n0) then [a1, a1 + n - n0), in ascending order.
 struct ClassRuns {
@@ -221,47 +341,59 @@ __device__ __forceinline__ ClassRuns class_runs(int c, int32_t R, int32_t nl, in
     return q;
 }
 
-// The chunk schedule, built by one whole CTA from rank offsets in shared
-// memory. s_P (R + 3 ints of shared memory) receives each class's prefix sums
-// P_c[i] = rows in the class's first i ranks. A worker finds the first and
-// last rank its share of each class touches by two quaternary searches,
-// counts the non-empty ranks in between, and after a CTA scan over the counts
-// writes its chunks, farthest class first.
-__device__ void cta_build_schedule(const int32_t *s_roff, int32_t R, int32_t W, HopTiers h, ep_chunk *chunks,
-                                   int32_t *n_chunks, int32_t *worker_begin, int *s_warp, int32_t *s_P) {
+// The chunk schedule, built by a group of threads from rank offsets in shared
+// memory (NC = 2 or 3 hop classes). s_P (R + 3 ints of shared memory)
+// receives each class's prefix sums P_c[i] = rows in the class's first i
+// ranks. A worker finds the first and last rank its share of each class
+// touches by two quaternary searches, counts the non-empty ranks in between,
+// and after a group scan over the counts writes its chunks, farthest class
+// first. Used for three classes; the two-class table has its own builder
+// above, which measured faster inside the layout and fused kernels (this one,
+// inlined there or called, cost them 2-4 us more).
+template <int NC, int BAR>
+__device__ __noinline__ void build_schedule_nc(const int32_t *s_roff, int32_t R, int32_t W, HopTiers h,
+                                               ep_chunk *chunks, int32_t *n_chunks, int32_t *worker_begin,
+                                               int *s_warp, int32_t *s_P, ThreadGroup<BAR> g) {
     const int32_t nl = h.self_rank / h.ranks_per_node * h.ranks_per_node;
     const int32_t nh = nl + h.ranks_per_node < R ? nl + h.ranks_per_node : R;
-    const int32_t pl = h.ranks_per_pod > 0 ? h.self_rank / h.ranks_per_pod * h.ranks_per_pod : 0;
-    const int32_t ph = h.ranks_per_pod > 0 ? (pl + h.ranks_per_pod < R ? pl + h.ranks_per_pod : R) : R;
-    ClassRuns q[3];
-    int32_t *P[3];
+    const int32_t pl = NC == 3 ? h.self_rank / h.ranks_per_pod * h.ranks_per_pod : 0;
+    const int32_t ph = NC == 3 ? (pl + h.ranks_per_pod < R ? pl + h.ranks_per_pod : R) : R;
+    ClassRuns q[NC];
+    int32_t *P[NC];
     int32_t base = 0;
 #pragma unroll
-    for (int c = 0; c < 3; ++c) {
+    for (int c = 0; c < NC; ++c) {
         q[c] = class_runs(c, R, nl, nh, pl, ph);
         P[c] = s_P + base;
         base += q[c].n + 1;
     }
 #pragma unroll
-    for (int c = 0; c < 3; ++c) {
+    for (int c = 0; c < NC; ++c) {
         const ClassRuns qc = q[c];
-        for (int32_t i = threadIdx.x; i <= qc.n; i += blockDim.x)
+        for (int32_t i = g.tid; i <= qc.n; i += g.nthr)
             P[c][i] = i <= qc.n0 ? s_roff[qc.a0 + i] - s_roff[qc.a0]
                                  : (s_roff[qc.a0 + qc.n0] - s_roff[qc.a0]) + (s_roff[qc.a1 + (i - qc.n0)] - s_roff[qc.a1]);
     }
-    __syncthreads();
-    int32_t N[3];
+    g.sync();
+    int32_t N[NC];
 #pragma unroll
-    for (int c = 0; c < 3; ++c) N[c] = P[c][q[c].n];
+    for (int c = 0; c < NC; ++c) N[c] = P[c][q[c].n];
 
     int carry = 0;
-    for (int32_t wb = 0; wb < W; wb += blockDim.x) {
-        const int32_t w = wb + (int32_t)threadIdx.x;
-        int32_t first[3] = {0, 0, 0}, last[3] = {-1, -1, -1}, lo[3] = {0, 0, 0}, hi[3] = {0, 0, 0};
+    for (int32_t wb = 0; wb < W; wb += g.nthr) {
+        const int32_t w = wb + (int32_t)g.tid;
+        int32_t first[NC], last[NC], lo[NC], hi[NC];
         int cnt = 0;
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            first[c] = 0;
+            last[c] = -1;
+            lo[c] = 0;
+            hi[c] = 0;
+        }
         if (w < W) {
 #pragma unroll
-            for (int c = 0; c < 3; ++c) {
+            for (int c = 0; c < NC; ++c) {
                 lo[c] = share_bound(N[c], w, W);
                 hi[c] = share_bound(N[c], w + 1, W);
                 if (hi[c] > lo[c]) {
@@ -272,12 +404,12 @@ __device__ void cta_build_schedule(const int32_t *s_roff, int32_t R, int32_t W, 
             }
         }
         int tile_total;
-        const int pos0 = carry + cta_exclusive_scan32(cnt, s_warp, &tile_total);
+        const int pos0 = carry + group_exclusive_scan32(cnt, s_warp, &tile_total, g);
         if (w < W) {
             worker_begin[w] = pos0;
             int pos = pos0;
 #pragma unroll
-            for (int c = 2; c >= 0; --c) {
+            for (int c = NC - 1; c >= 0; --c) {
                 const int32_t *Pc = P[c];
                 for (int32_t i = first[c]; i <= last[c]; ++i) {
                     if (Pc[i + 1] == Pc[i]) continue;
@@ -296,10 +428,23 @@ __device__ void cta_build_schedule(const int32_t *s_roff, int32_t R, int32_t W, 
         }
         carry += tile_total;
     }
-    if (threadIdx.x == 0) {
+    if (g.tid == 0) {
         worker_begin[W] = carry;
         *n_chunks = carry;
     }
+}
+
+template <int BAR>
+__device__ __forceinline__ void cta_build_schedule(const int32_t *s_roff, int32_t R, int32_t W, HopTiers h,
+                                                   ep_chunk *chunks, int32_t *n_chunks, int32_t *worker_begin,
+                                                   int *s_warp, int32_t *s_P, ThreadGroup<BAR> g) {
+    if (h.ranks_per_pod > 0)
+        build_schedule_nc<3, BAR>(s_roff, R, W, h, chunks, n_chunks, worker_begin, s_warp, s_P, g);
+    else if (BAR == 0)
+        build_schedule_two_tiers(s_roff, R, W, h.ranks_per_node, h.self_rank, chunks, n_chunks, worker_begin, s_warp,
+                                 s_P);
+    else
+        build_schedule_nc<2, BAR>(s_roff, R, W, h, chunks, n_chunks, worker_begin, s_warp, s_P, g);
 }
 
 // ---------------------------------------------------------------------------

@@ -189,7 +189,7 @@ layout_fused_kernel(const int32_t *__restrict__ idx, int32_t T, int32_t E, int32
     if (b == nb - 1) {
         for (int r = threadIdx.x; r <= R; r += blockDim.x) s_roff[r] = s_eoff[r * epr];
         __syncthreads();
-        cta_build_schedule(s_roff, R, W, tiers, chunks, n_chunks, worker_begin, s_warp32, s_P);
+        cta_build_schedule(s_roff, R, W, tiers, chunks, n_chunks, worker_begin, s_warp32, s_P, whole_cta());
     }
 }
 
@@ -265,7 +265,7 @@ layout_scan_kernel(int32_t *__restrict__ block_counts, int32_t nb, int32_t E, in
     // (c) chunk schedule.
     __shared__ int s_warp32[32];
     __shared__ int32_t s_P[kMaxE + 3];
-    cta_build_schedule(s_roff, R, W, tiers, chunks, n_chunks, worker_begin, s_warp32, s_P);
+    cta_build_schedule(s_roff, R, W, tiers, chunks, n_chunks, worker_begin, s_warp32, s_P, whole_cta());
 }
 
 __global__ void __launch_bounds__(256)
