@@ -164,8 +164,9 @@ __global__ void __launch_bounds__(kFusedThreads) dispatch_fused_kernel(FusedArgs
     const int ppw = np > 0 ? (np + kFusedWarps - 1) / kFusedWarps : 1;
     cta_rank_pairs(tile_e, np, ppw, E, cnt, tile_r, a.counts + (int64_t)b * E, 1);
 
-    // C.
-    bool ok = grid_barrier(&a.sync[0], (unsigned)a.nb);
+    // C. (a single CTA needs no grid barrier: after a CTA barrier its own
+    // global writes are visible to all its threads)
+    bool ok = a.nb > 1 ? grid_barrier(&a.sync[0], (unsigned)a.nb) : (__syncthreads(), true);
 
     // D. column scan: CTA b owns experts b, b + nb, ...; all their counts over
     // every tile are read in one batch, then scanned over the tiles.
@@ -208,7 +209,7 @@ __global__ void __launch_bounds__(kFusedThreads) dispatch_fused_kernel(FusedArgs
             }
         }
         // E.
-        ok = grid_barrier(&a.sync[1], (unsigned)a.nb);
+        ok = a.nb > 1 ? grid_barrier(&a.sync[1], (unsigned)a.nb) : (__syncthreads(), true);
     }
 
     if (ok) {
