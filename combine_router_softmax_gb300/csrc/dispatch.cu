@@ -134,25 +134,37 @@ dispatch_bulk_kernel(const char *__restrict__ x, const int32_t *__restrict__ slo
     }
     __syncwarp();
 
-    auto load = [&](int s, int64_t t) {
-        unsigned char *st = smem + (size_t)s * stage_bytes;
+    auto load_row = [&](int s, int64_t t) {
         mbar_arrive_expect_tx(&bar[s], (uint32_t)row_bytes + 4u * (uint32_t)k);
-        bulk_g2s(st, x + t * row_bytes, (uint32_t)row_bytes, &bar[s]);
-        bulk_g2s(st + row_pad, slot + t * k, 4u * (uint32_t)k, &bar[s]);
+        bulk_g2s(smem + (size_t)s * stage_bytes, x + t * row_bytes, (uint32_t)row_bytes, &bar[s]);
+    };
+    auto load_slots = [&](int s, int64_t t) {
+        bulk_g2s(smem + (size_t)s * stage_bytes + row_pad, slot + t * k, 4u * (uint32_t)k, &bar[s]);
+    };
+    auto load = [&](int s, int64_t t) {
+        load_row(s, t);
+        load_slots(s, t);
     };
 
     // Tokens per round: static stride, or grabbed from the shared counter
     // (NS at once for the first rounds, then one per refill, one refill ahead).
+    // The first rounds' x rows are requested before waiting for the grid that
+    // writes the slots (the layout, when launched right after it); their
+    // slots after.
     unsigned nxt = 0;
     if (lane == 0) {
         const int64_t c0 = dyn ? (int64_t)atomicAdd(ctr, (unsigned)NS) : 0;
         for (int s = 0; s < NS; ++s) {
             const int64_t t = dyn ? c0 + s : (s < n ? first + s * G : T);
             s_tok[s] = t < T ? t : -1;
-            if (t < T) load(s, t);
+            if (t < T) load_row(s, t);
         }
         if (dyn) nxt = atomicAdd(ctr, 1u);
     }
+    grid_dependency_wait();
+    if (lane == 0)
+        for (int s = 0; s < NS; ++s)
+            if (s_tok[s] >= 0) load_slots(s, s_tok[s]);
     __syncwarp();
 
     bool ok = true;
@@ -212,7 +224,7 @@ int bulk_stages(int32_t row_bytes) {
 }
 
 cudaError_t launch_bulk(const ep_config &c, const ep_bf16 *x, const int32_t *slot, ep_bf16 *send, int32_t *meta,
-                        cudaStream_t s, unsigned *ctr, bool ctr_zeroed) {
+                        cudaStream_t s, unsigned *ctr, bool ctr_zeroed, bool after_layout) {
     const int32_t row_bytes = c.H * 2;
     const int32_t row_pad = (row_bytes + 127) & ~127;
     const int32_t stage_bytes = row_pad + 128;
@@ -237,10 +249,19 @@ cudaError_t launch_bulk(const ep_config &c, const ep_bf16 *x, const int32_t *slo
         e = cudaMemsetAsync(ctr, 0, sizeof(unsigned), s);
         if (e != cudaSuccess) return e;
     }
-    dispatch_bulk_kernel<<<(unsigned)grid, 32, smem, s>>>(reinterpret_cast<const char *>(x), slot,
-                                                          reinterpret_cast<char *>(send), meta, c.T, c.k, row_bytes,
-                                                          row_pad, stage_bytes, NS, (int64_t)c.T * c.k, err, ctr);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = after_layout ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, dispatch_bulk_kernel, reinterpret_cast<const char *>(x), slot,
+                              reinterpret_cast<char *>(send), meta, c.T, c.k, row_bytes, row_pad, stage_bytes, NS,
+                              (int64_t)c.T * c.k, err, ctr);
 }
 
 }  // namespace
@@ -270,9 +291,9 @@ static bool use_bulk(const ep_config &c, const int32_t *slot) {
 }
 
 cudaError_t launch_dispatch(const ep_config &c, const ep_bf16 *x, const int32_t *slot, ep_bf16 *send,
-                            int32_t *meta, cudaStream_t s, unsigned *ctr, bool ctr_zeroed) {
+                            int32_t *meta, cudaStream_t s, unsigned *ctr, bool ctr_zeroed, bool after_layout) {
     if (c.T == 0) return cudaSuccess;
-    if (use_bulk(c, slot)) return launch_bulk(c, x, slot, send, meta, s, ctr, ctr_zeroed);
+    if (use_bulk(c, slot)) return launch_bulk(c, x, slot, send, meta, s, ctr, ctr_zeroed, after_layout);
     switch (c.k) {
         case 1: return launch_k<1>(c, x, slot, send, meta, s);
         case 2: return launch_k<2>(c, x, slot, send, meta, s);

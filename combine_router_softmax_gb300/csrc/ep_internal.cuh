@@ -72,8 +72,12 @@ int layout_kernel_count(const ep_config &c);
 
 // ctr: optional device counter (4 bytes) for dynamic token assignment, zeroed
 // here unless ctr_zeroed.
+// after_layout: the launch follows the layout kernel in the same stream and may
+// start while it runs (programmatic dependent launch; the kernel loads x rows
+// first and reads the slots only after griddepcontrol.wait).
 cudaError_t launch_dispatch(const ep_config &c, const ep_bf16 *x, const int32_t *slot, ep_bf16 *send,
-                            int32_t *meta, cudaStream_t s, unsigned *ctr = nullptr, bool ctr_zeroed = false);
+                            int32_t *meta, cudaStream_t s, unsigned *ctr = nullptr, bool ctr_zeroed = false,
+                            bool after_layout = false);
 
 cudaError_t launch_combine(const ep_config &c, const ep_bf16 *y, const int32_t *slot, const float *w,
                            ep_bf16 *out, cudaStream_t s);
@@ -133,6 +137,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Bounded wait on one mbarrier phase: false if it did not complete in time.
+// Programmatic dependent launch. griddepcontrol.wait returns once the grids
+// this one depends on have completed and their memory is visible (at once when
+// there are none); launch_dependents lets the dependent grid start early.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint32_t max_polls) {
     for (uint32_t i = 0; i < max_polls; ++i) {
         if (mbar_try_wait(bar, parity)) return true;

@@ -460,7 +460,7 @@ cudaError_t launch_dispatch_fused(const ep_config &c, int32_t W, const float *lo
         e = launch_layout(c, W, topk_idx, expert_count, expert_offset, rank_count, rank_offset, slot, chunks,
                           n_chunks, worker_begin, workspace, s, true);
         if (e != cudaSuccess) return e;
-        return launch_dispatch(c, x, slot, send, meta, s, ctr, true);
+        return launch_dispatch(c, x, slot, send, meta, s, ctr, true, true);
     }
     FusedArgs a;
     a.logits = logits;

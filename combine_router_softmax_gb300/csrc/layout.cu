@@ -85,6 +85,9 @@ layout_fused_kernel(const int32_t *__restrict__ idx, int32_t T, int32_t E, int32
                     int32_t *__restrict__ n_chunks, int32_t *__restrict__ worker_begin, int32_t W,
                     HopTiers tiers) {
     extern __shared__ int32_t sm[];
+    // A dispatch launched after this kernel may start now and fetch x rows
+    // (it waits for this grid before it reads a slot).
+    grid_launch_dependents();
     const int nw = blockDim.x >> 5;
     int32_t *cnt = sm;                         // [nw][E]
     int32_t *tile_e = cnt + nw * E;            // [nw][32 k]
@@ -271,6 +274,7 @@ layout_scan_kernel(int32_t *__restrict__ block_counts, int32_t nb, int32_t E, in
 __global__ void __launch_bounds__(256)
 layout_finalize_kernel(const int32_t *__restrict__ idx, const int32_t *__restrict__ block_base,
                        int32_t *__restrict__ slot, int64_t npairs, int32_t k, int32_t E, int32_t nb) {
+    grid_launch_dependents();  // as in layout_fused_kernel
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < npairs; i += stride) {
         const int e = __ldg(idx + i);
