@@ -42,6 +42,7 @@ template <int K, int U>
 __global__ void __launch_bounds__(kCombineThreads)
 combine_kernel(const uint4 *__restrict__ y, const int32_t *__restrict__ slot, const float *__restrict__ w,
                uint4 *__restrict__ out, int32_t hv, int32_t segs, int64_t units, int64_t rows) {
+    grid_dependency_wait();  // launched as a programmatic dependent: nothing is touched before this
     const int lane = threadIdx.x & 31;
     const int64_t gwarp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarp = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -94,6 +95,7 @@ combine_kernel(const uint4 *__restrict__ y, const int32_t *__restrict__ slot, co
 __global__ void __launch_bounds__(kCombineThreads)
 combine_kernel_rt(const uint4 *__restrict__ y, const int32_t *__restrict__ slot, const float *__restrict__ w,
                   uint4 *__restrict__ out, int32_t k, int32_t hv, int32_t segs, int64_t units, int64_t rows) {
+    grid_dependency_wait();
     constexpr int U = 2;
     const int lane = threadIdx.x & 31;
     const int64_t gwarp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -154,10 +156,9 @@ cudaError_t launch_ku(const ep_config &c, const ep_bf16 *y, const int32_t *slot,
     const int32_t segs = (hv + 32 * U - 1) / (32 * U);
     const int64_t units = (int64_t)c.T * segs;
     const int grid = grid_for(reinterpret_cast<const void *>(combine_kernel<K, U>), units);
-    combine_kernel<K, U><<<grid, kCombineThreads, 0, s>>>(reinterpret_cast<const uint4 *>(y), slot, w,
-                                                          reinterpret_cast<uint4 *>(out), hv, segs, units,
-                                                          (int64_t)c.T * c.k);
-    return cudaGetLastError();
+    return launch_dependent(combine_kernel<K, U>, dim3(grid), dim3(kCombineThreads), 0, s,
+                            reinterpret_cast<const uint4 *>(y), slot, w, reinterpret_cast<uint4 *>(out), hv, segs,
+                            units, (int64_t)c.T * c.k);
 }
 
 }  // namespace
@@ -177,10 +178,9 @@ cudaError_t launch_combine(const ep_config &c, const ep_bf16 *y, const int32_t *
     const int32_t segs = (hv + 63) / 64;
     const int64_t units = (int64_t)c.T * segs;
     const int grid = grid_for(reinterpret_cast<const void *>(combine_kernel_rt), units);
-    combine_kernel_rt<<<grid, kCombineThreads, 0, s>>>(reinterpret_cast<const uint4 *>(y), slot, w,
-                                                       reinterpret_cast<uint4 *>(out), c.k, hv, segs, units,
-                                                       (int64_t)c.T * c.k);
-    return cudaGetLastError();
+    return launch_dependent(combine_kernel_rt, dim3(grid), dim3(kCombineThreads), 0, s,
+                            reinterpret_cast<const uint4 *>(y), slot, w, reinterpret_cast<uint4 *>(out), c.k, hv,
+                            segs, units, (int64_t)c.T * c.k);
 }
 
 }  // namespace ep

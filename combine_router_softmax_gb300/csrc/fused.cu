@@ -265,7 +265,9 @@ __global__ void __launch_bounds__(kFusedThreads) dispatch_fused_kernel(FusedArgs
         atomicExch(a.n_chunks, -1);
     }
 
-    // G. dispatch the tile
+    // G. dispatch the tile (a combine launched after this kernel may get ready;
+    // it waits for this grid before it touches memory)
+    grid_launch_dependents();
     const int64_t rows = (int64_t)a.T * k;
     if (a.ns > 0) {
         if (warp != 0) return;
