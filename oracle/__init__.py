@@ -80,7 +80,12 @@ class Oracle:
         L.orc_f32_to_bf16.restype = ctypes.c_uint16
         L.orc_bf16_to_f32.argtypes = [ctypes.c_uint16]
         L.orc_bf16_to_f32.restype = ctypes.c_float
-        for f in ("orc_route", "orc_layout", "orc_schedule", "orc_dispatch", "orc_combine", "orc_expert_scale"):
+        L.orc_tff_encode.argtypes = [i64, i64, P(ctypes.c_uint8), ctypes.c_uint32, P(ctypes.c_uint8)]
+        L.orc_tff_decode.argtypes = [i64, i64, P(ctypes.c_uint8), ctypes.c_uint32, P(ctypes.c_uint8), P(i64)]
+        L.orc_tff_blocks_per_row.argtypes = [i64]
+        L.orc_tff_blocks_per_row.restype = i64
+        for f in ("orc_route", "orc_layout", "orc_schedule", "orc_dispatch", "orc_combine", "orc_expert_scale",
+                  "orc_tff_encode", "orc_tff_decode"):
             getattr(L, f).restype = ctypes.c_int
 
     @staticmethod
@@ -168,6 +173,29 @@ class Oracle:
                                               _ptr(send_bits, ctypes.c_uint16), _ptr(y, ctypes.c_uint16)),
                     "orc_expert_scale")
         return y
+
+    # -- Token-Flag Fusion block codec (orc_tff_encode / orc_tff_decode) ----
+    def tff_blocks_per_row(self, row_bytes: int) -> int:
+        return int(self.lib.orc_tff_blocks_per_row(row_bytes))
+
+    def tff_encode(self, rows_u8: np.ndarray, epoch: int) -> np.ndarray:
+        """rows uint8 [R, row_bytes] -> framed uint8 [R, blocks * 512]."""
+        rows_u8 = np.ascontiguousarray(rows_u8, dtype=np.uint8)
+        R, nbytes = rows_u8.shape
+        framed = np.full((R, self.tff_blocks_per_row(nbytes) * 512), 0xAB, np.uint8)
+        self._check(self.lib.orc_tff_encode(R, nbytes, _ptr(rows_u8, ctypes.c_uint8), epoch & 0xFFFFFFFF,
+                                            _ptr(framed, ctypes.c_uint8)), "orc_tff_encode")
+        return framed
+
+    def tff_decode(self, framed: np.ndarray, row_bytes: int, epoch: int, out: np.ndarray | None = None):
+        """framed uint8 [R, blocks * 512] -> (rows uint8 [R, row_bytes], bad block count)."""
+        framed = np.ascontiguousarray(framed, dtype=np.uint8)
+        R = framed.shape[0]
+        out = np.zeros((R, row_bytes), np.uint8) if out is None else np.ascontiguousarray(out, dtype=np.uint8)
+        bad = ctypes.c_int64(0)
+        self._check(self.lib.orc_tff_decode(R, row_bytes, _ptr(framed, ctypes.c_uint8), epoch & 0xFFFFFFFF,
+                                            _ptr(out, ctypes.c_uint8), ctypes.byref(bad)), "orc_tff_decode")
+        return out, bad.value
 
     def f32_to_bf16(self, f: float) -> int:
         return int(self.lib.orc_f32_to_bf16(ctypes.c_float(f)))

@@ -386,3 +386,95 @@ int orc_expert_scale(int64_t rows, int32_t H, int32_t E, const int32_t *expert_o
     }
     return ORC_OK;
 }
+
+/* ------------------------------------------------------------------------- */
+/* Data-as-Flag: the Token-Flag Fusion block codec.                           */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * "Data-as-Flag" / TFF (UBEP article): each 512-byte block carries 32 bytes
+ * of synchronization metadata and 480 bytes of token payload, so the flag
+ * travels with the data. The pages give the split, not the fields; the
+ * plainest reading, in the order the pages list the two parts:
+ *
+ *   block = [ metadata 32 B | payload 480 B ]
+ *   metadata = uint32 { epoch, row, block, nbytes, 0, 0, 0, 0 }
+ *     epoch : the flag (the value the receiver waits for)
+ *     row   : the send-buffer row the block belongs to
+ *     block : its index inside the row
+ *     nbytes: payload bytes it carries (480, or the row's remainder)
+ *   payload = row bytes [480 block, 480 block + nbytes), zero after nbytes.
+ *
+ * A row of row_bytes bytes takes ceil(row_bytes / 480) blocks; row r's
+ * blocks are consecutive and rows follow each other. Integers are stored
+ * little-endian.
+ */
+#define ORC_TFF_BLOCK 512
+#define ORC_TFF_META 32
+#define ORC_TFF_PAYLOAD 480
+
+int64_t orc_tff_blocks_per_row(int64_t row_bytes)
+{
+    return (row_bytes + ORC_TFF_PAYLOAD - 1) / ORC_TFF_PAYLOAD;
+}
+
+static void orc_put_u32(unsigned char *p, uint32_t v)
+{
+    p[0] = (unsigned char)(v & 0xFFu);
+    p[1] = (unsigned char)((v >> 8) & 0xFFu);
+    p[2] = (unsigned char)((v >> 16) & 0xFFu);
+    p[3] = (unsigned char)((v >> 24) & 0xFFu);
+}
+
+static uint32_t orc_get_u32(const unsigned char *p)
+{
+    return (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) | ((uint32_t)p[3] << 24);
+}
+
+int orc_tff_encode(int64_t rows, int64_t row_bytes, const unsigned char *in, uint32_t epoch,
+                   unsigned char *framed)
+{
+    if (rows < 0 || row_bytes <= 0) return ORC_EINVAL;
+    const int64_t nblk = orc_tff_blocks_per_row(row_bytes);
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t b = 0; b < nblk; ++b) {
+            unsigned char *blk = framed + (r * nblk + b) * ORC_TFF_BLOCK;
+            const int64_t off = b * ORC_TFF_PAYLOAD;
+            const int64_t n = row_bytes - off < ORC_TFF_PAYLOAD ? row_bytes - off : ORC_TFF_PAYLOAD;
+            memset(blk, 0, ORC_TFF_BLOCK);
+            orc_put_u32(blk + 0, epoch);
+            orc_put_u32(blk + 4, (uint32_t)r);
+            orc_put_u32(blk + 8, (uint32_t)b);
+            orc_put_u32(blk + 12, (uint32_t)n);
+            memcpy(blk + ORC_TFF_META, in + r * row_bytes + off, (size_t)n);
+        }
+    return ORC_OK;
+}
+
+/*
+ * The receiver's side: a block is accepted when its metadata reads
+ * {epoch, row, block, nbytes} as the encoder wrote them; its payload is then
+ * copied to the row. Blocks that do not match are counted in *bad and their
+ * bytes are left as they were in `out`.
+ */
+int orc_tff_decode(int64_t rows, int64_t row_bytes, const unsigned char *framed, uint32_t epoch,
+                   unsigned char *out, int64_t *bad)
+{
+    if (rows < 0 || row_bytes <= 0 || !bad) return ORC_EINVAL;
+    const int64_t nblk = orc_tff_blocks_per_row(row_bytes);
+    int64_t nbad = 0;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t b = 0; b < nblk; ++b) {
+            const unsigned char *blk = framed + (r * nblk + b) * ORC_TFF_BLOCK;
+            const int64_t off = b * ORC_TFF_PAYLOAD;
+            const int64_t n = row_bytes - off < ORC_TFF_PAYLOAD ? row_bytes - off : ORC_TFF_PAYLOAD;
+            if (orc_get_u32(blk + 0) != epoch || orc_get_u32(blk + 4) != (uint32_t)r ||
+                orc_get_u32(blk + 8) != (uint32_t)b || orc_get_u32(blk + 12) != (uint32_t)n) {
+                nbad += 1;
+                continue;
+            }
+            memcpy(out + r * row_bytes + off, blk + ORC_TFF_META, (size_t)n);
+        }
+    *bad = nbad;
+    return ORC_OK;
+}

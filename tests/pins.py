@@ -376,4 +376,72 @@ def pin_expert_scale(o):
     assert np.array_equal(o.expert(send, offset, E, identity=True), send)
 
 
+# ---------------------------------------------------------------------------
+# Token-Flag Fusion block codec
+# ---------------------------------------------------------------------------
+
+def _tff_rows(case):
+    if "rows_hex" in case:
+        return np.stack([np.frombuffer(bytes.fromhex(h), np.uint8) for h in case["rows_hex"]])
+    n = case["row_bytes"]
+    return (np.arange(n) % 251).astype(np.uint8)[None, :]
+
+
+def pin_tff_golden(o):
+    """Hand-worked frames (tests/golden/tff_small.json): metadata words, payload, zero fill."""
+    d = json.loads((GOLDEN / "tff_small.json").read_text())
+    for c in d["cases"]:
+        rows = _tff_rows(c)
+        framed = o.tff_encode(rows, c["epoch"])
+        nblk = len([b for b in c["blocks"] if b["row"] == 0])
+        assert framed.shape == (rows.shape[0], 512 * nblk), c["name"]
+        for b in c["blocks"]:
+            blk = framed[b["row"], 512 * b["block"]:512 * (b["block"] + 1)]
+            assert blk[:32].tobytes() == bytes.fromhex(b["meta_hex"]), (c["name"], b)
+            pay = bytes.fromhex(b["payload_hex"]) if "payload_hex" in b else \
+                rows[b["row"], b["payload_from"]:b["payload_from"] + b["payload_len"]].tobytes()
+            assert blk[32:32 + len(pay)].tobytes() == pay, (c["name"], b)
+            assert not blk[32 + len(pay):].any(), (c["name"], b)
+        back, bad = o.tff_decode(framed, c["row_bytes"], c["epoch"])
+        assert bad == 0 and np.array_equal(back, rows)
+
+
+def pin_tff_roundtrip_and_size(o):
+    """decode(encode(rows)) == rows with no bad block; a row takes the fewest
+    480-byte payloads that hold it (one fewer would not)."""
+    g = _rng(16)
+    for n in (2, 16, 478, 480, 482, 960, 14336, 4096 * 2, 24576 * 2):
+        rows = g.integers(0, 256, size=(3, n), dtype=np.uint8)
+        framed = o.tff_encode(rows, 0xFFFFFFFF)
+        nblk = framed.shape[1] // 512
+        assert framed.shape[1] % 512 == 0 and nblk * 480 >= n and (nblk - 1) * 480 < n
+        back, bad = o.tff_decode(framed, n, 0xFFFFFFFF)
+        assert bad == 0 and np.array_equal(back, rows)
+
+
+def pin_tff_rejects_stale_blocks(o):
+    """A block whose epoch, row, block index or length does not match is
+    counted and its bytes are not copied; every other block still is."""
+    g = _rng(17)
+    n = 1000  # 3 blocks per row
+    rows = g.integers(0, 256, size=(4, n), dtype=np.uint8)
+    framed = o.tff_encode(rows, 9)
+    hits = [(0, 0, 0, 8), (1, 2, 4, 3), (2, 1, 8, 7), (3, 2, 12, 1)]  # (row, block, metadata byte, new value)
+    for r, b, byte, v in hits:
+        framed[r, 512 * b + byte] = v
+    sentinel = np.full((4, n), 0xEE, np.uint8)
+    back, bad = o.tff_decode(framed, n, 9, out=sentinel)
+    assert bad == len(hits)
+    for r in range(4):
+        for b in range(3):
+            lo, hi = 480 * b, min(480 * (b + 1), n)
+            want = sentinel[r, lo:hi] if any(h[0] == r and h[1] == b for h in hits) else rows[r, lo:hi]
+            if any(h[0] == r and h[1] == b for h in hits):
+                assert (back[r, lo:hi] == 0xEE).all()
+            else:
+                assert np.array_equal(back[r, lo:hi], want)
+    _, bad_epoch = o.tff_decode(o.tff_encode(rows, 9), n, 10)
+    assert bad_epoch == 4 * 3
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

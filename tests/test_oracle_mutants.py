@@ -56,6 +56,14 @@ MUTANTS = [
     ("combine drops the last term",
      "            for (int32_t j = 0; j < k; ++j) {\n                int64_t s = slot[t * k + j];\n                if (s < 0 || s >= T * k) return ORC_EINVAL;\n                acc",
      "            for (int32_t j = 0; j < k - 1; ++j) {\n                int64_t s = slot[t * k + j];\n                if (s < 0 || s >= T * k) return ORC_EINVAL;\n                acc"),
+    ("TFF payload written over the metadata",
+     "memcpy(blk + ORC_TFF_META, in + r * row_bytes + off, (size_t)n);", "memcpy(blk, in + r * row_bytes + off, (size_t)n);"),
+    ("TFF last block claims a full payload",
+     "            orc_put_u32(blk + 12, (uint32_t)n);", "            orc_put_u32(blk + 12, (uint32_t)ORC_TFF_PAYLOAD);"),
+    ("TFF decoder ignores the row field",
+     "orc_get_u32(blk + 4) != (uint32_t)r ||", "0 ||"),
+    ("TFF block index off by one",
+     "            orc_put_u32(blk + 8, (uint32_t)b);", "            orc_put_u32(blk + 8, (uint32_t)(b + 1));"),
     ("bf16 ties rounded away from zero",
      "if (low > 0x8000u || (low == 0x8000u && (keep & 1u)))", "if (low >= 0x8000u)"),
     ("bf16 truncation",
