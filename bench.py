@@ -71,6 +71,8 @@ def parse_args(argv=None):
     p.add_argument("--schedule-ablation", action="store_true",
                    help="also time the dispatch pulled by the chunk schedule under three tables (latency-"
                         "homogenized, one class, whole ranks per worker) beside the token-major dispatch")
+    p.add_argument("--tff", action="store_true",
+                   help="also time the Token-Flag Fusion block codec (encode and decode of the send buffer)")
     p.add_argument("--separate", action="store_true",
                    help="step = ep_route, ep_layout, ep_dispatch, ep_combine (default: ep_dispatch_fused, ep_combine)")
     return p.parse_args(argv)
@@ -603,6 +605,55 @@ def e2e_pipelined(ep, buf, cfg, device, fused: bool, use_graph: bool, h_logits, 
     return {"total_ms": t0.elapsed_time(t1)}
 
 
+def tff_leg(ep, buf, w, device, flush_l2, K: int) -> dict:
+    """The Token-Flag Fusion codec on this step's send buffer: ep_tff_encode
+    (rows -> 512-byte blocks of 32 B metadata + 480 B payload) and
+    ep_tff_decode (back, checking every block's flag), each captured in a CUDA
+    graph and replayed K times with L2 flushed in between. Reports the framed
+    size over the payload size (the codec's bandwidth overhead) and each
+    kernel's bytes moved per second."""
+    import torch
+
+    cfg = buf.cfg
+    nbytes = ep.ep_tff_framed_bytes(cfg)
+    framed = torch.empty((nbytes,), dtype=torch.uint8, device=device)
+    rows_back = torch.empty_like(buf.send)
+    bad = torch.zeros(1, dtype=torch.int32, device=device)
+    cap = torch.cuda.Stream(device)
+    cap.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(cap):
+        buf.dispatch(cap)
+        ep.ep_tff_encode(cfg, buf.send, framed, 1, cap)
+        ep.ep_tff_decode(cfg, framed, 1, rows_back, bad, cap)
+    cap.synchronize()
+    same = bool(torch.equal(rows_back.view(torch.int16), buf.send.view(torch.int16))) and int(bad.item()) == 0
+    stream = torch.cuda.current_stream(device)
+    out = {}
+    for name, fn in (("encode", lambda: ep.ep_tff_encode(cfg, buf.send, framed, 2, cap)),
+                     ("decode", lambda: ep.ep_tff_decode(cfg, framed, 2, rows_back, bad, cap))):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            fn()
+        for _ in range(3):
+            flush_l2()
+            g.replay()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for a, b_ in ev:
+            flush_l2()
+            a.record(stream)
+            g.replay()
+            b_.record(stream)
+        torch.cuda.synchronize()
+        us = 1e3 * sum(a.elapsed_time(b_) for a, b_ in ev) / K
+        moved = nbytes + buf.send.numel() * 2
+        out[name + "_us"] = round(us, 2)
+        out[name + "_gbs"] = round(moved / (us * 1e-6) / 1e9, 1)
+    out.update({"payload_bytes": buf.send.numel() * 2, "framed_bytes": nbytes,
+                "overhead": round(nbytes / (buf.send.numel() * 2), 4), "roundtrip_exact": same,
+                "bad_blocks": int(bad.item()), "steps": K})
+    return out
+
+
 def run_gb300(args):
     import numpy as np
     import torch
@@ -802,6 +853,8 @@ def run_gb300(args):
     }
     if args.schedule_ablation:
         line["schedule_ablation"] = schedule_ablation_leg(ep, buf, w, device, flush_l2, min(K, 500))
+    if args.tff:
+        line["tff"] = tff_leg(ep, buf, w, device, flush_l2, min(K, 500))
     if args.data_as_flag:
         line["data_as_flag"] = data_as_flag_leg(ep, buf, w, device, flush_l2, min(K, 500))
     if rank == 0 and not args.no_cpu_baseline:

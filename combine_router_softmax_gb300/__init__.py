@@ -29,6 +29,7 @@ EXPORTS = ("ep_status_string", "ep_version", "ep_device_error", "ep_step_kernel_
            "ep_layout_workspace_size", "ep_dispatch_fused_workspace_size", "ep_schedule_capacity",
            "ep_dispatch_fused", "ep_check_bounded_wait", "ep_sentinel_arm", "ep_expert_scale",
            "ep_dispatch_expert_sp", "ep_dispatch_expert_sw", "ep_dispatch_scheduled_ctas", "ep_dispatch_scheduled",
+           "ep_tff_framed_bytes", "ep_tff_encode", "ep_tff_decode",
            "ep_route", "ep_layout", "ep_dispatch", "ep_combine", "ep_layout_static")
 # Size of the device array ep_layout_static uses instead of a workspace (include/ep.h).
 EP_LAYOUT_STATIC_SCRATCH_BYTES = 1 << 20
@@ -89,6 +90,9 @@ def _load() -> ctypes.CDLL:
     lib.ep_dispatch_expert_sp.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.ep_dispatch_expert_sw.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_uint32, vp]
     lib.ep_dispatch_scheduled_ctas.argtypes = [cfgp, P(ctypes.c_int32)]
+    lib.ep_tff_framed_bytes.argtypes = [cfgp, P(ctypes.c_size_t)]
+    lib.ep_tff_encode.argtypes = [cfgp, vp, vp, ctypes.c_uint32, vp]
+    lib.ep_tff_decode.argtypes = [cfgp, vp, ctypes.c_uint32, vp, vp, vp]
     lib.ep_dispatch_scheduled.argtypes = [cfgp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
     lib.ep_step_kernel_count.argtypes = [cfgp, P(ctypes.c_int32)]
     lib.ep_fused_step_kernel_count.argtypes = [cfgp, P(ctypes.c_int32)]
@@ -105,6 +109,7 @@ def _load() -> ctypes.CDLL:
     for f in ("ep_dispatch_fused_workspace_size", "ep_dispatch_fused", "ep_fused_step_kernel_count",
               "ep_check_bounded_wait", "ep_sentinel_arm", "ep_expert_scale", "ep_dispatch_expert_sp",
               "ep_dispatch_scheduled_ctas", "ep_dispatch_scheduled", "ep_dispatch_expert_sw",
+              "ep_tff_framed_bytes", "ep_tff_encode", "ep_tff_decode",
               "ep_device_error", "ep_step_kernel_count", "ep_layout_workspace_size", "ep_schedule_capacity", "ep_route", "ep_layout",
               "ep_dispatch", "ep_combine", "ep_layout_static"):
         getattr(lib, f).restype = ctypes.c_int
@@ -304,6 +309,30 @@ def ep_dispatch_scheduled(cfg: EpConfig, x, slot, chunks, n_chunks, worker_begin
                                       _ptr(send, torch.bfloat16, (T * k, H), "send"),
                                       _ptr(slot_meta, torch.int32, (T * k,), "slot_meta"), ns, _stream(stream)),
            "ep_dispatch_scheduled")
+
+
+EP_TFF_BLOCK_BYTES = 512
+
+
+def ep_tff_framed_bytes(cfg: EpConfig) -> int:
+    n = ctypes.c_size_t(0)
+    _check(_lib.ep_tff_framed_bytes(ctypes.byref(cfg), ctypes.byref(n)), "ep_tff_framed_bytes")
+    return n.value
+
+
+def ep_tff_encode(cfg: EpConfig, rows, framed, epoch: int, stream=None) -> None:
+    """rows bf16 [T*k, H] -> framed uint8 [ep_tff_framed_bytes] of 512-byte blocks."""
+    _check(_lib.ep_tff_encode(ctypes.byref(cfg), _ptr(rows, torch.bfloat16, (cfg.T * cfg.k, cfg.H), "rows"),
+                              _ptr(framed, torch.uint8, (ep_tff_framed_bytes(cfg),), "framed"),
+                              ctypes.c_uint32(epoch & 0xFFFFFFFF), _stream(stream)), "ep_tff_encode")
+
+
+def ep_tff_decode(cfg: EpConfig, framed, epoch: int, rows, bad_blocks, stream=None) -> None:
+    """framed -> rows bf16 [T*k, H]; rejected blocks are added to bad_blocks (int32 [1])."""
+    _check(_lib.ep_tff_decode(ctypes.byref(cfg), _ptr(framed, torch.uint8, (ep_tff_framed_bytes(cfg),), "framed"),
+                              ctypes.c_uint32(epoch & 0xFFFFFFFF),
+                              _ptr(rows, torch.bfloat16, (cfg.T * cfg.k, cfg.H), "rows"),
+                              _ptr(bad_blocks, torch.int32, (1,), "bad_blocks"), _stream(stream)), "ep_tff_decode")
 
 
 EP_SENTINEL_BF16 = 0xFFFF

@@ -299,6 +299,39 @@ ep_status ep_dispatch_scheduled(const ep_config *cfg, const ep_bf16 *x, const in
     return from_cuda(e);
 }
 
+ep_status ep_tff_framed_bytes(const ep_config *cfg, size_t *bytes) {
+    ep_status st = check_config(cfg);
+    if (st != EP_OK) return st;
+    if ((st = check_rows(cfg)) != EP_OK) return st;
+    if (!bytes) return EP_ERR_INVALID_ARG;
+    *bytes = (size_t)cfg->T * (size_t)cfg->k * (size_t)ep::tff_blocks_per_row(*cfg) * EP_TFF_BLOCK_BYTES;
+    return EP_OK;
+}
+
+ep_status ep_tff_encode(const ep_config *cfg, const ep_bf16 *rows, void *framed, uint32_t epoch,
+                        cudaStream_t stream) {
+    ep_status st = check_config(cfg);
+    if (st != EP_OK) return st;
+    if ((st = check_rows(cfg)) != EP_OK) return st;
+    if (cfg->T == 0) return EP_OK;
+    if (!rows || !framed || !aligned16(rows) || !aligned16(framed)) return EP_ERR_INVALID_ARG;
+    if ((int64_t)cfg->T * cfg->k * ep::tff_blocks_per_row(*cfg) > INT32_MAX) return EP_ERR_UNSUPPORTED;
+    return from_cuda(ep::launch_tff_encode(*cfg, rows, framed, epoch, stream));
+}
+
+ep_status ep_tff_decode(const ep_config *cfg, const void *framed, uint32_t epoch, ep_bf16 *rows,
+                        uint32_t *bad_blocks, cudaStream_t stream) {
+    ep_status st = check_config(cfg);
+    if (st != EP_OK) return st;
+    if ((st = check_rows(cfg)) != EP_OK) return st;
+    if (cfg->T == 0) return EP_OK;
+    if (!rows || !framed || !bad_blocks || !aligned16(rows) || !aligned16(framed) ||
+        (reinterpret_cast<uintptr_t>(bad_blocks) & 3u))
+        return EP_ERR_INVALID_ARG;
+    if ((int64_t)cfg->T * cfg->k * ep::tff_blocks_per_row(*cfg) > INT32_MAX) return EP_ERR_UNSUPPORTED;
+    return from_cuda(ep::launch_tff_decode(*cfg, framed, epoch, rows, bad_blocks, stream));
+}
+
 ep_status ep_sentinel_arm(const ep_config *cfg, ep_bf16 *send, cudaStream_t stream) {
     ep_status st = check_config(cfg);
     if (st != EP_OK) return st;

@@ -216,6 +216,13 @@ cudaError_t launch_dispatch_scheduled(const ep_config &c, int32_t W, const ep_bf
                                       const ep_chunk *chunks, const int32_t *n_chunks, const int32_t *worker_begin,
                                       ep_bf16 *send, int32_t *meta, int64_t *cta_ns, cudaStream_t s);
 
+// Data-as-Flag by Token-Flag Fusion: the 512-byte block codec (tff.cu).
+int64_t tff_blocks_per_row(const ep_config &c);
+cudaError_t launch_tff_encode(const ep_config &c, const ep_bf16 *rows, void *framed, unsigned epoch,
+                              cudaStream_t s);
+cudaError_t launch_tff_decode(const ep_config &c, const void *framed, unsigned epoch, ep_bf16 *rows,
+                              unsigned *bad, cudaStream_t s);
+
 // Data-as-Flag by sentinel polling (sp.cu).
 cudaError_t launch_sentinel_arm(const ep_config &c, ep_bf16 *send, cudaStream_t s);
 cudaError_t launch_expert_scale(const ep_config &c, const ep_bf16 *send, const int32_t *expert_offset,

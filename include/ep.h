@@ -287,6 +287,41 @@ ep_status ep_dispatch_scheduled(const ep_config *cfg, const ep_bf16 *x, const in
                                 ep_bf16 *send, int32_t *slot_meta, int64_t *cta_ns, cudaStream_t stream);
 
 /*
+ * Data-as-Flag by Token-Flag Fusion (the UBEP article, "Data-as-Flag", TFF):
+ * the 512-byte block codec.
+ *
+ * Each send row (T k rows of H bf16) travels as ceil(2 H / 480) blocks of 512
+ * bytes: 32 bytes of metadata, then 480 bytes of payload (zero after the
+ * row's last byte). Metadata: uint32 little-endian {epoch, row, block,
+ * nbytes, 0, 0, 0, 0}, where epoch is the flag the receiver waits for, row
+ * the send row, block the index inside the row and nbytes the payload bytes
+ * the block carries. Row r's blocks are consecutive; rows follow each other.
+ *
+ * ep_tff_framed_bytes : bytes of the framed buffer, T k ceil(2H/480) 512.
+ * ep_tff_encode       : rows [T k, H] -> framed. Every block's payload and
+ *                       metadata are stored before its epoch word, which is a
+ *                       release store (the GPU has no 512-byte atomic store).
+ * ep_tff_decode       : framed -> rows [T k, H]. A block is accepted when its
+ *                       metadata reads exactly {epoch, row, block, nbytes}
+ *                       (epoch acquire-loaded first); its payload is copied to
+ *                       the row. Rejected blocks leave their row bytes as
+ *                       they were and are added to *bad_blocks (uint32 in
+ *                       device memory, accumulated, not cleared).
+ * framed and rows 16-byte aligned; T k ceil(2H/480) <= INT32_MAX.
+ */
+#define EP_TFF_BLOCK_BYTES 512
+#define EP_TFF_META_BYTES 32
+#define EP_TFF_PAYLOAD_BYTES 480
+
+ep_status ep_tff_framed_bytes(const ep_config *cfg, size_t *bytes);
+
+ep_status ep_tff_encode(const ep_config *cfg, const ep_bf16 *rows, void *framed, uint32_t epoch,
+                        cudaStream_t stream);
+
+ep_status ep_tff_decode(const ep_config *cfg, const void *framed, uint32_t epoch, ep_bf16 *rows,
+                        uint32_t *bad_blocks, cudaStream_t stream);
+
+/*
  * Data-as-Flag by Sentinel Polling (the UBEP article, "Data-as-Flag" / SP).
  *
  * The receiver fills its buffer with a sentinel no payload can take, the
