@@ -1,8 +1,9 @@
 // ep_internal.cuh -- shared declarations of the CUDA side of the C ABI.
 //
-// Kernels live in route.cu, layout.cu, dispatch.cu and combine.cu; each file
-// exposes one host launcher declared here. The C entry points in ep_api.cu
-// validate arguments, then call the launchers.
+// Kernels live in route.cu, layout.cu, dispatch.cu, combine.cu, fused.cu,
+// gather.cu, sp.cu and tff.cu; each file exposes its host launchers, declared
+// here. The C entry points in ep_api.cu validate arguments, then call the
+// launchers.
 #pragma once
 
 #include <cstddef>
@@ -136,7 +137,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait on one mbarrier phase: false if it did not complete in time.
 // Programmatic dependent launch. griddepcontrol.wait returns once the grids
 // this one depends on have completed and their memory is visible (at once when
 // there are none); launch_dependents lets the dependent grid start early.
@@ -162,6 +162,7 @@ cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, si
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// Bounded wait on one mbarrier phase: false if it did not complete in time.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint32_t max_polls) {
     for (uint32_t i = 0; i < max_polls; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -177,6 +178,36 @@ __device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src, uint32
             smem_u32(dst_smem)),
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
+}
+
+// L2 cache policies for the bulk copies' cache hints: keep (lines likely to be
+// read again soon) or evict first (lines written once and not read back soon).
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// bulk_g2s with an L2 cache policy for the source lines.
+__device__ __forceinline__ void bulk_g2s_hint(void *dst_smem, const void *src, uint32_t bytes, uint64_t *bar,
+                                              uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+            "r"(smem_u32(dst_smem)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+// bulk_s2g (below) with an L2 cache policy for the destination lines.
+__device__ __forceinline__ void bulk_s2g_hint(void *dst, const void *src_smem, uint32_t bytes, uint64_t policy) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(dst),
+                 "r"(smem_u32(src_smem)), "r"(bytes), "l"(policy)
+                 : "memory");
 }
 
 // shared -> global bulk copy, tracked by this thread's bulk groups.

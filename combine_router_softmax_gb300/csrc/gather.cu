@@ -102,12 +102,15 @@ __global__ void __launch_bounds__(32) dispatch_gather_kernel(GatherArgs a) {
             }
             __syncwarp();
             if (lane == 0) {
+                // x rows are read k times: ask L2 to keep them; send rows are
+                // written once: let them go first
+                const uint64_t keep = l2_policy_evict_last(), drop = l2_policy_evict_first();
                 auto load = [&](int i) {
                     const uint32_t g = used + (uint32_t)i;
                     const int st = (int)(g % (uint32_t)a.stages);
                     mbar_arrive_expect_tx(&bar[st], (uint32_t)a.row_bytes);
-                    bulk_g2s(smem + (size_t)st * a.row_pad, a.x + (int64_t)s_src[i] * a.row_bytes,
-                             (uint32_t)a.row_bytes, &bar[st]);
+                    bulk_g2s_hint(smem + (size_t)st * a.row_pad, a.x + (int64_t)s_src[i] * a.row_bytes,
+                                  (uint32_t)a.row_bytes, &bar[st], keep);
                 };
                 const int pre = n < a.stages ? n : a.stages;
                 for (int i = 0; i < pre; ++i) load(i);
@@ -119,8 +122,8 @@ __global__ void __launch_bounds__(32) dispatch_gather_kernel(GatherArgs a) {
                         ok = false;
                         break;
                     }
-                    bulk_s2g(a.send + (int64_t)s_row[i] * a.row_bytes, smem + (size_t)st * a.row_pad,
-                             (uint32_t)a.row_bytes);
+                    bulk_s2g_hint(a.send + (int64_t)s_row[i] * a.row_bytes, smem + (size_t)st * a.row_pad,
+                                  (uint32_t)a.row_bytes, drop);
                     bulk_commit();
                     // the stage of row i - 1 is free once its store has read it
                     if (i >= 1 && i - 1 + a.stages < n) {
