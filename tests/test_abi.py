@@ -149,3 +149,48 @@ def test_binding_rejects_cpu_tensors(lib):
     with pytest.raises(TypeError):
         lib.ep_route(cfg, torch.zeros((4, 8), dtype=torch.float64), torch.zeros((4, 2), dtype=torch.int32),
                      torch.zeros((4, 2)))
+
+
+U = ctypes.c_void_p(0x10008)  # 8-byte aligned, not 16
+
+
+def test_tff_framed_bytes(lib):
+    """T k ceil(2H / 480) blocks of 512 bytes."""
+    n = ctypes.c_size_t(0)
+    for T, H, k, blocks in ((64, 256, 2, 2), (3, 7168, 8, 30), (5, 240, 2, 1), (1, 8, 1, 1), (2, 24576, 4, 103)):
+        cfg = _cfg(lib, T=T, H=H, k=k)
+        assert lib._lib.ep_tff_framed_bytes(ctypes.byref(cfg), ctypes.byref(n)) == lib.EP_OK
+        assert n.value == T * k * blocks * 512
+    assert lib._lib.ep_tff_framed_bytes(ctypes.byref(_cfg(lib, H=12)), ctypes.byref(n)) == lib.EP_ERR_UNSUPPORTED
+
+
+def test_added_entry_points_reject_bad_arguments(lib):
+    L = lib._lib
+    cfg = _cfg(lib, H=1024, k=4)
+    bad = lib.EP_ERR_INVALID_ARG
+    # TFF codec: null or misaligned buffers
+    assert L.ep_tff_encode(ctypes.byref(cfg), None, FAKE, 1, None) == bad
+    assert L.ep_tff_encode(ctypes.byref(cfg), U, FAKE, 1, None) == bad
+    assert L.ep_tff_decode(ctypes.byref(cfg), FAKE, 1, FAKE, None, None) == bad
+    assert L.ep_tff_decode(ctypes.byref(cfg), FAKE, 1, FAKE, ctypes.c_void_p(0x10002), None) == bad
+    # sentinel arm / expert scale
+    assert L.ep_sentinel_arm(ctypes.byref(cfg), None, None) == bad
+    assert L.ep_sentinel_arm(ctypes.byref(cfg), U, None) == bad
+    assert L.ep_expert_scale(ctypes.byref(cfg), FAKE, None, FAKE, FAKE, None) == bad
+    # producer/consumer handoffs: null tables, misaligned slot, unsupported shapes
+    args = [FAKE] * 10
+    assert L.ep_dispatch_expert_sp(ctypes.byref(cfg), *args[:5], None, *args[6:], None) == bad
+    assert L.ep_dispatch_expert_sp(ctypes.byref(cfg), FAKE, U, *args[2:], None) == bad
+    assert L.ep_dispatch_expert_sp(ctypes.byref(_cfg(lib, H=1024, k=2)), *args, None) == lib.EP_ERR_UNSUPPORTED
+    assert L.ep_dispatch_expert_sp(ctypes.byref(_cfg(lib, H=256, k=4)), *args, None) == lib.EP_ERR_UNSUPPORTED
+    assert L.ep_dispatch_expert_sw(ctypes.byref(cfg), *args, None, 1, None) == bad
+    assert L.ep_dispatch_expert_sw(ctypes.byref(cfg), *args, ctypes.c_void_p(0x10002), 1, None) == bad
+    assert L.ep_dispatch_expert_sw(ctypes.byref(_cfg(lib, H=1024, k=6)), *args, FAKE, 1, None) == \
+        lib.EP_ERR_UNSUPPORTED
+    # schedule-driven dispatch: null pointers, misaligned cta_ns, rows above 48 KiB
+    assert L.ep_dispatch_scheduled(ctypes.byref(cfg), None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == bad
+    assert L.ep_dispatch_scheduled(ctypes.byref(cfg), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                   ctypes.c_void_p(0x10004), None) == bad
+    big = _cfg(lib, H=32768, k=4)
+    assert L.ep_dispatch_scheduled(ctypes.byref(big), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == \
+        lib.EP_ERR_UNSUPPORTED
