@@ -461,15 +461,18 @@ __device__ __forceinline__ void red_release_gpu_add(unsigned *p, unsigned v) {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// Grid barrier for co-resident CTAs: after a CTA barrier, thread 0 fences the
-// CTA's global writes, arrives with a release add and polls with acquire
-// loads. Bounded: returns false (for every thread of the CTA) if the count did
-// not arrive in time.
+// Grid barrier for co-resident CTAs: after a CTA barrier, thread 0 arrives
+// with a release add and polls with acquire loads, then a CTA barrier releases
+// the other threads. Bounded: returns false (for every thread of the CTA) if
+// the count did not arrive in time.
 __device__ bool grid_barrier(unsigned *arrivals, unsigned expected, unsigned max_polls = kBarrierSpinLimit) {
     __shared__ int s_ok;
     __syncthreads();
     if (threadIdx.x == 0) {
-        __threadfence();
+        // The CTA barrier above orders every thread's writes before this
+        // release add (release is cumulative); the acquire loads and the CTA
+        // barrier below order every thread's later reads after the wait. No
+        // separate fence is needed on either side.
         red_release_gpu_add(arrivals, 1u);
         int ok = 1;
         unsigned spins = 0;
@@ -480,7 +483,6 @@ __device__ bool grid_barrier(unsigned *arrivals, unsigned expected, unsigned max
             }
             if (spins > 64) __nanosleep(32);
         }
-        __threadfence();
         s_ok = ok;
     }
     __syncthreads();
