@@ -231,16 +231,16 @@ cudaError_t launch_bulk(const ep_config &c, const ep_bf16 *x, const int32_t *slo
     const int NS = bulk_stages(row_bytes);
     const size_t smem = (size_t)NS * stage_bytes + kBulkMaxStages * (sizeof(uint64_t) + sizeof(int64_t));
     int dev = 0;
-    cudaGetDevice(&dev);
+    cudaError_t e = current_device(&dev);
+    if (e != cudaSuccess) return e;
     static bool attr_set[kMaxDevices_] = {false};
     if (!attr_set[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(dispatch_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             200 * 1024);
+        e = cudaFuncSetAttribute(dispatch_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
     int32_t *err = nullptr;
-    cudaError_t e = dispatch_error_word(&err);
+    e = dispatch_error_word(&err);
     if (e != cudaSuccess) return e;
     const int occ = max_blocks_per_sm(reinterpret_cast<const void *>(dispatch_bulk_kernel), 32, smem);
     int64_t grid = (int64_t)sm_count(dev) * occ;

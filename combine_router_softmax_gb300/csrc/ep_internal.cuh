@@ -47,6 +47,14 @@ struct LayoutWorkspace {
 };
 LayoutWorkspace layout_workspace(const ep_config &c);
 
+// The current device's ordinal, checked against the per-device caches
+// (cudaErrorInvalidDevice beyond them).
+inline cudaError_t current_device(int *dev) {
+    const cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) return e;
+    return (*dev < 0 || *dev >= kMaxDevices_) ? cudaErrorInvalidDevice : cudaSuccess;
+}
+
 // Cached device properties (per device ordinal).
 int sm_count(int device);
 int current_device_sm_count();

@@ -199,7 +199,7 @@ cudaError_t launch_dispatch_scheduled(const ep_config &c, int32_t W, const ep_bf
 
     const GatherPlan p = plan_gather(c, W);
     int dev = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = current_device(&dev)) != cudaSuccess) return e;
     static bool attr_set[kMaxDevices_] = {false};
     if (!attr_set[dev]) {
         if ((e = cudaFuncSetAttribute(dispatch_gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -370,7 +370,7 @@ cudaError_t launch_handoff(const ep_config &c, int32_t W, const ep_bf16 *x, cons
     const int32_t row_bytes = c.H * 2;
     if (c.k % 4 != 0 || row_bytes < 1024 || row_bytes > 48 * 1024) return cudaErrorNotSupported;
     int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    cudaError_t e = current_device(&dev);
     if (e != cudaSuccess) return e;
     static bool attr_set[kMaxDevices_] = {false};
     if (!attr_set[dev]) {
