@@ -12,7 +12,7 @@
 // written once. Units are spread over a grid sized to the resident capacity
 // of the GPU, which keeps the load balanced when T is small relative to the
 // SM count and rows are long (H = 7168: 7 segments per row).
-#include "ep_internal.cuh"
+#include "block_common.cuh"
 
 namespace ep {
 namespace {
@@ -118,13 +118,27 @@ __global__ void __launch_bounds__(32)
 dispatch_bulk_kernel(const char *__restrict__ x, const int32_t *__restrict__ slot, char *__restrict__ send,
                      int32_t *__restrict__ meta, int32_t T, int32_t k, int32_t row_bytes, int32_t row_pad,
                      int32_t stage_bytes, int32_t NS, int64_t rows, int32_t *__restrict__ err,
-                     unsigned *__restrict__ ctr) {
+                     unsigned *__restrict__ ctr, ScheduleTask st, int32_t sched_on) {
     extern __shared__ __align__(128) unsigned char smem[];
+    const int lane = threadIdx.x;
+    if (sched_on && blockIdx.x == 0) {
+        // The extra CTA: the chunk schedule the layout left to this kernel,
+        // built from the layout's rank offsets while the other CTAs move rows.
+        __shared__ int s_warp32[32];
+        grid_dependency_wait();
+        if (*reinterpret_cast<volatile int32_t *>(st.n_chunks) == -1) return;  // the layout gave up
+        int32_t *s_roff = reinterpret_cast<int32_t *>(smem);
+        int32_t *s_P = s_roff + st.R + 1;
+        for (int r = lane; r <= st.R; r += 32) s_roff[r] = st.rank_offset[r];
+        __syncthreads();
+        cta_build_schedule(s_roff, st.R, st.W, st.tiers, st.chunks, st.n_chunks, st.worker_begin, s_warp32, s_P,
+                           whole_cta());
+        return;
+    }
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + (size_t)NS * stage_bytes);
     int64_t *s_tok = reinterpret_cast<int64_t *>(bar + kBulkMaxStages);  // token of each stage, -1 = none
-    const int lane = threadIdx.x;
-    const int64_t G = gridDim.x;
-    const int64_t first = blockIdx.x;
+    const int64_t G = gridDim.x - sched_on;
+    const int64_t first = blockIdx.x - sched_on;
     const int64_t n = first < T ? (T - first + G - 1) / G : 0;  // static order: tokens first + i G
     const bool dyn = ctr != nullptr;
 
@@ -224,7 +238,8 @@ int bulk_stages(int32_t row_bytes) {
 }
 
 cudaError_t launch_bulk(const ep_config &c, const ep_bf16 *x, const int32_t *slot, ep_bf16 *send, int32_t *meta,
-                        cudaStream_t s, unsigned *ctr, bool ctr_zeroed, bool after_layout) {
+                        cudaStream_t s, unsigned *ctr, bool ctr_zeroed, bool after_layout,
+                        const ScheduleTask *sched) {
     const int32_t row_bytes = c.H * 2;
     const int32_t row_pad = (row_bytes + 127) & ~127;
     const int32_t stage_bytes = row_pad + 128;
@@ -245,6 +260,11 @@ cudaError_t launch_bulk(const ep_config &c, const ep_bf16 *x, const int32_t *slo
     const int occ = max_blocks_per_sm(reinterpret_cast<const void *>(dispatch_bulk_kernel), 32, smem);
     int64_t grid = (int64_t)sm_count(dev) * occ;
     if (grid > c.T) grid = c.T;
+    // the schedule CTA (index 0) needs (2 R + 4) ints of the stage memory
+    const int32_t sched_on = sched && (size_t)(2 * sched->R + 4) * sizeof(int32_t) <= smem ? 1 : 0;
+    if (sched && !sched_on) return cudaErrorNotSupported;
+    ScheduleTask st = sched ? *sched : ScheduleTask{};
+    grid += sched_on;
     if (ctr && !ctr_zeroed) {
         e = cudaMemsetAsync(ctr, 0, sizeof(unsigned), s);
         if (e != cudaSuccess) return e;
@@ -261,7 +281,7 @@ cudaError_t launch_bulk(const ep_config &c, const ep_bf16 *x, const int32_t *slo
     cfg.numAttrs = after_layout ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, dispatch_bulk_kernel, reinterpret_cast<const char *>(x), slot,
                               reinterpret_cast<char *>(send), meta, c.T, c.k, row_bytes, row_pad, stage_bytes, NS,
-                              (int64_t)c.T * c.k, err, ctr);
+                              (int64_t)c.T * c.k, err, ctr, st, sched_on);
 }
 
 }  // namespace
@@ -290,10 +310,14 @@ static bool use_bulk(const ep_config &c, const int32_t *slot) {
            row_bytes <= 48 * 1024;
 }
 
+bool dispatch_uses_bulk(const ep_config &c, const int32_t *slot) { return c.T > 0 && use_bulk(c, slot); }
+
 cudaError_t launch_dispatch(const ep_config &c, const ep_bf16 *x, const int32_t *slot, ep_bf16 *send,
-                            int32_t *meta, cudaStream_t s, unsigned *ctr, bool ctr_zeroed, bool after_layout) {
+                            int32_t *meta, cudaStream_t s, unsigned *ctr, bool ctr_zeroed, bool after_layout,
+                            const ScheduleTask *sched) {
     if (c.T == 0) return cudaSuccess;
-    if (use_bulk(c, slot)) return launch_bulk(c, x, slot, send, meta, s, ctr, ctr_zeroed, after_layout);
+    if (use_bulk(c, slot)) return launch_bulk(c, x, slot, send, meta, s, ctr, ctr_zeroed, after_layout, sched);
+    if (sched) return cudaErrorNotSupported;  // only the bulk kernel builds a schedule
     switch (c.k) {
         case 1: return launch_k<1>(c, x, slot, send, meta, s);
         case 2: return launch_k<2>(c, x, slot, send, meta, s);

@@ -63,14 +63,20 @@ int max_blocks_per_sm(const void *fn, int threads, size_t smem);
 
 // za / zb: optional words (na / nb of them) the route kernel sets to zero for
 // kernels that follow it in the same call sequence.
+// zc: optional int32 word the route kernel also sets to zero.
 cudaError_t launch_route(const ep_config &c, const float *logits, int32_t *idx, float *w, cudaStream_t s,
-                         unsigned *za = nullptr, int na = 0, unsigned *zb = nullptr, int nb = 0);
+                         unsigned *za = nullptr, int na = 0, unsigned *zb = nullptr, int nb = 0,
+                         int32_t *zc = nullptr);
 
 // sync_zeroed: the caller already zeroed the workspace's sync words (skip the memset).
+// defer_schedule: when the layout runs as the single cooperative kernel, leave
+// the chunk schedule to the caller (*deferred = true; chunks, n_chunks and
+// worker_begin are then not written, except n_chunks = -1 on failure).
 cudaError_t launch_layout(const ep_config &c, int32_t W, const int32_t *idx, int32_t *expert_count,
                           int32_t *expert_offset, int32_t *rank_count, int32_t *rank_offset, int32_t *slot,
                           ep_chunk *chunks, int32_t *n_chunks, int32_t *worker_begin, void *workspace,
-                          cudaStream_t s, bool sync_zeroed = false);
+                          cudaStream_t s, bool sync_zeroed = false, bool defer_schedule = false,
+                          bool *deferred = nullptr);
 
 // Runs two CTAs into a grid barrier that expects three; *gave_up counts the
 // CTAs that stopped waiting after max_polls polls (2 when the bound works).
@@ -84,9 +90,22 @@ int layout_kernel_count(const ep_config &c);
 // after_layout: the launch follows the layout kernel in the same stream and may
 // start while it runs (programmatic dependent launch; the kernel loads x rows
 // first and reads the slots only after griddepcontrol.wait).
+// A chunk schedule for one extra CTA of the bulk dispatch to build from
+// rank_offset (after the layout grid it depends on), unless *n_chunks is -1.
+struct ScheduleTask {
+    const int32_t *rank_offset;
+    ep_chunk *chunks;
+    int32_t *n_chunks;
+    int32_t *worker_begin;
+    int32_t R, W;
+    HopTiers tiers;
+};
+// sched: build that schedule in the dispatch kernel (bulk path only; see
+// dispatch_uses_bulk).
 cudaError_t launch_dispatch(const ep_config &c, const ep_bf16 *x, const int32_t *slot, ep_bf16 *send,
                             int32_t *meta, cudaStream_t s, unsigned *ctr = nullptr, bool ctr_zeroed = false,
-                            bool after_layout = false);
+                            bool after_layout = false, const ScheduleTask *sched = nullptr);
+bool dispatch_uses_bulk(const ep_config &c, const int32_t *slot);
 
 cudaError_t launch_combine(const ep_config &c, const ep_bf16 *y, const int32_t *slot, const float *w,
                            ep_bf16 *out, cudaStream_t s);

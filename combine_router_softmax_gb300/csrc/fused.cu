@@ -459,12 +459,19 @@ cudaError_t launch_dispatch_fused(const ep_config &c, int32_t W, const float *lo
         char *ws = static_cast<char *>(workspace);
         unsigned *lsync = reinterpret_cast<unsigned *>(ws + layout_workspace(c).sync_off);
         unsigned *ctr = reinterpret_cast<unsigned *>(ws + fused_counter_offset(c));
-        cudaError_t e = launch_route(c, logits, topk_idx, topk_w, s, lsync, 2, ctr, 1);
+        // When the bulk dispatch follows the single-kernel layout, an extra CTA of
+        // the dispatch builds the chunk schedule, so the layout does not hold the
+        // dispatch back for it; the route kernel zeroes n_chunks, which the
+        // layout sets to -1 if it fails.
+        const bool defer = dispatch_uses_bulk(c, slot);
+        cudaError_t e = launch_route(c, logits, topk_idx, topk_w, s, lsync, 2, ctr, 1, defer ? n_chunks : nullptr);
         if (e != cudaSuccess) return e;
+        bool deferred = false;
         e = launch_layout(c, W, topk_idx, expert_count, expert_offset, rank_count, rank_offset, slot, chunks,
-                          n_chunks, worker_begin, workspace, s, true);
+                          n_chunks, worker_begin, workspace, s, true, defer, &deferred);
         if (e != cudaSuccess) return e;
-        return launch_dispatch(c, x, slot, send, meta, s, ctr, true, true);
+        const ScheduleTask st{rank_offset, chunks, n_chunks, worker_begin, c.R, W, hop_tiers(c)};
+        return launch_dispatch(c, x, slot, send, meta, s, ctr, true, true, deferred ? &st : nullptr);
     }
     FusedArgs a;
     a.logits = logits;

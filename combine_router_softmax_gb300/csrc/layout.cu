@@ -83,7 +83,7 @@ layout_fused_kernel(const int32_t *__restrict__ idx, int32_t T, int32_t E, int32
                     int32_t *__restrict__ expert_offset, int32_t *__restrict__ rank_count,
                     int32_t *__restrict__ rank_offset, int32_t *__restrict__ slot, ep_chunk *__restrict__ chunks,
                     int32_t *__restrict__ n_chunks, int32_t *__restrict__ worker_begin, int32_t W,
-                    HopTiers tiers) {
+                    HopTiers tiers, int32_t defer_schedule) {
     extern __shared__ int32_t sm[];
     // A dispatch launched after this kernel may start now and fetch x rows
     // (it waits for this grid before it reads a slot).
@@ -189,7 +189,7 @@ layout_fused_kernel(const int32_t *__restrict__ idx, int32_t T, int32_t E, int32
         }
         if (threadIdx.x == 0) rank_offset[R] = s_eoff[E];
     }
-    if (b == nb - 1) {
+    if (b == nb - 1 && !defer_schedule) {
         for (int r = threadIdx.x; r <= R; r += blockDim.x) s_roff[r] = s_eoff[r * epr];
         __syncthreads();
         cta_build_schedule(s_roff, R, W, tiers, chunks, n_chunks, worker_begin, s_warp32, s_P, whole_cta());
@@ -361,7 +361,8 @@ int layout_kernel_count(const ep_config &c) {
 cudaError_t launch_layout(const ep_config &c, int32_t W, const int32_t *idx, int32_t *expert_count,
                           int32_t *expert_offset, int32_t *rank_count, int32_t *rank_offset, int32_t *slot,
                           ep_chunk *chunks, int32_t *n_chunks, int32_t *worker_begin, void *workspace,
-                          cudaStream_t s, bool sync_zeroed) {
+                          cudaStream_t s, bool sync_zeroed, bool defer_schedule, bool *deferred) {
+    if (deferred) *deferred = false;
     int nw = 0;
     int64_t nb = 0;
     if (!layout_fused_fits(c, &nw, &nb))
@@ -378,9 +379,11 @@ cudaError_t launch_layout(const ep_config &c, int32_t W, const int32_t *idx, int
     const size_t smem = fused_smem_bytes(nw, c.E, c.R, c.k);
     int32_t T = c.T, E = c.E, R = c.R, k = c.k, nbi = (int32_t)nb;
     HopTiers tiers = hop_tiers(c);
+    int32_t defer = defer_schedule ? 1 : 0;
+    if (deferred) *deferred = defer_schedule;
     void *args[] = {(void *)&idx, &T, &E, &R, &k, &nbi, (void *)&counts, (void *)&sync, (void *)&expert_count,
                     (void *)&expert_offset, (void *)&rank_count, (void *)&rank_offset, (void *)&slot,
-                    (void *)&chunks, (void *)&n_chunks, (void *)&worker_begin, &W, &tiers};
+                    (void *)&chunks, (void *)&n_chunks, (void *)&worker_begin, &W, &tiers, &defer};
     return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(layout_fused_kernel), dim3((unsigned)nb),
                                        dim3((unsigned)(nw * 32)), args, smem, s);
 }

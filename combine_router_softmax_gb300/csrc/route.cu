@@ -19,12 +19,13 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
 route_kernel(const float *__restrict__ logits, int32_t T, int32_t E, int32_t k, int32_t n_groups,
              int32_t topk_groups, int32_t renormalize, int32_t *__restrict__ topk_idx,
              float *__restrict__ topk_w, unsigned *__restrict__ zero_a, int n_zero_a, unsigned *__restrict__ zero_b,
-             int n_zero_b) {
+             int n_zero_b, int32_t *__restrict__ zero_c) {
     extern __shared__ float s_dyn[];  // [kRouteWarps][E] logits, group-limited routing only
     // Reset the counters that later kernels of the same call sequence start from.
     if (blockIdx.x == 0) {
         if ((int)threadIdx.x < n_zero_a) zero_a[threadIdx.x] = 0u;
         if ((int)threadIdx.x < n_zero_b) zero_b[threadIdx.x] = 0u;
+        if (threadIdx.x == 0 && zero_c) *zero_c = 0;
     }
     __shared__ int2 s_cand[kRouteWarps][32];  // candidate (logit bits, expert)
     __shared__ int2 s_pick[kRouteWarps][32];  // the k picks in order
@@ -43,26 +44,26 @@ route_kernel(const float *__restrict__ logits, int32_t T, int32_t E, int32_t k, 
 }
 template <int VPL>
 cudaError_t launch_vpl(const ep_config &c, const float *logits, int32_t *idx, float *w, cudaStream_t s,
-                       unsigned *za, int na, unsigned *zb, int nb) {
+                       unsigned *za, int na, unsigned *zb, int nb, int32_t *zc) {
     const size_t smem = c.n_groups > 1 ? sizeof(float) * kRouteWarps * (size_t)c.E : 0;
     const unsigned grid = (unsigned)((c.T + kRouteWarps - 1) / kRouteWarps);
     route_kernel<VPL><<<grid, kRouteWarps * 32, smem, s>>>(logits, c.T, c.E, c.k, c.n_groups, c.topk_groups,
-                                                         c.renormalize, idx, w, za, na, zb, nb);
+                                                         c.renormalize, idx, w, za, na, zb, nb, zc);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_route(const ep_config &c, const float *logits, int32_t *idx, float *w, cudaStream_t s,
-                         unsigned *za, int na, unsigned *zb, int nb) {
+                         unsigned *za, int na, unsigned *zb, int nb, int32_t *zc) {
     if (c.T == 0) return cudaSuccess;
     const int vpl = (c.E + 31) / 32;
-    if (vpl <= 1) return launch_vpl<1>(c, logits, idx, w, s, za, na, zb, nb);
-    if (vpl <= 2) return launch_vpl<2>(c, logits, idx, w, s, za, na, zb, nb);
-    if (vpl <= 4) return launch_vpl<4>(c, logits, idx, w, s, za, na, zb, nb);
-    if (vpl <= 8) return launch_vpl<8>(c, logits, idx, w, s, za, na, zb, nb);
-    if (vpl <= 16) return launch_vpl<16>(c, logits, idx, w, s, za, na, zb, nb);
-    return launch_vpl<32>(c, logits, idx, w, s, za, na, zb, nb);
+    if (vpl <= 1) return launch_vpl<1>(c, logits, idx, w, s, za, na, zb, nb, zc);
+    if (vpl <= 2) return launch_vpl<2>(c, logits, idx, w, s, za, na, zb, nb, zc);
+    if (vpl <= 4) return launch_vpl<4>(c, logits, idx, w, s, za, na, zb, nb, zc);
+    if (vpl <= 8) return launch_vpl<8>(c, logits, idx, w, s, za, na, zb, nb, zc);
+    if (vpl <= 16) return launch_vpl<16>(c, logits, idx, w, s, za, na, zb, nb, zc);
+    return launch_vpl<32>(c, logits, idx, w, s, za, na, zb, nb, zc);
 }
 
 }  // namespace ep
