@@ -43,6 +43,7 @@ struct FusedPlan {
     int ns = 0;       // x-row stages per CTA (bulk path), 0 = vector copy
     int row_pad = 0;  // bytes per stage
     size_t smem = 0;
+    int sched_cta = 0;  // 1: one more CTA, without a tile, builds the chunk schedule
 };
 
 size_t align128(size_t b) { return (b + 127) & ~(size_t)127; }
@@ -102,6 +103,7 @@ struct FusedArgs {
     HopTiers tiers;
     int32_t nb, tb, ns, row_pad;
     int32_t early_dependents;  // signal dependents at the dispatch phase (small sends only)
+    int32_t sched_cta;         // 1: CTA nb holds no tile and builds the chunk schedule
 };
 
 template <int VPL>
@@ -129,9 +131,14 @@ __global__ void __launch_bounds__(kFusedThreads) dispatch_fused_kernel(FusedArgs
     const int warp = threadIdx.x >> 5;
     const int b = blockIdx.x;
     const int E = a.E, k = a.k;
+    // The schedule CTA (index nb, when present) holds no tile: it only joins the
+    // two grid barriers, then builds the chunk schedule while the tile CTAs
+    // write their slots and rows.
+    const bool sched_only = a.sched_cta && b == a.nb;
+    const unsigned arrivals = (unsigned)(a.nb + a.sched_cta);
     // tile b = tokens [floor(b T / nb), floor((b + 1) T / nb)): every CTA within one token of the others
-    const int64_t t0 = (int64_t)b * a.T / a.nb;
-    const int ntok = (int)((int64_t)(b + 1) * a.T / a.nb - t0);  // may be 0 when T < nb
+    const int64_t t0 = sched_only ? a.T : (int64_t)b * a.T / a.nb;
+    const int ntok = sched_only ? 0 : (int)((int64_t)(b + 1) * a.T / a.nb - t0);  // may be 0 when T < nb
     const int np = ntok * k;
     const int32_t row_bytes = a.H * 2;
 
@@ -163,15 +170,15 @@ __global__ void __launch_bounds__(kFusedThreads) dispatch_fused_kernel(FusedArgs
 
     // B. rank the tile's pairs; publish the tile's counts
     const int ppw = np > 0 ? (np + kFusedWarps - 1) / kFusedWarps : 1;
-    cta_rank_pairs(tile_e, np, ppw, E, cnt, tile_r, a.counts + (int64_t)b * E, 1);
+    if (!sched_only) cta_rank_pairs(tile_e, np, ppw, E, cnt, tile_r, a.counts + (int64_t)b * E, 1);
 
     // C. (a single CTA needs no grid barrier: after a CTA barrier its own
     // global writes are visible to all its threads)
-    bool ok = a.nb > 1 ? grid_barrier(&a.sync[0], (unsigned)a.nb) : (__syncthreads(), true);
+    bool ok = arrivals > 1 ? grid_barrier(&a.sync[0], arrivals) : (__syncthreads(), true);
 
     // D. column scan: CTA b owns experts b, b + nb, ...; all their counts over
     // every tile are read in one batch, then scanned over the tiles.
-    if (ok) {
+    if (ok && !sched_only) {
         const int nb = a.nb;
         const int my_n = b < E ? (E - b + nb - 1) / nb : 0;
         const int nv = my_n * nb;
@@ -209,15 +216,15 @@ __global__ void __launch_bounds__(kFusedThreads) dispatch_fused_kernel(FusedArgs
                 if (threadIdx.x == 0) a.totals[e] = total;
             }
         }
-        // E.
-        ok = a.nb > 1 ? grid_barrier(&a.sync[1], (unsigned)a.nb) : (__syncthreads(), true);
     }
+    // E.
+    if (ok) ok = arrivals > 1 ? grid_barrier(&a.sync[1], arrivals) : (__syncthreads(), true);
 
     if (ok) {
         // F. expert offsets and this tile's slots
         for (int e = threadIdx.x; e < E; e += blockDim.x) {
             s_tot[e] = __ldcg(a.totals + e);
-            s_base[e] = __ldcg(a.bases + (int64_t)b * E + e);
+            if (!sched_only) s_base[e] = __ldcg(a.bases + (int64_t)b * E + e);
         }
         __syncthreads();
         {
@@ -254,7 +261,7 @@ __global__ void __launch_bounds__(kFusedThreads) dispatch_fused_kernel(FusedArgs
             }
             if (threadIdx.x == 0) a.rank_offset[a.R] = s_eoff[E];
         }
-        if (b == a.nb - 1) {
+        if (a.sched_cta ? sched_only : b == a.nb - 1) {
             for (int r = threadIdx.x; r <= a.R; r += blockDim.x) s_roff[r] = s_eoff[r * epr];
             __syncthreads();
             cta_build_schedule(s_roff, a.R, a.W, a.tiers, a.chunks, a.n_chunks, a.worker_begin, s_warp32, s_P,
@@ -369,9 +376,10 @@ bool plan_fused(const ep_config &c, FusedPlan *p) {
     const int sms = sm_count(dev);
     // Try 2, then 1 CTA per SM (more CTAs = smaller tiles = shorter metadata phases).
     for (int per_sm = 2; per_sm >= 1; --per_sm) {
-        int nb = sms * per_sm;
+        int nb = sms * per_sm - 1;  // one resident slot kept for the schedule CTA
         if (nb > kMaxFusedCTAs) nb = kMaxFusedCTAs;
         if (nb > c.T) nb = c.T;
+        if (nb < 1) nb = 1;
         const int tb = (int)((c.T + nb - 1) / nb);  // largest tile
         // Routing needs a warp per token to keep its latency hidden; when a
         // warp would route more than one token the separate route kernel
@@ -393,8 +401,10 @@ bool plan_fused(const ep_config &c, FusedPlan *p) {
         const SmemLayout L = smem_layout(ns, row_pad, tb, c.k, c.E, c.R, c.n_groups > 1);
         if (L.bytes > kFusedSmemLimit) continue;
         const int occ = max_blocks_per_sm(reinterpret_cast<const void *>(kern), kFusedThreads, L.bytes);
-        if (nb > sms * occ) continue;
+        const int sched = nb > 1 ? 1 : 0;
+        if (nb + sched > sms * occ) continue;
         p->nb = nb;
+        p->sched_cta = sched;
         p->tb = tb;
         p->ns = ns;
         p->row_pad = row_pad;
@@ -508,6 +518,7 @@ cudaError_t launch_dispatch_fused(const ep_config &c, int32_t W, const float *lo
     a.W = W;
     a.tiers = hop_tiers(c);
     a.nb = p.nb;
+    a.sched_cta = p.sched_cta;
     a.tb = p.tb;
     a.ns = p.ns;
     a.row_pad = p.row_pad;
@@ -516,7 +527,8 @@ cudaError_t launch_dispatch_fused(const ep_config &c, int32_t W, const float *lo
     e = cudaMemsetAsync(a.sync, 0, 2 * sizeof(unsigned), s);
     if (e != cudaSuccess) return e;
     void *args[] = {&a};
-    return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(pick_kernel(c.E)), dim3((unsigned)p.nb),
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(pick_kernel(c.E)),
+                                       dim3((unsigned)(p.nb + p.sched_cta)),
                                        dim3(kFusedThreads), args, p.smem, s);
 }
 
