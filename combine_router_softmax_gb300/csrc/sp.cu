@@ -23,6 +23,7 @@
 #include <cuda_bf16.h>
 
 #include "ep_internal.cuh"
+#include "flag_ops.cuh"
 
 namespace ep {
 namespace {
@@ -36,15 +37,6 @@ constexpr uint32_t kSpMaxPolls = 1u << 20;  // about a second of 64 ns sleeps an
 constexpr uint32_t kSentinel2 = 0xFFFFFFFFu;  // two sentinel bf16 values
 
 static __device__ int32_t g_sp_error;
-
-__device__ __forceinline__ uint4 ld_relaxed_v4(const uint4 *p) {
-    uint4 r;
-    asm volatile("ld.relaxed.gpu.global.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p)
-                 : "memory");
-    return r;
-}
 
 __device__ __forceinline__ bool half_is_sentinel(uint32_t w) {
     return (w & 0xFFFFu) == 0xFFFFu || (w >> 16) == 0xFFFFu;
@@ -110,16 +102,6 @@ struct SpArgs {
     int32_t T, H, E, k, W, row_pad;
     unsigned epoch;
 };
-
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-__device__ __forceinline__ void st_release_u32(unsigned *p, unsigned v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
 
 // Expert that owns row s: the e with eoff[e] <= s < eoff[e + 1] (empty experts skipped).
 __device__ __forceinline__ int owner_expert(const int32_t *eoff, int32_t E, int64_t s) {

@@ -15,6 +15,7 @@
 // block's epoch before it reads the rest, so a block whose flag matches is
 // complete.
 #include "ep_internal.cuh"
+#include "flag_ops.cuh"
 
 namespace ep {
 namespace {
@@ -22,26 +23,6 @@ namespace {
 constexpr int kTffThreads = 256;
 constexpr int kTffPayload = 480;
 constexpr int kTffVecs = kTffPayload / 16;  // 30
-
-__device__ __forceinline__ void st_release_u32(unsigned *p, unsigned v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-// Coherent 16-byte load (the framed buffer may be written while it is read).
-__device__ __forceinline__ uint4 ld_v4(const uint4 *p) {
-    uint4 r;
-    asm volatile("ld.relaxed.gpu.global.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-                 : "l"(p)
-                 : "memory");
-    return r;
-}
 
 // Blocks per warp step: 8 blocks = 240 payload vectors, 8 per lane in flight.
 constexpr int kTffGroup = 8;
@@ -120,7 +101,7 @@ tff_decode_kernel(const uint4 *__restrict__ framed, uint4 *__restrict__ rows, in
         for (int u = 0; u < kTffGroup; ++u) {
             const int v = lane + 32 * u;
             const int g = v / kTffVecs, j = v - g * kTffVecs;
-            if (g < kTffGroup && ((ok >> g) & 1u)) val[u] = ld_v4(framed + (q0 + g) * 32 + 2 + j);
+            if (g < kTffGroup && ((ok >> g) & 1u)) val[u] = ld_relaxed_v4(framed + (q0 + g) * 32 + 2 + j);
         }
 #pragma unroll
         for (int u = 0; u < kTffGroup; ++u) {
