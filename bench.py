@@ -768,9 +768,15 @@ def run_gb300(args):
         gclk = clocks.stop()
         if gclk is not None:
             clk = gclk
-        local_total_ms = sum(a.elapsed_time(b_) for a, b_ in gev)
+        per_step_ms = [a.elapsed_time(b_) for a, b_ in gev]
+        local_total_ms = sum(per_step_ms)
     else:
+        per_step_ms = list(step_ms)
         local_total_ms = sum(step_ms)
+    q = sorted(per_step_ms)
+    step_stats = {"median": round(1e3 * q[len(q) // 2], 2), "p10": round(1e3 * q[len(q) // 10], 2),
+                  "p90": round(1e3 * q[(9 * len(q)) // 10], 2), "min": round(1e3 * q[0], 2),
+                  "max": round(1e3 * q[-1], 2)}
     max_total_ms = reduce_max(local_total_ms, world, device)
     value = world * K * bytes_step / (max_total_ms * 1e-3) / 1e9
     ms_per_step = max_total_ms / K
@@ -833,6 +839,7 @@ def run_gb300(args):
                    else "the step's C-ABI calls launched per step"),
         "calls": [n for n, _ in calls],
         "stream_us_per_layer": round(stream_ms_per_step * 1e3, 2),
+        "us_per_layer_stats": step_stats,
         "hbm_fraction": round(value / world / peak, 4),
         "kernel_us": {n: round(v * 1e3, 2) for n, v in kern_ms.items()},
         "roofline": {
