@@ -202,17 +202,17 @@ __device__ void cta_rank_pairs(const int32_t *tile_e, int np, int ppw, int32_t E
     __syncthreads();
 }
 
-// Rank phase for the CTA's tokens [t_cta, t_cta + 32 nw): loads their pairs
-// into tile_e (32 tokens per warp) and ranks them with cta_rank_pairs.
+// Rank phase for the CTA's tokens [t_cta, t_cta + tpw nw): loads their pairs
+// into tile_e (tpw tokens per warp) and ranks them with cta_rank_pairs.
 __device__ void cta_rank_tokens(const int32_t *__restrict__ idx, int32_t T, int32_t E, int32_t k, int64_t t_cta,
                                 int32_t *cnt, int32_t *tile_e, int32_t *tile_r, int32_t *cta_count,
-                                int64_t stride) {
+                                int64_t stride, int tpw = 32) {
     const int nw = blockDim.x >> 5;
     const int64_t left = (int64_t)T - t_cta;
-    const int ntok = left <= 0 ? 0 : (left >= 32 * nw ? 32 * nw : (int)left);
+    const int ntok = left <= 0 ? 0 : (left >= tpw * nw ? tpw * nw : (int)left);
     const int np = ntok * k;
     for (int i = threadIdx.x; i < np; i += blockDim.x) tile_e[i] = __ldg(idx + t_cta * k + i);
-    cta_rank_pairs(tile_e, np, 32 * k, E, cnt, tile_r, cta_count, stride);
+    cta_rank_pairs(tile_e, np, tpw * k, E, cnt, tile_r, cta_count, stride);
 }
 
 // Largest i in [0, n) with P[i] <= x, for P non-decreasing with P[0] <= x.

@@ -43,19 +43,40 @@ constexpr size_t kFusedSmemBudget = 160 * 1024;
 
 size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
 
-// Shared memory of the fused kernel for nw warps.
-size_t fused_smem_bytes(int nw, int32_t E, int32_t R, int32_t k) {
-    return sizeof(int32_t) * ((size_t)nw * E + 2 * (size_t)nw * 32 * k + 3 * (size_t)E + 2 + 2 * (size_t)R + 4);
+// Shared memory of the fused kernel for nw warps of tpw tokens each.
+size_t fused_smem_bytes(int nw, int tpw, int32_t E, int32_t R, int32_t k) {
+    return sizeof(int32_t) * ((size_t)nw * E + 2 * (size_t)nw * tpw * k + 3 * (size_t)E + 2 + 2 * (size_t)R + 4);
 }
 
-// Warps per fused CTA (8, 16 or 32): the fewest that keep the grid at <= 32
-// CTAs, within the shared-memory budget. 0 if not even 8 fit.
-int fused_warps(int64_t T, int32_t E, int32_t R, int32_t k) {
-    int best = 0;
-    for (int nw = kLayoutWarps; nw <= kFusedMaxWarps; nw <<= 1) {
-        if (fused_smem_bytes(nw, E, R, k) > kFusedSmemBudget) break;
-        best = nw;
-        if ((T + 32 * nw - 1) / (32 * nw) <= 32) break;
+// The single-kernel layout's tiling: nw warps (16, 8 or 32) of tpw tokens (4
+// to 32) per CTA, nb CTAs. The rank phase was the kernel's longest (a warp
+// ranks its pairs 32 at a time) and the count-table read comes next (a thread
+// sums nb / tpe rows of its expert's column), so the CTAs are many and small
+// and, where shared memory allows, wide: for each warp count the fewest tokens
+// per warp (at least 4) that keep the grid at <= kLayoutTargetCTAs CTAs,
+// preferring 16 warps, then 8, then 32; above the target the smallest grid.
+// nw = 0 if nothing fits the shared-memory budget.
+struct LayoutTiling {
+    int nw = 0, tpw = 32;
+    int64_t nb = 0;
+};
+constexpr int64_t kLayoutTargetCTAs = 64;
+
+LayoutTiling fused_tiling(int64_t T, int32_t E, int32_t R, int32_t k) {
+    LayoutTiling best;
+    const int order[3] = {16, 8, 32};
+    for (int i = 0; i < 3; ++i) {
+        const int nw = order[i];
+        int tpw = 4;
+        while (tpw < 32 && (T + (int64_t)nw * tpw - 1) / ((int64_t)nw * tpw) > kLayoutTargetCTAs) tpw <<= 1;
+        if (fused_smem_bytes(nw, tpw, E, R, k) > kFusedSmemBudget) continue;
+        const int64_t nb = (T + (int64_t)nw * tpw - 1) / ((int64_t)nw * tpw);
+        if (best.nw == 0 || nb < best.nb) {
+            best.nw = nw;
+            best.tpw = tpw;
+            best.nb = nb;
+        }
+        if (nb <= kLayoutTargetCTAs) break;
     }
     return best;
 }
@@ -66,8 +87,8 @@ LayoutWorkspace layout_workspace(const ep_config &c) {
     LayoutWorkspace w;
     const int64_t nb = layout_blocks(c.T);
     w.block_counts_off = 0;
-    const int nw = fused_warps(c.T, c.E, c.R, c.k);
-    const int64_t nbf = nw > 0 ? (c.T + 32 * nw - 1) / (32 * nw) : nb;
+    const LayoutTiling t = fused_tiling(c.T, c.E, c.R, c.k);
+    const int64_t nbf = t.nw > 0 ? t.nb : nb;
     w.sync_off = align256(sizeof(int32_t) * (size_t)nbf * (size_t)c.E);
     const size_t fallback = align256(sizeof(int32_t) * (size_t)nb * (size_t)c.E);
     const size_t fused = w.sync_off + 256;
@@ -83,16 +104,16 @@ layout_fused_kernel(const int32_t *__restrict__ idx, int32_t T, int32_t E, int32
                     int32_t *__restrict__ expert_offset, int32_t *__restrict__ rank_count,
                     int32_t *__restrict__ rank_offset, int32_t *__restrict__ slot, ep_chunk *__restrict__ chunks,
                     int32_t *__restrict__ n_chunks, int32_t *__restrict__ worker_begin, int32_t W,
-                    HopTiers tiers, int32_t defer_schedule) {
+                    HopTiers tiers, int32_t defer_schedule, int32_t tpw) {
     extern __shared__ int32_t sm[];
     // A dispatch launched after this kernel may start now and fetch x rows
     // (it waits for this grid before it reads a slot).
     grid_launch_dependents();
     const int nw = blockDim.x >> 5;
     int32_t *cnt = sm;                         // [nw][E]
-    int32_t *tile_e = cnt + nw * E;            // [nw][32 k]
-    int32_t *tile_r = tile_e + nw * 32 * k;    // [nw][32 k]
-    int32_t *s_tot = tile_r + nw * 32 * k;     // [E]   pairs of expert e, all CTAs
+    int32_t *tile_e = cnt + nw * E;            // [nw][tpw k]
+    int32_t *tile_r = tile_e + nw * tpw * k;   // [nw][tpw k]
+    int32_t *s_tot = tile_r + nw * tpw * k;    // [E]   pairs of expert e, all CTAs
     int32_t *s_pre = s_tot + E;                // [E]   pairs of expert e in CTAs before this one
     int32_t *s_eoff = s_pre + E;               // [E+2] expert offsets (+ total)
     int32_t *s_roff = s_eoff + E + 2;          // [R+1] rank offsets
@@ -100,8 +121,8 @@ layout_fused_kernel(const int32_t *__restrict__ idx, int32_t T, int32_t E, int32
     __shared__ int s_warp32[32];
 
     const int b = blockIdx.x;
-    const int64_t t_cta = (int64_t)b * 32 * nw;
-    cta_rank_tokens(idx, T, E, k, t_cta, cnt, tile_e, tile_r, counts + (int64_t)b * E, 1);
+    const int64_t t_cta = (int64_t)b * tpw * nw;
+    cta_rank_tokens(idx, T, E, k, t_cta, cnt, tile_e, tile_r, counts + (int64_t)b * E, 1, tpw);
 
     if (nb > 1 && !grid_barrier(&sync[0], (unsigned)nb)) {
         if (threadIdx.x == 0) {
@@ -169,11 +190,11 @@ layout_fused_kernel(const int32_t *__restrict__ idx, int32_t T, int32_t E, int32
     // Final slots of this CTA's pairs.
     {
         const int64_t left = (int64_t)T - t_cta;
-        const int np = (left <= 0 ? 0 : (left >= 32 * nw ? 32 * nw : (int)left)) * k;
+        const int np = (left <= 0 ? 0 : (left >= tpw * nw ? tpw * nw : (int)left)) * k;
         for (int p = threadIdx.x; p < np; p += blockDim.x) {
             const int e = tile_e[p];
             const int r = tile_r[p];
-            slot[t_cta * k + p] = r < 0 ? -1 : s_eoff[e] + s_pre[e] + cnt[(p / (32 * k)) * E + e] + r;
+            slot[t_cta * k + p] = r < 0 ? -1 : s_eoff[e] + s_pre[e] + cnt[(p / (tpw * k)) * E + e] + r;
         }
     }
 
@@ -327,12 +348,13 @@ cudaError_t launch_fallback(const ep_config &c, int32_t W, const int32_t *idx, i
 
 }  // namespace
 
-static bool layout_fused_fits(const ep_config &c, int *nw_out, int64_t *nb_out) {
+static bool layout_fused_fits(const ep_config &c, int *nw_out, int64_t *nb_out, int *tpw_out = nullptr) {
     if (c.T == 0) return false;
-    const int nw = fused_warps(c.T, c.E, c.R, c.k);
+    const LayoutTiling t = fused_tiling(c.T, c.E, c.R, c.k);
+    const int nw = t.nw;
     if (nw == 0) return false;
-    const int64_t nb = (c.T + 32 * nw - 1) / (32 * nw);
-    const size_t smem = fused_smem_bytes(nw, c.E, c.R, c.k);
+    const int64_t nb = t.nb;
+    const size_t smem = fused_smem_bytes(nw, t.tpw, c.E, c.R, c.k);
     static bool attr_set[kMaxDevices_] = {false};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices_) return false;
@@ -348,6 +370,7 @@ static bool layout_fused_fits(const ep_config &c, int *nw_out, int64_t *nb_out) 
     if (nb > (int64_t)sm_count(dev) * per_sm) return false;
     *nw_out = nw;
     *nb_out = nb;
+    if (tpw_out) *tpw_out = t.tpw;
     return true;
 }
 
@@ -363,9 +386,9 @@ cudaError_t launch_layout(const ep_config &c, int32_t W, const int32_t *idx, int
                           ep_chunk *chunks, int32_t *n_chunks, int32_t *worker_begin, void *workspace,
                           cudaStream_t s, bool sync_zeroed, bool defer_schedule, bool *deferred) {
     if (deferred) *deferred = false;
-    int nw = 0;
+    int nw = 0, tpw = 32;
     int64_t nb = 0;
-    if (!layout_fused_fits(c, &nw, &nb))
+    if (!layout_fused_fits(c, &nw, &nb, &tpw))
         return launch_fallback(c, W, idx, expert_count, expert_offset, rank_count, rank_offset, slot, chunks,
                                n_chunks, worker_begin, workspace, s);
 
@@ -376,14 +399,14 @@ cudaError_t launch_layout(const ep_config &c, int32_t W, const int32_t *idx, int
         cudaError_t e = cudaMemsetAsync(sync, 0, 2 * sizeof(unsigned), s);
         if (e != cudaSuccess) return e;
     }
-    const size_t smem = fused_smem_bytes(nw, c.E, c.R, c.k);
+    const size_t smem = fused_smem_bytes(nw, tpw, c.E, c.R, c.k);
     int32_t T = c.T, E = c.E, R = c.R, k = c.k, nbi = (int32_t)nb;
     HopTiers tiers = hop_tiers(c);
     int32_t defer = defer_schedule ? 1 : 0;
     if (deferred) *deferred = defer_schedule;
     void *args[] = {(void *)&idx, &T, &E, &R, &k, &nbi, (void *)&counts, (void *)&sync, (void *)&expert_count,
                     (void *)&expert_offset, (void *)&rank_count, (void *)&rank_offset, (void *)&slot,
-                    (void *)&chunks, (void *)&n_chunks, (void *)&worker_begin, &W, &tiers, &defer};
+                    (void *)&chunks, (void *)&n_chunks, (void *)&worker_begin, &W, &tiers, &defer, &tpw};
     return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(layout_fused_kernel), dim3((unsigned)nb),
                                        dim3((unsigned)(nw * 32)), args, smem, s);
 }
