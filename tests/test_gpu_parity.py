@@ -454,3 +454,40 @@ def test_dispatch_fused_vs_oracle(ep, orc):
     assert np.array_equal(bf16_from_dev(b.send), r["send"])
     assert np.array_equal(b.slot_meta.cpu().numpy(), r["meta"])
     assert bf16_ulp_distance(bf16_from_dev(b.out), r["out"]).max() <= 1
+
+
+# ---------------------------------------------------------------------------
+# tiling boundaries: where the layout's tokens per warp change (its grid is
+# kept near 64 CTAs of 16 warps) and where the fused dispatch kernel's range
+# ends (at most 8 tokens per tile, one resident slot kept for the schedule CTA)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("T", [1023, 1024, 1025, 2047, 2049, 4095, 4097, 8191, 8193, 16385, 32769])
+def test_layout_tiling_boundaries(ep, orc, T):
+    w = ep_synth.CONFIGS["prefill"].with_(name=f"prefill-T{T}", T=T)
+    logits = ep_synth.gate_logits(w.seed + 7, w.T, w.E, w.zipf_s)
+    g, r = _route_layout(ep, orc, w, logits)
+    assert_route(g, r, logits, w.renormalize)
+    assert_layout(g, r)
+
+
+@pytest.mark.parametrize("T", [2423, 2424, 2425, 2431, 2432, 2433])
+def test_dispatch_fused_range_end(ep, T):
+    w = ep_synth.CONFIGS["prefill"].with_(name=f"prefill-T{T}", T=T)
+    logits = torch.from_numpy(ep_synth.gate_logits(w.seed, w.T, w.E, w.zipf_s)).cuda()
+    x = bf16_to_dev(ep_synth.hidden_bf16_bits(w.seed, w.T, w.H))
+    cfg = ep.EpConfig.from_workload(w)
+    a = ep.LayerBuffers.allocate(cfg)
+    f = ep.LayerBuffers.allocate(cfg)
+    for b_ in (a, f):
+        b_.logits.copy_(logits)
+        b_.x.copy_(x)
+    a.route(); a.layout(); a.dispatch()
+    f.dispatch_fused()
+    torch.cuda.synchronize()
+    assert ep.ep_device_error() == 0
+    for name in ("topk_idx", "expert_offset", "rank_offset", "slot", "send", "slot_meta", "n_chunks"):
+        assert torch.equal(getattr(a, name), getattr(f, name)), f"{name} differs"
+    n = int(a.n_chunks.item())
+    assert torch.equal(a.chunks[:n], f.chunks[:n])
+    assert torch.equal(a.worker_begin[:w.num_workers + 1], f.worker_begin[:w.num_workers + 1])
