@@ -173,10 +173,20 @@ def measured_peak_gbs():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def _code_only(text: str) -> str:
+    """Source text without comments and blank space, so that an edit to a
+    comment does not mark a captured kernel as changed."""
+    import re
+
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.strip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES[kernel] + ["ep_internal.cuh"]:
-        h.update((ROOT / "combine_router_softmax_gb300" / "csrc" / rel).read_bytes())
+        h.update(_code_only((ROOT / "combine_router_softmax_gb300" / "csrc" / rel).read_text()).encode())
     return h.hexdigest()[:16]
 
 

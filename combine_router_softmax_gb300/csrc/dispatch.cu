@@ -100,13 +100,20 @@ cudaError_t launch_k(const ep_config &c, const ep_bf16 *x, const int32_t *slot, 
 // CTAs per SM. Tokens go to CTAs in a fixed stride, or -- when the caller
 // provides a counter in device memory -- are grabbed one at a time from it,
 // so CTAs that happen to get more bandwidth take more rows (measured: with a
-// fixed stride the last CTA ends ~20 % after the median one). Lane 0 streams token rows (and their k slots) into NS shared
-// memory stages with TMA bulk loads completing on per-stage mbarriers; once a
-// stage lands, lanes j < k each issue one bulk store of the row to send row
-// slot[t, j] and write its slot_meta. The stage is refilled with the token NS
-// places later as soon as those stores have finished reading it. The copy
-// engine moves whole rows, so the SM issues ~10 instructions per 14 KB row
-// instead of 900 vector loads/stores.
+// fixed stride the last CTA ends ~20 % after the median one). Lane 0 streams
+// token rows (and their k slots) into NS shared memory stages with TMA bulk
+// loads completing on per-stage mbarriers; once a stage lands, lanes j < k
+// each issue one bulk store of the row to send row slot[t, j] and write its
+// slot_meta. The stage is refilled with the token NS places later as soon as
+// those stores have finished reading it. The copy engine moves whole rows, so
+// the SM issues ~10 instructions per 14 KB row instead of 900 vector
+// loads/stores.
+//
+// Launched right after the layout (in ep_dispatch_fused) the kernel is a
+// programmatic dependent of it: the first rounds' x rows are requested before
+// griddepcontrol.wait, the slots only after. There it may also carry the
+// chunk schedule the layout left undone: CTA 0 then builds the schedule from
+// the rank offsets instead of moving rows.
 // ---------------------------------------------------------------------------
 
 static __device__ int32_t g_dispatch_error;
