@@ -1,14 +1,19 @@
 // combine.cu -- weighted top-k gather-reduce back to token order (ep_combine).
 //
 // out[t, h] = bf16_rne( fma(w[t,k-1], y[s_{k-1}, h], ... fma(w[t,0], y[s_0, h], 0) ) )
-// with s_j = slot[t, j]: the k expert outputs of a token are gathered back
-// ("later gathered during the Combine phase", UBEP article, opening section)
-// and summed in fp32, one fused multiply-add per term, j = 0 .. k-1.
+// with s_j = slot[t, j]: the k expert outputs of a token are brought back to
+// it in the Combine step that follows the experts (UBEP article, opening
+// section) and summed in fp32, one fused multiply-add per term, j = 0 .. k-1.
 //
 // Work unit = (token, segment of 32 * U 16-byte vectors). Each lane issues
 // all k * U row loads of its unit before the first multiply-add, so a warp
 // keeps k * U * 512 bytes in flight; y is read exactly once (streaming,
 // non-allocating loads) and out written once.
+//
+// The kernel is launched as a programmatic dependent of whatever precedes it
+// on the stream: its CTAs may become resident early, but each one waits on
+// griddepcontrol.wait before its first memory access, so it sees every write
+// of the previous kernel.
 #include <cuda_bf16.h>
 
 #include "ep_internal.cuh"

@@ -1,9 +1,9 @@
 // dispatch.cu -- row scatter into the rank-partitioned send buffer (ep_dispatch).
 //
 // send[slot[t, j], :] = x[t, :] and slot_meta[slot[t, j]] = t k + j: each token
-// row goes to the send-buffer row of every selected expert ("each token must
-// be dispatched to the device hosting its selected expert", UBEP article,
-// opening section). This is the data-movement half of the article's kernel
+// row goes to the send-buffer row of every selected expert (the UBEP article,
+// opening section: a token has to reach the device that holds each expert
+// chosen for it). This is the data-movement half of the article's kernel
 // decomposition; on one GPU it is a pure HBM copy: read x once, write k rows.
 //
 // Work unit = (token, segment of 32 * U 16-byte vectors). A warp loads its U

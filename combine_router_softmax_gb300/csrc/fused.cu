@@ -16,10 +16,16 @@
 //      experts and their totals;
 //   E. bounded grid barrier;
 //   F. each CTA reads its tile's bases and the totals, scans the totals into
-//      expert offsets and writes its slots; CTA 0 writes counts and offsets and
-//      the last CTA builds the chunk schedule;
+//      expert offsets and writes its slots; CTA 0 writes counts and offsets.
+//      The chunk schedule is built by one extra CTA that holds no tile (it
+//      joins both barriers, skips steps 0, A, B, D and G, and so overlaps the
+//      schedule with the other CTAs' row copies); with a single tile CTA there
+//      is no extra CTA, that CTA builds it, and the barriers reduce to
+//      __syncthreads;
 //   G. dispatch of the CTA's own tile from the prefetched stages: lanes j < k
-//      bulk-store each row to its k send rows.
+//      bulk-store each row to its k send rows. When the send buffer is small
+//      (<= 16 MB) every CTA signals programmatic dependents here, so that a
+//      combine launched after it can start its prologue early.
 // Every result equals what ep_route, ep_layout and ep_dispatch write.
 #include "block_common.cuh"
 #include "route_token.cuh"

@@ -6,8 +6,9 @@
 // "Kernel Decomposition" replaces the global barriers between those phases by
 // cores that poll global memory for the metadata they need. Here:
 //
-//  * rank phase (every CTA, on its own tokens): a warp walks its 32 tokens in
-//    order with one shared-memory counter per expert (lanes j < k take the k
+//  * rank phase (every CTA, on its own tokens): a warp walks its tpw tokens
+//    (4 to 32, see fused_tiling) in order with one shared-memory counter per
+//    expert (lanes j < k take the k
 //    distinct experts of a token at once), giving each pair its rank among
 //    the warp's earlier pairs of the same expert; the per-warp histograms are
 //    scanned per expert. No atomic decides an order, so slots are
@@ -19,7 +20,9 @@
 //    second kernel). Every CTA then reads the whole [CTA][expert] count table
 //    and computes, redundantly and in parallel, the expert offsets and its
 //    own prefix inside each expert's segment, and writes its final slots.
-//    CTA 0 writes the counts/offsets and the last CTA the chunk schedule.
+//    CTA 0 writes the counts/offsets and the last CTA the chunk schedule,
+//    unless the caller defers the schedule to the dispatch kernel that
+//    follows (its extra CTA builds it while the other CTAs copy rows).
 //
 //  * fallback (T beyond what one co-resident grid holds): three kernels --
 //    rank, a one-CTA scan (+ schedule), finalize.

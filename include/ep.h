@@ -138,8 +138,9 @@ ep_status ep_fused_step_kernel_count(const ep_config *cfg, int32_t *kernels);
 /*
  * ep_route -- router softmax and top-k for every token.
  *
- * Defines (the pages give no router; this is the plainest reading of
- * "each token is dispatched to the device hosting its selected expert"):
+ * Defines (the pages give no router, only that a token travels to the device
+ * of the expert chosen for it, UBEP article, opening section; this is the
+ * plainest gate that chooses experts per token):
  *   p[t, e]       = softmax over all E experts of logits[t, :]
  *   topk_idx[t,:] = the k experts with the largest logits, in descending order;
  *                   equal logits go to the lower expert index. With
