@@ -797,6 +797,17 @@ def run_gb300(args):
     dom = max(kern_ms, key=kern_ms.get)
     peak, peak_kind = measured_peak_gbs()
     achieved = kb[dom] / (kern_ms[dom] * 1e-3) / 1e9
+    # kernels each call launches: ep_dispatch_fused or ep_layout the ones the
+    # step count leaves after the single-kernel calls
+    names = [n for n, _ in calls]
+    multi = "dispatch_fused" if "dispatch_fused" in names else "layout"
+    call_kernels = {n: 1 for n in names}
+    call_kernels[multi] = launches_per_step - (len(names) - 1)
+    by_call = {n: {"us": round(kern_ms[n] * 1e3, 2), "kernels": call_kernels[n],
+                   "algorithmic_bytes": kb[n],
+                   "achieved": round(kb[n] / (kern_ms[n] * 1e-3) / 1e9, 1),
+                   "frac": round(kb[n] / (kern_ms[n] * 1e-3) / 1e9 / peak, 4),
+                   "traffic": ncu_traffic(n, w0.name)} for n in kern_ms}
 
     # end to end: pinned host inputs in, result out, every step
     E2E = args.e2e_steps if args.e2e_steps is not None else min(K, 200)
@@ -855,8 +866,10 @@ def run_gb300(args):
         "roofline": {
             "bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "traffic": ncu_traffic(dom, w0.name),
-            "algorithmic_bytes_per_launch": kb[dom], "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+            "algorithmic_bytes_per_launch": kb[dom], "kernels_in_call": call_kernels[dom],
+            "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
             if peak_kind == "measured" else "fallback 6.8 TB/s",
+            "by_call": by_call,
         },
         "e2e": {"value": round(pipe_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h_logits.numel() * 4 + h_x.numel() * 2,
                 "d2h_bytes_per_step": h_out.numel() * 2, "ms_per_step": round(pipe_ms, 5), "steps": E2E,

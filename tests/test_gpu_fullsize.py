@@ -54,7 +54,62 @@ def test_fullsize(ep, orc, w):
     synthetic_expert(b.send, b.expert_offset, w.E, out=b.y)
     b.combine()
     torch.cuda.synchronize()
+    check_against_oracle(orc, w, b, logits, x)
 
+
+# The benchmark's own launch configuration: ep_dispatch_fused + ep_combine
+# captured once in a CUDA graph and replayed. Small T runs the single fused
+# kernel (with and without its schedule CTA), large T the route, layout and
+# dispatch kernels chained by programmatic dependent launch.
+GRAPH = [
+    ep_synth.get_workload("sweep-uniform-T1"),
+    ep_synth.get_workload("sweep-zipf-T8"),
+    ep_synth.get_workload("sweep-uniform-T64"),
+    ep_synth.CONFIGS["decode"],
+    ep_synth.get_workload("sweep-zipf-T512"),
+    ep_synth.CONFIGS["prefill"],
+    ep_synth.CONFIGS["mid"],
+    ep_synth.get_workload("sweep-zipf-T32768"),
+]
+
+
+def poison_outputs(b):
+    """Every buffer the step writes gets a value no correct step leaves there."""
+    for t in (b.topk_idx, b.expert_count, b.expert_offset, b.rank_count, b.rank_offset, b.slot, b.chunks,
+              b.n_chunks, b.worker_begin, b.slot_meta):
+        t.fill_(-7)
+    b.topk_w.fill_(float("nan"))
+    b.send.view(torch.int16).fill_(-1)  # 0xFFFF: a bf16 NaN
+    b.out.view(torch.int16).fill_(-1)
+
+
+@pytest.mark.parametrize("w", GRAPH, ids=lambda w: w.name)
+def test_fullsize_bench_graph(ep, orc, w):
+    import bench
+
+    logits = ep_synth.gate_logits(w.seed, w.T, w.E, w.zipf_s)
+    x = ep_synth.hidden_bf16_bits(w.seed, w.T, w.H)
+    cfg = ep.EpConfig.from_workload(w)
+    b = ep.LayerBuffers.allocate(cfg)
+    b.logits.copy_(torch.from_numpy(logits))
+    b.x.copy_(bf16_to_dev(x))
+    dev = torch.device("cuda", torch.cuda.current_device())
+    # expert output of this batch, as the benchmark makes it before timing
+    b.bind(torch.cuda.current_stream(dev)).dispatch_fused()
+    synthetic_expert(b.send, b.expert_offset, w.E, out=b.y)
+    torch.cuda.synchronize()
+
+    g = bench.capture_step_graph(b, dev, fused=True)
+    for _ in range(2):  # the second replay starts from what the first left in the workspace
+        poison_outputs(b)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+    assert ep.ep_device_error() == 0
+    check_against_oracle(orc, w, b, logits, x)
+
+
+def check_against_oracle(orc, w, b, logits, x):
     # route + layout + schedule: every token
     idx, w64 = orc.route(logits, w.k, w.n_groups, w.topk_groups, w.renormalize)
     lay = orc.layout(idx, w.E, w.R)
@@ -76,6 +131,7 @@ def test_fullsize(ep, orc, w):
     # sampled tokens: send rows and combine output
     rng = np.random.default_rng(w.T)
     S = np.unique(np.concatenate([[0, 1, w.T // 2, w.T - 1], rng.integers(0, w.T, size=96)]))
+    S = S[S < w.T]
     send_rows = bf16_from_dev(b.send[torch.from_numpy(lay["slot"][S].ravel()).long().cuda()])
     assert np.array_equal(send_rows, np.repeat(x[S], w.k, axis=0)), "send rows differ from x"
 
