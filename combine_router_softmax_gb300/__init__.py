@@ -146,6 +146,10 @@ def _ptr(t: torch.Tensor | None, dtype: torch.dtype, shape: tuple | None, name: 
         raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
     if not t.is_cuda:
         raise ValueError(f"{name}: must be a CUDA tensor")
+    cur = torch.cuda.current_device()
+    if t.device.index != cur:
+        # the kernels run on the current device and would dereference another device's memory
+        raise ValueError(f"{name}: on {t.device}, but the current device is cuda:{cur}")
     if not t.is_contiguous():
         raise ValueError(f"{name}: must be contiguous")
     if shape is not None and tuple(t.shape) != tuple(shape):
@@ -156,6 +160,8 @@ def _ptr(t: torch.Tensor | None, dtype: torch.dtype, shape: tuple | None, name: 
 def _stream(stream) -> ctypes.c_void_p:
     if stream is None:
         stream = torch.cuda.current_stream()
+    elif stream.device.index != torch.cuda.current_device():
+        raise ValueError(f"stream: on {stream.device}, but the current device is cuda:{torch.cuda.current_device()}")
     return ctypes.c_void_p(stream.cuda_stream)
 
 

@@ -146,11 +146,10 @@ combine_kernel_rt(const uint4 *__restrict__ y, const int32_t *__restrict__ slot,
 }
 
 int grid_for(const void *kern, int64_t units) {
-    int dev = 0;
-    cudaGetDevice(&dev);
     const int occ = max_blocks_per_sm(kern, kCombineThreads, 0);
     const int64_t want = (units * 32 + kCombineThreads - 1) / kCombineThreads;
-    const int64_t cap = (int64_t)sm_count(dev) * occ;
+    // 0 if the device query failed: the launch then reports the error
+    const int64_t cap = (int64_t)current_device_sm_count() * occ;
     return (int)(want < cap ? want : cap);
 }
 

@@ -83,11 +83,10 @@ cudaError_t launch_k(const ep_config &c, const ep_bf16 *x, const int32_t *slot, 
     const int32_t segs = (hv + 32 * kDispatchU - 1) / (32 * kDispatchU);
     const int64_t units = (int64_t)c.T * segs;
     const int64_t rows = (int64_t)c.T * c.k;
-    int dev = 0;
-    cudaGetDevice(&dev);
     const int occ = max_blocks_per_sm(reinterpret_cast<const void *>(dispatch_kernel<K>), kDispatchThreads, 0);
     const int64_t want = (units * 32 + kDispatchThreads - 1) / kDispatchThreads;
-    const int64_t cap = (int64_t)sm_count(dev) * occ;
+    // 0 if the device query failed: the launch then reports the error
+    const int64_t cap = (int64_t)current_device_sm_count() * occ;
     const int64_t grid = want < cap ? want : cap;
     dispatch_kernel<K><<<(unsigned)grid, kDispatchThreads, 0, s>>>(
         reinterpret_cast<const uint4 *>(x), slot, reinterpret_cast<uint4 *>(send), meta, c.k, hv, segs, units,
@@ -255,7 +254,7 @@ cudaError_t launch_bulk(const ep_config &c, const ep_bf16 *x, const int32_t *slo
     int dev = 0;
     cudaError_t e = current_device(&dev);
     if (e != cudaSuccess) return e;
-    static bool attr_set[kMaxDevices_] = {false};
+    static std::atomic<bool> attr_set[kMaxDevices_];  // zero-initialised: false
     if (!attr_set[dev]) {
         e = cudaFuncSetAttribute(dispatch_bulk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
         if (e != cudaSuccess) return e;
@@ -294,7 +293,7 @@ cudaError_t launch_bulk(const ep_config &c, const ep_bf16 *x, const int32_t *slo
 }  // namespace
 
 cudaError_t dispatch_error_word(int32_t **addr) {
-    static int32_t *cached[kMaxDevices_] = {nullptr};
+    static std::atomic<int32_t *> cached[kMaxDevices_];  // zero-initialised: null
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;

@@ -6,6 +6,7 @@
 // launchers.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
 

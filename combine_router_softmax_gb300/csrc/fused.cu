@@ -366,7 +366,7 @@ bool plan_fused(const ep_config &c, FusedPlan *p) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices_) return false;
     const FusedKernel kern = pick_kernel(c.E);
-    static bool attr_set[kMaxDevices_][6] = {};
+    static std::atomic<bool> attr_set[kMaxDevices_][6];  // zero-initialised: false
     const int vi = ((c.E + 31) / 32 <= 1) ? 0 : ((c.E + 31) / 32 <= 2) ? 1 : ((c.E + 31) / 32 <= 4) ? 2
                  : ((c.E + 31) / 32 <= 8) ? 3 : ((c.E + 31) / 32 <= 16) ? 4 : 5;
     if (!attr_set[dev][vi]) {
@@ -423,7 +423,7 @@ bool plan_fused(const ep_config &c, FusedPlan *p) {
 }  // namespace
 
 cudaError_t fused_error_word(int32_t **addr) {
-    static int32_t *cached[kMaxDevices_] = {nullptr};
+    static std::atomic<int32_t *> cached[kMaxDevices_];  // zero-initialised: null
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;

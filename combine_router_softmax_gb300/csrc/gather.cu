@@ -200,7 +200,7 @@ cudaError_t launch_dispatch_scheduled(const ep_config &c, int32_t W, const ep_bf
     const GatherPlan p = plan_gather(c, W);
     int dev = 0;
     if ((e = current_device(&dev)) != cudaSuccess) return e;
-    static bool attr_set[kMaxDevices_] = {false};
+    static std::atomic<bool> attr_set[kMaxDevices_];  // zero-initialised: false
     if (!attr_set[dev]) {
         if ((e = cudaFuncSetAttribute(dispatch_gather_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       (int)(kGatherStageBudget + 4096))) != cudaSuccess)

@@ -358,7 +358,7 @@ static bool layout_fused_fits(const ep_config &c, int *nw_out, int64_t *nb_out, 
     if (nw == 0) return false;
     const int64_t nb = t.nb;
     const size_t smem = fused_smem_bytes(nw, t.tpw, c.E, c.R, c.k);
-    static bool attr_set[kMaxDevices_] = {false};
+    static std::atomic<bool> attr_set[kMaxDevices_];  // zero-initialised: false
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices_) return false;
     if (!attr_set[dev]) {

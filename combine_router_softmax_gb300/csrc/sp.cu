@@ -302,7 +302,7 @@ size_t sp_smem(int row_pad, int32_t E) {
 }  // namespace
 
 cudaError_t sp_error_word(int32_t **addr) {
-    static int32_t *cached[kMaxDevices_] = {nullptr};
+    static std::atomic<int32_t *> cached[kMaxDevices_];  // zero-initialised: null
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -354,7 +354,7 @@ cudaError_t launch_handoff(const ep_config &c, int32_t W, const ep_bf16 *x, cons
     int dev = 0;
     cudaError_t e = current_device(&dev);
     if (e != cudaSuccess) return e;
-    static bool attr_set[kMaxDevices_] = {false};
+    static std::atomic<bool> attr_set[kMaxDevices_];  // zero-initialised: false
     if (!attr_set[dev]) {
         if ((e = cudaFuncSetAttribute(dispatch_expert_sp_kernel<kSW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       110 * 1024)) != cudaSuccess)

@@ -4,8 +4,8 @@
  *
  * The operations are the ones the UBEP article ("NJU x Huawei UBEP:
  * Reengineering MoE Expert Parallelism", kad8.com) names for an expert-parallel
- * communication library: each token is dispatched to the device that hosts each
- * of its selected experts and gathered back in the Combine phase (opening
+ * communication library: a token goes to the device of each expert chosen for
+ * it, and the experts' outputs return to it in the Combine step (opening
  * section); the dispatch needs token counts, offsets from prefix sums and a
  * reordering of tokens ("Three Bottlenecks" / BSP Serialization, "Kernel
  * Decomposition"); and per-worker traffic is balanced across hop-latency
@@ -212,8 +212,9 @@ ep_status ep_layout(const ep_config *cfg, const int32_t *topk_idx,
 
 /*
  * ep_dispatch -- scatter each token row to the send-buffer rows of its k
- * slots ("each token must be dispatched to the device hosting its selected
- * expert"; here the send buffer is partitioned by destination rank):
+ * slots (UBEP article, opening section: a token has to reach the device that
+ * holds each expert chosen for it; here the send buffer is partitioned by
+ * destination rank):
  *   send[slot[t, j], :] = x[t, :]        (bit copy)
  *   slot_meta[slot[t, j]] = t k + j      (source token and top-k position)
  *
@@ -384,8 +385,8 @@ ep_status ep_dispatch_expert_sp(const ep_config *cfg, const ep_bf16 *x, const in
 
 /*
  * ep_combine -- gather the k expert-output rows of every token back to token
- * order and sum them with the top-k weights ("later gathered during the
- * Combine phase"):
+ * order and sum them with the top-k weights (UBEP article, opening section:
+ * the expert outputs come back to their token in the Combine step):
  *   acc = 0; for j = 0 .. k-1: acc = fmaf(topk_w[t, j], y[slot[t, j], h], acc)
  *   out[t, h] = bf16 round-to-nearest-even(acc)
  * in fp32 with one fused multiply-add per term, in fixed j order.

@@ -314,8 +314,8 @@ int orc_schedule(int32_t R, int32_t ranks_per_node, int32_t ranks_per_pod, int32
 /* ------------------------------------------------------------------------- */
 
 /*
- * Dispatch (UBEP article, opening section: each token is sent to the device
- * hosting its selected expert): every token row is copied, bit for bit, to
+ * Dispatch (UBEP article, opening section: a token travels to the device that
+ * holds each expert chosen for it): every token row is copied, bit for bit, to
  * the send-buffer row of each of its k slots, and that row records where it
  * came from:  send[slot[t, j], :] = x[t, :],  meta[slot[t, j]] = t k + j.
  */

@@ -305,6 +305,20 @@ def test_argument_errors(ep):
     assert ei.value.status == ep.EP_ERR_CAPACITY
 
 
+def test_tensor_on_another_device_rejected(ep, monkeypatch):
+    """The binding refuses tensors (and streams) of a device other than the
+    current one before anything is launched; one GPU is enough to check it by
+    making the binding believe another device is current."""
+    cfg = ep.EpConfig.make(T=16, H=16, E=8, R=4, k=2, num_workers=4)
+    b = ep.LayerBuffers.allocate(cfg)
+    stream = torch.cuda.current_stream()
+    monkeypatch.setattr(torch.cuda, "current_device", lambda: 1)
+    with pytest.raises(ValueError, match="current device is cuda:1"):
+        ep.ep_dispatch(cfg, b.x, b.slot, b.send, b.slot_meta)
+    with pytest.raises(ValueError, match="stream: on cuda:0"):
+        ep._stream(stream)
+
+
 @pytest.mark.parametrize("E,k,renorm", [(4, 1, 1), (4, 3, 0), (16, 5, 1), (32, 8, 1), (32, 2, 0), (64, 4, 1),
                                         (128, 8, 0), (512, 6, 1), (1024, 8, 1), (1024, 7, 0), (96, 8, 1)])
 def test_route_shapes(ep, orc, E, k, renorm):
