@@ -140,23 +140,30 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        sm, smax, reasons = [], None, set()
-        for line in out.strip().splitlines():
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 10:
-                continue
-            try:
-                sm.append(float(f[2]))
-                smax = float(f[3])
-            except ValueError:
-                continue
-            names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-            for name, val in zip(names, f[6:10]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": len(sm)}
+        return parse_clock_samples(out)
+
+
+def parse_clock_samples(out: str) -> dict:
+    """Median SM clock, max clock and the throttle reasons seen in nvidia-smi
+    CSV lines of ``ClockSampler.QUERY`` (noheader, nounits); lines that do not
+    parse are skipped."""
+    sm, smax, reasons = [], None, set()
+    for line in out.strip().splitlines():
+        f = [x.strip() for x in line.split(",")]
+        if len(f) < 10:
+            continue
+        try:
+            sm.append(float(f[2]))
+            smax = float(f[3])
+        except ValueError:
+            continue
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for name, val in zip(names, f[6:10]):
+            if val.lower() == "active":
+                reasons.add(name)
+    if not sm:
+        return {"sm_mhz": None, "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": 0}
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": len(sm)}
 
 
 # ---------------------------------------------------------------------------

@@ -1,0 +1,98 @@
+"""Host logic of the benchmark that decides what its JSON line reports (CPU).
+
+The byte accounting is pinned to hand-computed totals, the nvidia-smi clock
+parser to made-up sample lines, and the DRAM-traffic lookup to the rule that
+a capture stops counting once the kernel source it was taken on changes.
+"""
+from __future__ import annotations
+
+import json
+
+import pytest
+
+import bench
+import ep_synth
+
+
+def test_prefill_bytes_by_hand():
+    """T=4096, H=7168, E=256, R=32, k=8, worked out term by term:
+    route    T E 4 + T k 8                 =   4,194,304 +     262,144
+    layout   T k 8 + (2E + 2R + 2) 4       =     262,144 +       2,312
+    dispatch T H 2 + T k H 2 + T k 8       =  58,720,256 + 469,762,048 + 262,144
+    combine  T k H 2 + T k 8 + T H 2       = 469,762,048 +     262,144 + 58,720,256"""
+    w = ep_synth.CONFIGS["prefill"]
+    kb = w.algorithmic_bytes()
+    assert kb["route"] == 4_456_448
+    assert kb["layout"] == 264_456
+    assert kb["dispatch"] == 528_744_448
+    assert kb["combine"] == 528_744_448
+    assert w.total_bytes() == 1_062_209_800
+    assert bench.call_bytes(w, "dispatch_fused") == 4_456_448 + 264_456 + 528_744_448
+    assert bench.call_bytes(w, "combine") == 528_744_448
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "prefill", "mid", "sweep-zipf-T1", "sweep-uniform-T32768"])
+def test_step_bytes_are_the_sum_of_the_calls(name):
+    w = ep_synth.get_workload(name) if name.startswith("sweep") else ep_synth.CONFIGS[name]
+    fused = sum(bench.call_bytes(w, n) for n in ("dispatch_fused", "combine"))
+    separate = sum(bench.call_bytes(w, n) for n in ("route", "layout", "dispatch", "combine"))
+    assert fused == separate == w.total_bytes()
+    # collected by term: rows 4 T H (k + 1) (x read, k send rows written, k y rows read, out written),
+    # logits 4 T E, the eight T k int32/fp32 arrays 32 T k, counts and offsets 8 (E + R + 1)
+    T, H, E, R, k = w.T, w.H, w.E, w.R, w.k
+    assert w.total_bytes() == 4 * T * H * (k + 1) + 4 * T * E + 32 * T * k + 8 * (E + R + 1)
+
+
+def _line(sm, smax, *active):
+    names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+    flags = ", ".join("Active" if n in active else "Not Active" for n in names)
+    return f"2026/12/02 10:00:00.000, 0, {sm}, {smax}, 812.40, 0x0000000000000000, {flags}"
+
+
+def test_clock_parser_median_and_reasons():
+    out = "\n".join([_line(2070, 2070), _line(1980, 2070, "sw_power_cap"), _line(2055, 2070)])
+    c = bench.parse_clock_samples(out)
+    assert c == {"sm_mhz": 2055.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 3}
+
+
+def test_clock_parser_reports_every_throttle_reason_seen():
+    out = "\n".join([_line(1500, 2070, "hw_slowdown"), _line(1400, 2070, "hw_thermal_slowdown", "sw_thermal_slowdown")])
+    c = bench.parse_clock_samples(out)
+    assert c["reasons"] == ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"]
+    assert c["sm_mhz"] == 1450.0
+
+
+def test_clock_parser_skips_lines_it_cannot_read():
+    out = "\n".join(["", "garbage", "a, b, [N/A], [N/A], x, y, z, w, v, u", _line(2070, 2070)])
+    assert bench.parse_clock_samples(out) == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 1}
+    assert bench.parse_clock_samples("")["sm_mhz"] is None
+
+
+def test_code_only_ignores_comments_and_blank_space():
+    a = "int f(int x) {\n    return x + 1;  // one more\n}\n"
+    b = "/* header\n   text */\nint f(int x) {\n\n        return x + 1;\n}\n"
+    c = "int f(int x) {\n    return x + 2;\n}\n"
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only(a) != bench._code_only(c)
+
+
+def test_traffic_summary_entries_are_complete():
+    data = json.loads((bench.ROOT / "profiles" / "dram_traffic.txt").read_text())
+    assert "ncu" in data["command"] and "--clock-control none" in data["command"]
+    for kernel, ent in data["prefill"].items():
+        assert kernel in bench.KERNEL_SOURCES
+        assert isinstance(ent["dram_bytes_per_launch"], int) and ent["dram_bytes_per_launch"] > 0
+        assert len(ent["source_sha256_16"]) == 16
+    p = data["prefill"]
+    assert p["dispatch_fused"]["dram_bytes_per_launch"] == sum(
+        p[k]["dram_bytes_per_launch"] for k in ("route", "layout", "dispatch"))
+
+
+def test_traffic_is_dropped_once_the_kernel_source_changes(monkeypatch):
+    data = json.loads((bench.ROOT / "profiles" / "dram_traffic.txt").read_text())
+    kernel = "combine"
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda k: data["prefill"][k]["source_sha256_16"])
+    assert bench.ncu_traffic(kernel, "prefill") == data["prefill"][kernel]["dram_bytes_per_launch"]
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda k: "0" * 16)
+    assert bench.ncu_traffic(kernel, "prefill") is None
+    assert bench.ncu_traffic(kernel, "no-such-workload") is None
