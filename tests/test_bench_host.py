@@ -7,6 +7,8 @@ a capture stops counting once the kernel source it was taken on changes.
 from __future__ import annotations
 
 import json
+import os
+import time
 
 import pytest
 
@@ -96,3 +98,20 @@ def test_traffic_is_dropped_once_the_kernel_source_changes(monkeypatch):
     monkeypatch.setattr(bench, "kernel_source_hash", lambda k: "0" * 16)
     assert bench.ncu_traffic(kernel, "prefill") is None
     assert bench.ncu_traffic(kernel, "no-such-workload") is None
+
+
+def test_clock_sampler_with_a_fake_nvidia_smi(tmp_path, monkeypatch):
+    """The sampler starts nvidia-smi, stops it and parses what it printed; a
+    stand-in script on PATH prints two samples, then waits to be stopped."""
+    fake = tmp_path / "nvidia-smi"
+    fake.write_text("#!/bin/sh\n"
+                    f"echo '{_line(2070, 2070)}'\n"
+                    f"echo '{_line(2040, 2070, 'sw_power_cap')}'\n"
+                    "exec sleep 30\n")
+    fake.chmod(0o755)
+    monkeypatch.setenv("PATH", f"{tmp_path}{os.pathsep}{os.environ['PATH']}")
+    s = bench.ClockSampler(0)
+    time.sleep(0.5)
+    c = s.stop()
+    assert c == {"sm_mhz": 2055.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 2}
+    assert bench.ClockSampler(0, enabled=False).stop() is None
