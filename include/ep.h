@@ -240,8 +240,9 @@ ep_status ep_dispatch(const ep_config *cfg, const ep_bf16 *x, const int32_t *slo
  * are latency-bound; when a CTA would have to route more than 8 tokens (T
  * above 8 tokens per resident CTA, about 2400 on a GB300) the call runs the
  * three separate steps instead (the route kernel zeroing the layout's and
- * dispatch's counters, the dispatch taking tokens dynamically), with the same
- * results.
+ * dispatch's counters, the dispatch taking tokens dynamically and building
+ * the chunk schedule in one extra CTA while the others copy rows), with the
+ * same results.
  *
  * workspace : >= ep_dispatch_fused_workspace_size bytes, 256-byte aligned.
  * A CTA that gives up a bounded wait sets ep_device_error bit 1 (2) and
