@@ -21,6 +21,14 @@
  *    array of ep_layout_static, below).
  *  - Work is enqueued on `stream` (0 = legacy default stream) and is
  *    asynchronous: results are ready when the stream reaches that point.
+ *    ep_combine, and the dispatch kernel inside ep_dispatch_fused, are
+ *    launched as programmatic dependents of the kernel before them on the
+ *    stream: their CTAs may become resident early, but each waits for that
+ *    kernel to complete (griddepcontrol.wait) before it touches memory. Stream
+ *    order is therefore kept whenever that kernel itself ends after the work
+ *    queued before it -- any kernel launched without programmatic stream
+ *    serialization, or one launched with it that waits on its own
+ *    predecessor before it ends.
  *  - bf16 tensors are passed as `ep_bf16` (the 16-bit pattern of a bfloat16).
  *    x, send, y and out must be 16-byte aligned; H must be a multiple of 8 so
  *    that every row is a whole number of 16-byte vectors.
