@@ -425,8 +425,8 @@ ep_status ep_combine(const ep_config *cfg, const ep_bf16 *y, const int32_t *slot
  * cudaMalloc, cudaFree or other allocating routine.
  *  - Limit: shapes whose ep_layout_workspace_size exceeds
  *    EP_LAYOUT_STATIC_SCRATCH_BYTES return EP_ERR_CAPACITY with nothing
- *    enqueued (the size is about 4 * E * ceil(T / 256) bytes: e.g. E = 256
- *    allows T <= 262144 tokens).
+ *    enqueued (the size is at most 4 E max(ceil(T / 256), 64) + 512 bytes:
+ *    e.g. E = 256 allows T <= 262144 tokens).
  *  - Set-up: the first call on a device (made with that device current) looks
  *    up the array's device address; make that first call before any stream
  *    capture. Later calls on the device reuse the address.

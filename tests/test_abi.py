@@ -105,13 +105,31 @@ def test_pod_tier_capacity_and_validation(lib):
         assert rc == lib.EP_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("E,R,k", [(8, 4, 2), (256, 32, 8), (128, 16, 8), (96, 6, 12), (1024, 32, 32)])
+def test_layout_workspace_within_the_documented_bound(lib, E, R, k):
+    """include/ep.h: the layout's scratch is at most 4 E max(ceil(T / 256), 64)
+    + 512 bytes and at least the three-kernel layout's 4 E ceil(T / 256)."""
+    for T in (1, 63, 64, 1000, 2049, 4096, 16385, 32768, 32769, 65536, 100000, 262144):
+        n = lib.ep_layout_workspace_size(lib.EpConfig.make(T=T, H=64, E=E, R=R, k=k, num_workers=8))
+        blocks = (T + 255) // 256
+        assert 4 * E * blocks <= n <= 4 * E * max(blocks, 64) + 512, (T, n)
+
+
+def test_static_layout_limit_is_the_documented_one(lib):
+    """E = 256 fits ep_layout_static's 1 MiB array up to T = 262144 and no further."""
+    def ws(T):
+        return lib.ep_layout_workspace_size(lib.EpConfig.make(T=T, H=64, E=256, R=32, k=8, num_workers=8))
+
+    assert ws(262144) <= lib.EP_LAYOUT_STATIC_SCRATCH_BYTES < ws(262145)
+
+
 def test_layout_capacity_and_workspace_errors(lib):
     L = lib._lib
     cfg = _cfg(lib, T=1000)
     cap = lib.ep_schedule_capacity(cfg)
     assert cap == 2 * 8 + 4
     ws = lib.ep_layout_workspace_size(cfg)
-    assert ws >= 16 * 4 * 4 and ws % 256 == 0  # 4 layout CTAs x 16 experts
+    assert ws >= 16 * 4 * 4 and ws % 256 == 0  # at least the three-kernel layout's 4 CTAs x 16 experts
     args = [FAKE] * 6
     # chunk table too small
     rc = L.ep_layout(ctypes.byref(cfg), *args, FAKE, ctypes.c_int32(cap - 1), FAKE, FAKE, FAKE,
