@@ -104,14 +104,18 @@ def test_clock_sampler_with_a_fake_nvidia_smi(tmp_path, monkeypatch):
     """The sampler starts nvidia-smi, stops it and parses what it printed; a
     stand-in script on PATH prints two samples, then waits to be stopped."""
     fake = tmp_path / "nvidia-smi"
+    printed = tmp_path / "printed"
     fake.write_text("#!/bin/sh\n"
                     f"echo '{_line(2070, 2070)}'\n"
                     f"echo '{_line(2040, 2070, 'sw_power_cap')}'\n"
+                    f"touch '{printed}'\n"
                     "exec sleep 30\n")
     fake.chmod(0o755)
     monkeypatch.setenv("PATH", f"{tmp_path}{os.pathsep}{os.environ['PATH']}")
     s = bench.ClockSampler(0)
-    time.sleep(0.5)
+    deadline = time.monotonic() + 20
+    while not printed.exists() and time.monotonic() < deadline:
+        time.sleep(0.05)
     c = s.stop()
     assert c == {"sm_mhz": 2055.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 2}
     assert bench.ClockSampler(0, enabled=False).stop() is None
