@@ -338,6 +338,93 @@ def pin_combine_fp64_bound(o):
     assert (np.abs(out - exact) <= bound).all()
 
 
+def _round_to_bits(q, mant_bits: int):
+    """The rational q rounded to the nearest binary number of `mant_bits`
+    significant bits, ties to the even one (normal range, exponent >= -126)."""
+    from fractions import Fraction
+
+    if q == 0:
+        return Fraction(0)
+    sign = -1 if q < 0 else 1
+    a = abs(q)
+    e = a.numerator.bit_length() - a.denominator.bit_length()  # 2^(e-1) < a < 2^(e+1)
+    if Fraction(2) ** e > a:
+        e -= 1
+    e = max(e, -126)  # now 2^e <= a < 2^(e+1)
+    ulp = Fraction(2) ** (e - (mant_bits - 1))
+    n, rem = divmod(a / ulp, 1)
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    return sign * n * ulp
+
+
+def _fma_chain_bf16(w_row, y_cols, order):
+    """acc = 0; acc = fp32(w_j * y_j + acc) for j in `order` (one rounding of the
+    exact product-sum per term, as a fused multiply-add does); bf16 RNE of acc.
+    Exact rational arithmetic throughout."""
+    from fractions import Fraction
+
+    acc = Fraction(0)
+    for j in order:
+        acc = _round_to_bits(Fraction(float(w_row[j])) * Fraction(float(y_cols[j])) + acc, 24)
+    out = np.float32(float(_round_to_bits(acc, 8)))
+    return np.uint16(out.view(np.uint32) >> np.uint32(16))
+
+
+def pin_combine_exact_fma_chain(o):
+    """The combine equals its definition computed exactly: one fused multiply-add
+    per term in j = 0 .. k-1 order (exact product plus accumulator, rounded once to
+    fp32), then bf16 round-to-nearest-even. Half of the tokens are built so that
+    the order and the single rounding decide the result: their first two terms
+    cancel exactly (w_1 = -w_0, y_1 = y_0, large) and the last two are small, so a
+    sum in another order, or with the product rounded before the add, leaves a
+    different residue; the pin checks that those alternatives do differ here."""
+    g = _rng(21)
+    T, H, k = 48, 24, 4
+    w = np.empty((T, k), np.float32)
+    yv = np.empty((T, k, H), np.float32)
+    for t in range(T):
+        if t % 2 == 0:  # cancelling pair, then two small terms
+            w0 = np.float32(g.uniform(0.5, 1.0))
+            w[t] = [w0, -w0, g.uniform(-1, 1), g.uniform(-1, 1)]
+            big = np.ldexp(g.uniform(1, 2, H), g.integers(0, 7, H)) * g.choice([-1, 1], H)
+            yv[t, 0] = yv[t, 1] = big
+            yv[t, 2:] = np.ldexp(g.uniform(1, 2, (2, H)), g.integers(-14, -9, (2, H))) * g.choice([-1, 1], (2, H))
+        else:  # arbitrary terms, mixed signs
+            w[t] = g.uniform(-1, 1, k)
+            yv[t] = g.normal(size=(k, H)) * 4
+    ybits_t = ep_synth.bf16_bits_from_f32(yv.reshape(-1)).reshape(T, k, H)
+    slot = g.permutation(T * k).astype(np.int32).reshape(T, k)
+    y = np.zeros((T * k, H), np.uint16)
+    y[slot.reshape(-1)] = ybits_t.reshape(T * k, H)
+    out = o.combine(y, slot, w)
+    yf = ep_synth.bf16_bits_to_f32(ybits_t)
+
+    def sign_free(b):
+        return np.where(b == 0x8000, 0, b)
+
+    forward = reverse = 0
+    two_roundings = 0
+    for t in range(T):
+        for h in range(H):
+            ref = _fma_chain_bf16(w[t], yf[t, :, h], range(k))
+            assert sign_free(out[t, h]) == sign_free(ref), (t, h, hex(out[t, h]), hex(ref))
+            forward += 1
+            if t % 2 == 0:
+                reverse += int(_fma_chain_bf16(w[t], yf[t, :, h], range(k - 1, -1, -1)) != ref)
+                # product rounded to fp32 first, then the add rounded again
+                from fractions import Fraction
+
+                acc = Fraction(0)
+                for j in range(k):
+                    p = _round_to_bits(Fraction(float(w[t, j])) * Fraction(float(yf[t, j, h])), 24)
+                    acc = _round_to_bits(p + acc, 24)
+                alt = np.uint16(np.float32(float(_round_to_bits(acc, 8))).view(np.uint32) >> np.uint32(16))
+                two_roundings += int(alt != ref)
+    assert forward == T * H
+    assert reverse > 0 and two_roundings > 0, (reverse, two_roundings)
+
+
 def pin_bf16_rounding(o):
     """The oracle's float -> bf16 rounding equals torch's (RNE) on ties, carries,
     overflow, subnormals and signed zeros."""

@@ -56,6 +56,21 @@ MUTANTS = [
     ("combine drops the last term",
      "            for (int32_t j = 0; j < k; ++j) {\n                int64_t s = slot[t * k + j];\n                if (s < 0 || s >= T * k) return ORC_EINVAL;\n                acc",
      "            for (int32_t j = 0; j < k - 1; ++j) {\n                int64_t s = slot[t * k + j];\n                if (s < 0 || s >= T * k) return ORC_EINVAL;\n                acc"),
+    ("combine sums the terms in reverse order",
+     "                int64_t s = slot[t * k + j];\n                if (s < 0 || s >= T * k) return ORC_EINVAL;\n"
+     "                acc = fmaf(w[t * k + j], orc_bf16_to_f32(y[s * H + h]), acc);",
+     "                int64_t s = slot[t * k + (k - 1 - j)];\n                if (s < 0 || s >= T * k) return ORC_EINVAL;\n"
+     "                acc = fmaf(w[t * k + (k - 1 - j)], orc_bf16_to_f32(y[s * H + h]), acc);"),
+    ("combine rounds the product before the add",
+     "acc = fmaf(w[t * k + j], orc_bf16_to_f32(y[s * H + h]), acc);",
+     "acc = w[t * k + j] * orc_bf16_to_f32(y[s * H + h]) + acc;"),
+    ("combine accumulates in double",
+     "            float acc = 0.0f;\n            for (int32_t j = 0; j < k; ++j) {\n"
+     "                int64_t s = slot[t * k + j];\n                if (s < 0 || s >= T * k) return ORC_EINVAL;\n"
+     "                acc = fmaf(w[t * k + j], orc_bf16_to_f32(y[s * H + h]), acc);",
+     "            double acc = 0.0;\n            for (int32_t j = 0; j < k; ++j) {\n"
+     "                int64_t s = slot[t * k + j];\n                if (s < 0 || s >= T * k) return ORC_EINVAL;\n"
+     "                acc = fma((double)w[t * k + j], (double)orc_bf16_to_f32(y[s * H + h]), acc);"),
     ("TFF payload written over the metadata",
      "memcpy(blk + ORC_TFF_META, in + r * row_bytes + off, (size_t)n);", "memcpy(blk, in + r * row_bytes + off, (size_t)n);"),
     ("TFF last block claims a full payload",
