@@ -70,6 +70,12 @@ def pin_route_group_bruteforce(o):
             kept = sorted(range(ng), key=lambda q: (-score[q], q))[:tg]
             elig = [(e // gs) in kept for e in range(E)]
             assert list(idx[t]) == _sorted_topk(l[t], k, elig), (E, ng, tg, k, t)
+        # unrenormalised weights are entries of the softmax over ALL E experts
+        # (the group limit restricts the choice, not the softmax)
+        idx_raw, w_raw = o.route(l, k, ng, tg, renormalize=0)
+        full = scipy.special.softmax(l.astype(np.float64), axis=1)
+        assert np.array_equal(idx_raw, idx)
+        assert np.allclose(w_raw, np.take_along_axis(full, idx_raw.astype(np.int64), axis=1), rtol=1e-12, atol=0)
         # keeping every group is no limit at all
         idx_all, w_all = o.route(l, k, ng, ng)
         idx_plain, w_plain = o.route(l, k, 1, 1)

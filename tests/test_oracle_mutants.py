@@ -27,6 +27,17 @@ MUTANTS = [
      "w[t * k + j] = p[idx[t * k + j]];"),
     ("softmax denominator not shifted by the max",
      "            S += p[e];", "            S += exp((double)l[e]);"),
+    ("softmax exponent in fp32",
+     "p[e] = exp((double)l[e] - m);", "p[e] = (double)expf((float)((double)l[e] - m));"),
+    ("group score is the sum",
+     "if (l[g * gsize + i] > s) s = l[g * gsize + i];", "s += l[g * gsize + i];"),
+    ("softmax over the eligible experts only",
+     "p[e] = exp((double)l[e] - m);", "p[e] = eligible[e] ? exp((double)l[e] - m) : 0.0;"),
+    ("renormalisation over all E",
+     "for (int32_t j = 0; j < k; ++j) s += p[idx[t * k + j]];", "for (int32_t j = 0; j < E; ++j) s += p[j];"),
+    ("rank count taken from the rank's first expert",
+     "for (int32_t r = 0; r < R; ++r) rank_count[r] = rank_offset[r + 1] - rank_offset[r];",
+     "for (int32_t r = 0; r < R; ++r) rank_count[r] = expert_count[r * epr];"),
     ("rank offset indexed by rank, not by first expert",
      "rank_offset[r] = expert_offset[r * epr];", "rank_offset[r] = expert_offset[r];"),
     ("offset scan off by one expert",
@@ -48,6 +59,12 @@ MUTANTS = [
      "r / ranks_per_node != self_rank / ranks_per_pod) return 2;"),
     ("pod tier folded into the node tier",
      "self_rank / ranks_per_pod) return 2;", "self_rank / ranks_per_pod) return 1;"),
+    ("schedule chunk at position 0 one row long",
+     "rec[4] = (int32_t)(b - a);", "rec[4] = (int32_t)(b - a + (a == 0));"),
+    ("schedule worker_begin[W] one short",
+     "    worker_begin[W] = n;\n", "    worker_begin[W] = n - (n > 0);\n"),
+    ("meta drops the top-k position",
+     "meta[s] = (int32_t)(t * k + j);", "meta[s] = (int32_t)(t * k);"),
     ("meta transposed",
      "meta[s] = (int32_t)(t * k + j);", "meta[s] = (int32_t)(j * T + t);"),
     ("combine weight operand transposed",
@@ -71,6 +88,18 @@ MUTANTS = [
      "            double acc = 0.0;\n            for (int32_t j = 0; j < k; ++j) {\n"
      "                int64_t s = slot[t * k + j];\n                if (s < 0 || s >= T * k) return ORC_EINVAL;\n"
      "                acc = fma((double)w[t * k + j], (double)orc_bf16_to_f32(y[s * H + h]), acc);"),
+    ("expert scale e / E",
+     "float scale = (float)(e + 1) / (float)E;", "float scale = (float)e / (float)E;"),
+    ("expert ownership boundary off by one",
+     "while (e < E - 1 && s >= expert_offset[e + 1]) ++e;", "while (e < E - 1 && s > expert_offset[e + 1]) ++e;"),
+    ("TFF decoder ignores the epoch",
+     "if (orc_get_u32(blk + 0) != epoch ||", "if (0 ||"),
+    ("TFF decoder ignores the block index",
+     "orc_get_u32(blk + 8) != (uint32_t)b ||", "0 ||"),
+    ("TFF decoder ignores the length",
+     "orc_get_u32(blk + 12) != (uint32_t)n) {", "0) {"),
+    ("TFF payload not zero-filled",
+     "            memset(blk, 0, ORC_TFF_BLOCK);\n", "            memset(blk, 0, ORC_TFF_META);\n"),
     ("TFF payload written over the metadata",
      "memcpy(blk + ORC_TFF_META, in + r * row_bytes + off, (size_t)n);", "memcpy(blk, in + r * row_bytes + off, (size_t)n);"),
     ("TFF last block claims a full payload",
