@@ -2,8 +2,11 @@
 rejects bad arguments on the host before touching the GPU. CPU only: no call
 here reaches a kernel launch or a CUDA API call."""
 import ctypes
+import os
 import pathlib
 import re
+import shutil
+import subprocess
 
 import pytest
 
@@ -212,3 +215,48 @@ def test_added_entry_points_reject_bad_arguments(lib):
     big = _cfg(lib, H=32768, k=4)
     assert L.ep_dispatch_scheduled(ctypes.byref(big), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == \
         lib.EP_ERR_UNSUPPORTED
+
+
+def test_header_is_plain_c(lib, tmp_path):
+    """include/ep.h compiles as C11 with every warning an error, and a C program
+    that names every entry point links against the library and calls the
+    host-only ones (no GPU needed)."""
+    gcc = shutil.which("gcc")
+    cuda_inc = pathlib.Path(os.environ.get("CUDA_HOME", "/usr/local/cuda")) / "include"
+    if not gcc or not (cuda_inc / "cuda_runtime_api.h").exists():
+        pytest.skip("gcc or the CUDA headers are not available")
+    names = declared_functions()
+    table = ",\n    ".join(f"(fn_t){n}" for n in names)
+    src = tmp_path / "use_ep.c"
+    src.write_text(f"""#include <stdio.h>
+#include "ep.h"
+
+typedef void (*fn_t)(void);
+static const fn_t entry_points[] = {{
+    {table}
+}};
+
+int main(void) {{
+    ep_config c = {{1000, 64, 16, 4, 2, 1, 1, 1, 2, 0, 8, 0}};
+    size_t ws = 0;
+    int32_t cap = 0;
+    ep_status a = ep_layout_workspace_size(&c, &ws);
+    ep_status b = ep_schedule_capacity(&c, &cap);
+    printf("%d %d %d %zu %d %s\\n", (int)(sizeof entry_points / sizeof entry_points[0]), (int)a, (int)b, ws,
+           (int)cap, ep_status_string(EP_ERR_CAPACITY));
+    return 0;
+}}
+""")
+    exe = tmp_path / "use_ep"
+    libdir = pathlib.Path(lib.__file__).resolve().parent
+    r = subprocess.run([gcc, "-std=c11", "-Wall", "-Wextra", "-Werror", "-pedantic", f"-I{ROOT / 'include'}",
+                        f"-I{cuda_inc}", str(src), "-o", str(exe), f"-L{libdir}", "-lep_gb300",
+                        f"-Wl,-rpath,{libdir}"], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split(maxsplit=5)
+    cfg = lib.EpConfig.make(T=1000, H=64, E=16, R=4, k=2, ranks_per_node=2, num_workers=8)
+    assert int(out[0]) == len(names)
+    assert out[1] == out[2] == "0"
+    assert int(out[3]) == lib.ep_layout_workspace_size(cfg)
+    assert int(out[4]) == lib.ep_schedule_capacity(cfg) == 2 * 8 + 4
+    assert out[5].startswith("EP_ERR_CAPACITY")
