@@ -7,6 +7,7 @@ import pathlib
 import re
 import shutil
 import subprocess
+import sys
 
 import pytest
 
@@ -260,3 +261,16 @@ int main(void) {{
     assert int(out[3]) == lib.ep_layout_workspace_size(cfg)
     assert int(out[4]) == lib.ep_schedule_capacity(cfg) == 2 * 8 + 4
     assert out[5].startswith("EP_ERR_CAPACITY")
+
+
+def test_package_refuses_to_import_without_the_library(tmp_path):
+    """With the CUDA library missing, importing the package fails loudly: there is
+    no CPU or PyTorch fallback to land on."""
+    pkg = tmp_path / "combine_router_softmax_gb300"
+    pkg.mkdir()
+    shutil.copy(ROOT / "combine_router_softmax_gb300" / "__init__.py", pkg / "__init__.py")
+    env = dict(os.environ, PYTHONPATH=str(tmp_path))
+    r = subprocess.run([sys.executable, "-c", "import combine_router_softmax_gb300"], cwd=tmp_path, env=env,
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode != 0
+    assert "ImportError" in r.stderr and "There is no fallback path" in r.stderr
