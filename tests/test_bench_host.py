@@ -119,3 +119,27 @@ def test_clock_sampler_with_a_fake_nvidia_smi(tmp_path, monkeypatch):
     c = s.stop()
     assert c == {"sm_mhz": 2055.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"], "samples": 2}
     assert bench.ClockSampler(0, enabled=False).stop() is None
+
+
+@pytest.mark.parametrize("R,W", [(32, 152), (64, 7), (5, 5), (1, 3)])
+def test_rank_static_table_tiles_the_rows_once(R, W):
+    """The ablation's rank-static table: worker r mod W takes rank r's whole
+    segment; every send row is in exactly one chunk, each chunk inside one
+    rank, and worker_begin indexes each worker's chunks (the form
+    ep_dispatch_scheduled reads)."""
+    import numpy as np
+
+    g = np.random.default_rng(R * 1000 + W)
+    counts = g.integers(0, 50, size=R)
+    counts[g.integers(0, R)] = 0  # an empty rank
+    rank_offset = np.concatenate([[0], np.cumsum(counts)])
+    rows, wb = bench.rank_static_table(rank_offset, W)
+    assert len(wb) == W + 1 and wb[0] == 0 and wb[-1] == len(rows)
+    assert all(wb[i] <= wb[i + 1] for i in range(W))
+    covered = np.zeros(int(rank_offset[-1]), np.int32)
+    for w in range(W):
+        for worker, hop, r, begin, n in rows[wb[w]:wb[w + 1]]:
+            assert worker == w == r % W and hop == 0 and n > 0
+            assert begin == rank_offset[r] and n == rank_offset[r + 1] - rank_offset[r]
+            covered[begin:begin + n] += 1
+    assert (covered == 1).all()
