@@ -12,6 +12,30 @@ namespace {
 
 constexpr unsigned kBarrierSpinLimit = 1u << 22;  // polls of ~64 ns before giving up
 
+// A launch reports a CTA that gave up on a bounded wait through *n_chunks = -1,
+// the same word that carries the chunk count on success. The CTA that gives up
+// and the CTA that writes the count are different CTAs of one launch with no
+// order between them, so both go through these helpers: the failing CTA first
+// raises the launch's failure word (zeroed before the launch), and the count's
+// writer re-reads that word after its own write and puts -1 back if it is
+// raised. With a full fence on each side, -1 is the final value whenever any
+// CTA failed, whichever of the two writes to n_chunks lands last; a -1 left by
+// an earlier failed call is overwritten by the next successful one.
+__device__ __forceinline__ void mark_launch_failed(unsigned *fail, int32_t *n_chunks) {
+    atomicExch(fail, 1u);
+    __threadfence();
+    atomicExch(n_chunks, -1);
+}
+
+// fail may be null when no CTA of the launch can give up before the count is written.
+__device__ __forceinline__ void publish_chunk_count(int32_t *n_chunks, int32_t count, unsigned *fail) {
+    atomicExch(n_chunks, count);
+    if (fail) {
+        __threadfence();
+        if (atomicOr(fail, 0u) != 0u) atomicExch(n_chunks, -1);
+    }
+}
+
 // ---------------------------------------------------------------------------
 // shared device pieces
 // ---------------------------------------------------------------------------
@@ -255,7 +279,7 @@ __device__ __forceinline__ int32_t share_bound(int32_t N, int32_t w, int32_t W) 
 // scan over the counts writes its chunks.
 __device__ void build_schedule_two_tiers(const int32_t *s_roff, int32_t R, int32_t W, int32_t ranks_per_node,
                                          int32_t self_rank, ep_chunk *chunks, int32_t *n_chunks,
-                                         int32_t *worker_begin, int *s_warp, int32_t *s_P) {
+                                         int32_t *worker_begin, int *s_warp, int32_t *s_P, unsigned *fail) {
     const int32_t node = self_rank / ranks_per_node;
     const int32_t n_lo = node * ranks_per_node;
     const int32_t n_hi = n_lo + ranks_per_node < R ? n_lo + ranks_per_node : R;
@@ -315,7 +339,7 @@ __device__ void build_schedule_two_tiers(const int32_t *s_roff, int32_t R, int32
     }
     if (threadIdx.x == 0) {
         worker_begin[W] = carry;
-        *n_chunks = carry;
+        publish_chunk_count(n_chunks, carry, fail);
     }
 }
 
@@ -353,7 +377,7 @@ __device__ __forceinline__ ClassRuns class_runs(int c, int32_t R, int32_t nl, in
 template <int NC, int BAR>
 __device__ __noinline__ void build_schedule_nc(const int32_t *s_roff, int32_t R, int32_t W, HopTiers h,
                                                ep_chunk *chunks, int32_t *n_chunks, int32_t *worker_begin,
-                                               int *s_warp, int32_t *s_P, ThreadGroup<BAR> g) {
+                                               int *s_warp, int32_t *s_P, ThreadGroup<BAR> g, unsigned *fail) {
     const int32_t nl = h.self_rank / h.ranks_per_node * h.ranks_per_node;
     const int32_t nh = nl + h.ranks_per_node < R ? nl + h.ranks_per_node : R;
     const int32_t pl = NC == 3 ? h.self_rank / h.ranks_per_pod * h.ranks_per_pod : 0;
@@ -430,21 +454,22 @@ __device__ __noinline__ void build_schedule_nc(const int32_t *s_roff, int32_t R,
     }
     if (g.tid == 0) {
         worker_begin[W] = carry;
-        *n_chunks = carry;
+        publish_chunk_count(n_chunks, carry, fail);
     }
 }
 
 template <int BAR>
 __device__ __forceinline__ void cta_build_schedule(const int32_t *s_roff, int32_t R, int32_t W, HopTiers h,
                                                    ep_chunk *chunks, int32_t *n_chunks, int32_t *worker_begin,
-                                                   int *s_warp, int32_t *s_P, ThreadGroup<BAR> g) {
+                                                   int *s_warp, int32_t *s_P, ThreadGroup<BAR> g,
+                                                   unsigned *fail = nullptr) {
     if (h.ranks_per_pod > 0)
-        build_schedule_nc<3, BAR>(s_roff, R, W, h, chunks, n_chunks, worker_begin, s_warp, s_P, g);
+        build_schedule_nc<3, BAR>(s_roff, R, W, h, chunks, n_chunks, worker_begin, s_warp, s_P, g, fail);
     else if (BAR == 0)
         build_schedule_two_tiers(s_roff, R, W, h.ranks_per_node, h.self_rank, chunks, n_chunks, worker_begin, s_warp,
-                                 s_P);
+                                 s_P, fail);
     else
-        build_schedule_nc<2, BAR>(s_roff, R, W, h, chunks, n_chunks, worker_begin, s_warp, s_P, g);
+        build_schedule_nc<2, BAR>(s_roff, R, W, h, chunks, n_chunks, worker_begin, s_warp, s_P, g, fail);
 }
 
 // ---------------------------------------------------------------------------

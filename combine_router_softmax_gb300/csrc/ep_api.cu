@@ -11,7 +11,7 @@ namespace ep {
 
 namespace {
 constexpr int kMaxDevices = kMaxDevices_;
-int g_sm_count[kMaxDevices] = {0};
+std::atomic<int> g_sm_count[kMaxDevices];  // zero-initialised: not yet queried
 
 struct OccEntry {
     const void *fn;
@@ -27,10 +27,10 @@ int g_occ_n = 0;
 
 int sm_count(int device) {
     if (device < 0 || device >= kMaxDevices) return 0;
-    int v = g_sm_count[device];
+    int v = g_sm_count[device].load(std::memory_order_relaxed);
     if (v == 0) {
         if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return 0;
-        g_sm_count[device] = v;
+        g_sm_count[device].store(v, std::memory_order_relaxed);
     }
     return v;
 }

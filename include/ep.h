@@ -115,12 +115,15 @@ int ep_version(void);
  * (ep_layout reports its own bounded wait through *n_chunks = -1.) */
 ep_status ep_device_error(int32_t *flags);
 
-/* Diagnostics: checks that the library's device-side waits are bounded.
- * Launches two CTAs into a grid barrier (the kind ep_layout and
- * ep_dispatch_fused use) that expects three arrivals, so the wait can never
- * complete; each CTA must give up after max_polls polls (> 0) and count
- * itself in *gave_up (device int32, zeroed first). Expected result: 2. The
- * kernel returns normally; nothing faults or hangs. */
+/* Diagnostics: checks that the library's device-side waits are bounded and
+ * that a launch's failure mark survives. Launches two CTAs into a grid barrier
+ * (the kind ep_layout and ep_dispatch_fused use) that expects three arrivals,
+ * so the wait can never complete; each CTA must give up after max_polls polls
+ * (> 0), count itself in *gave_up (device int32, zeroed first) and mark the
+ * launch failed the way ep_layout marks *n_chunks = -1. A third CTA then
+ * writes a chunk count the way the schedule's writer does, after the failure
+ * mark; if that count survives, *gave_up is set to -1. Expected result: 2.
+ * The kernels return normally; nothing faults or hangs. */
 ep_status ep_check_bounded_wait(int32_t max_polls, int32_t *gave_up, cudaStream_t stream);
 
 /* Bytes of device scratch that ep_layout needs for `cfg` (it depends on T and
@@ -425,11 +428,16 @@ ep_status ep_combine(const ep_config *cfg, const ep_bf16 *y, const int32_t *slot
  * cudaMalloc, cudaFree or other allocating routine.
  *  - Limit: shapes whose ep_layout_workspace_size exceeds
  *    EP_LAYOUT_STATIC_SCRATCH_BYTES return EP_ERR_CAPACITY with nothing
- *    enqueued (the size is at most 4 E max(ceil(T / 256), 64) + 512 bytes:
- *    e.g. E = 256 allows T <= 262144 tokens).
+ *    enqueued. That size is max(a(4 E ceil(T / 256)), a(4 E n) + 256) bytes,
+ *    a() rounding up to a multiple of 256 and n <= max(ceil(T / 256), 64)
+ *    the single-kernel layout's CTA count: E = 256 allows T <= 262144 tokens
+ *    (exactly 1 MiB at T = 262144).
  *  - Set-up: the first call on a device (made with that device current) looks
  *    up the array's device address; make that first call before any stream
- *    capture. Later calls on the device reuse the address.
+ *    capture. Later calls on the device reuse the address, so a
+ *    cudaDeviceReset (or anything else that destroys the device's primary
+ *    context) leaves it stale: after one, do not call ep_layout_static on that
+ *    device again in the same process.
  *  - Sharing: every call on a device shares the one array, which keeps the
  *    last call's contents (the kernels overwrite all of it they read). Calls
  *    whose work overlaps on the GPU -- on different streams, or from
