@@ -1,14 +1,18 @@
 """Full-size workloads through the same calls and launch configuration the
-benchmark times (GPU).
+benchmark times (GPU), compared with the oracle element by element.
 
-route, layout and the chunk schedule are compared with the oracle on every
-token (cheap on the CPU). The send buffer and the combine output are checked
-on sampled tokens, which the oracle computes one by one: a token's combine
-output depends only on its own x row, experts and weights, so the oracle
-solves the sub-problem made of the sampled tokens alone (its own route,
-layout, dispatch, expert and combine) and that equals its full-size answer
-for those tokens. Properties that hold at any size (slot_meta is a
-permutation, the send rows of a token equal its x row) are checked in full.
+* route, layout and the chunk schedule: every token (cheap on the CPU).
+* dispatch: every element of the send buffer and every slot_meta entry
+  against orc_dispatch. The dispatch copies whole rows, so restricting x to a
+  block of columns restricts the send buffer to the same columns; the oracle
+  dispatches blocks of COLS columns at a time, which bounds host memory at
+  T = 32768 (3.8 GB of send rows), and each block of the GPU's send buffer is
+  compared with its block.
+* combine: every element of ``out`` within 1 bf16 ulp of orc_combine. A
+  token's output depends only on its own logits and x row (its experts,
+  weights and expert rows), so the oracle's whole path run on a chunk of
+  CHUNK consecutive tokens gives the full-size answer for those tokens; the
+  chunks cover every token.
 """
 from __future__ import annotations
 
@@ -22,9 +26,13 @@ from test_gpu_parity import assert_layout, assert_route
 
 pytestmark = pytest.mark.gpu
 
+COLS = 1024     # columns of x per oracle dispatch block
+CHUNK = 4096    # tokens per oracle combine chunk
+
 FULL = [
     ep_synth.CONFIGS["prefill"],
     ep_synth.CONFIGS["mid"],
+    ep_synth.get_workload("sweep-uniform-T4096"),
     ep_synth.get_workload("sweep-zipf-T4096"),
     ep_synth.get_workload("sweep-uniform-T32768"),
     ep_synth.get_workload("sweep-zipf-T32768"),
@@ -48,6 +56,7 @@ def test_fullsize(ep, orc, w):
     b = ep.LayerBuffers.allocate(cfg)
     b.logits.copy_(torch.from_numpy(logits))
     b.x.copy_(bf16_to_dev(x))
+    poison_outputs(b)
     b.route()
     b.layout()
     b.dispatch()
@@ -60,15 +69,22 @@ def test_fullsize(ep, orc, w):
 # The benchmark's own launch configuration: ep_dispatch_fused + ep_combine
 # captured once in a CUDA graph and replayed. Small T runs the single fused
 # kernel (with and without its schedule CTA), large T the route, layout and
-# dispatch kernels chained by programmatic dependent launch.
+# dispatch kernels chained by programmatic dependent launch. Every workload
+# the benchmark times is here: the sweep's small-T latency points, decode,
+# prefill, mid, both sweep T = 4096 points and the default T = 32768.
 GRAPH = [
     ep_synth.get_workload("sweep-uniform-T1"),
+    ep_synth.get_workload("sweep-zipf-T1"),
+    ep_synth.get_workload("sweep-uniform-T8"),
     ep_synth.get_workload("sweep-zipf-T8"),
     ep_synth.get_workload("sweep-uniform-T64"),
+    ep_synth.get_workload("sweep-zipf-T64"),
     ep_synth.CONFIGS["decode"],
     ep_synth.get_workload("sweep-zipf-T512"),
     ep_synth.CONFIGS["prefill"],
     ep_synth.CONFIGS["mid"],
+    ep_synth.get_workload("sweep-uniform-T4096"),
+    ep_synth.get_workload("sweep-zipf-T4096"),
     ep_synth.get_workload("sweep-zipf-T32768"),
 ]
 
@@ -110,10 +126,11 @@ def test_fullsize_bench_graph(ep, orc, w):
 
 
 def check_against_oracle(orc, w, b, logits, x):
+    T, H, k = w.T, w.H, w.k
     # route + layout + schedule: every token
-    idx, w64 = orc.route(logits, w.k, w.n_groups, w.topk_groups, w.renormalize)
+    idx, w64 = orc.route(logits, k, w.n_groups, w.topk_groups, w.renormalize)
     lay = orc.layout(idx, w.E, w.R)
-    ch, wb = orc.schedule(lay["rank_offset"], w.ranks_per_node, w.self_rank, w.num_workers)
+    ch, wb = orc.schedule(lay["rank_offset"], w.ranks_per_node, w.self_rank, w.num_workers, w.ranks_per_pod)
     n = int(b.n_chunks.item())
     g = dict(idx=b.topk_idx.cpu().numpy(), w=b.topk_w.cpu().numpy(),
              expert_count=b.expert_count.cpu().numpy(), expert_offset=b.expert_offset.cpu().numpy(),
@@ -122,21 +139,24 @@ def check_against_oracle(orc, w, b, logits, x):
     assert_route(g, dict(idx=idx, w=w64), logits, w.renormalize)
     assert_layout(g, dict(chunks=ch, worker_begin=wb, **lay))
 
-    # slot_meta is a permutation of 0 .. T k - 1 and agrees with slot
-    meta = b.slot_meta
-    assert torch.equal(torch.sort(meta).values, torch.arange(w.T * w.k, device="cuda", dtype=torch.int32))
-    slot_flat = b.slot.view(-1).long()
-    assert torch.equal(meta[slot_flat], torch.arange(w.T * w.k, device="cuda", dtype=torch.int32))
+    # dispatch: the whole send buffer and slot_meta, element by element
+    for c0 in range(0, H, COLS):
+        c1 = min(H, c0 + COLS)
+        send_ref, meta_ref = orc.dispatch(np.ascontiguousarray(x[:, c0:c1]), lay["slot"])
+        got = bf16_from_dev(b.send[:, c0:c1].contiguous())
+        assert np.array_equal(got, send_ref), f"send buffer differs in columns [{c0}, {c1})"
+        if c0 == 0:
+            assert np.array_equal(b.slot_meta.cpu().numpy(), meta_ref), "slot_meta differs"
+        del send_ref, got
 
-    # sampled tokens: send rows and combine output
-    rng = np.random.default_rng(w.T)
-    S = np.unique(np.concatenate([[0, 1, w.T // 2, w.T - 1], rng.integers(0, w.T, size=96)]))
-    S = S[S < w.T]
-    send_rows = bf16_from_dev(b.send[torch.from_numpy(lay["slot"][S].ravel()).long().cuda()])
-    assert np.array_equal(send_rows, np.repeat(x[S], w.k, axis=0)), "send rows differ from x"
-
-    sub = orc.run_path(logits[S], x[S], E=w.E, R=1, k=w.k, n_groups=w.n_groups, topk_groups=w.topk_groups,
-                       renormalize=w.renormalize, ranks_per_node=1, self_rank=0, W=1)
-    out_g = bf16_from_dev(b.out[torch.from_numpy(S).long().cuda()])
-    d = bf16_ulp_distance(out_g, sub["out"])
-    assert d.max() <= 1, f"combine differs by {d.max()} bf16 ulp on sampled tokens"
+    # combine: every output element, token chunk by token chunk
+    worst = 0
+    for t0 in range(0, T, CHUNK):
+        t1 = min(T, t0 + CHUNK)
+        sub = orc.run_path(logits[t0:t1], x[t0:t1], E=w.E, R=1, k=k, n_groups=w.n_groups,
+                           topk_groups=w.topk_groups, renormalize=w.renormalize, ranks_per_node=1, self_rank=0, W=1)
+        assert np.array_equal(sub["idx"], idx[t0:t1])  # the chunk routes its tokens as the whole batch does
+        d = bf16_ulp_distance(bf16_from_dev(b.out[t0:t1]), sub["out"])
+        worst = max(worst, int(d.max()))
+        del sub
+    assert worst <= 1, f"combine differs by {worst} bf16 ulp"

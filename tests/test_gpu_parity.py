@@ -413,7 +413,7 @@ FUSED = [
                       num_workers=152),
     ep_synth.Workload("pods-T4096", T=4096, H=1024, E=256, R=64, k=8, ranks_per_node=4, ranks_per_pod=16,
                       self_rank=5, num_workers=152),
-] + [w for w in ep_synth.sweep_workloads() if w.T in (1, 8, 64, 512, 32768)]
+] + [w for w in ep_synth.sweep_workloads() if w.T in (1, 8, 64, 512, 4096, 32768)]
 
 
 @pytest.mark.parametrize("w", FUSED, ids=lambda w: w.name)
