@@ -71,25 +71,39 @@ def uniform_f64(seed: int, tensor_id: int, n: int, offset: int = 0) -> np.ndarra
     return (uint64_stream(seed, tensor_id, n, offset) >> np.uint64(11)).astype(np.float64) * 2.0**-53
 
 
+def _normal_chunk(out: np.ndarray, seed: int, tensor_id: int, pos: int, m: int, offset: int) -> None:
+    g0 = offset + pos  # global index of the first normal in this chunk
+    p0, p1 = g0 // 2, (g0 + m + 1) // 2  # pair range covering [g0, g0 + m)
+    u = uint64_stream(seed, tensor_id, 2 * (p1 - p0), 2 * p0)
+    u1 = ((u[0::2] >> np.uint64(11)).astype(np.float64) + 1.0) * 2.0**-53  # (0, 1]
+    u2 = (u[1::2] >> np.uint64(11)).astype(np.float64) * 2.0**-53  # [0, 1)
+    r = np.sqrt(-2.0 * np.log(u1))
+    th = 2.0 * math.pi * u2
+    pair = np.empty(2 * (p1 - p0), dtype=np.float64)
+    pair[0::2] = r * np.cos(th)
+    pair[1::2] = r * np.sin(th)
+    s = g0 - 2 * p0
+    out[pos:pos + m] = pair[s:s + m]
+
+
 def normal_f64(seed: int, tensor_id: int, n: int, offset: int = 0) -> np.ndarray:
-    """``n`` standard normals (Box-Muller), element ``i`` fixed by ``offset + i``."""
+    """``n`` standard normals (Box-Muller), element ``i`` fixed by ``offset + i``.
+
+    Chunks are independent (each element depends only on its index), so large
+    draws are spread over a thread pool; numpy releases the GIL in its array
+    loops. The result does not depend on the number of threads."""
     out = np.empty(n, dtype=np.float64)
-    pos = 0
-    while pos < n:
-        m = min(_CHUNK, n - pos)
-        g0 = offset + pos  # global index of the first normal in this chunk
-        p0, p1 = g0 // 2, (g0 + m + 1) // 2  # pair range covering [g0, g0 + m)
-        u = uint64_stream(seed, tensor_id, 2 * (p1 - p0), 2 * p0)
-        u1 = ((u[0::2] >> np.uint64(11)).astype(np.float64) + 1.0) * 2.0**-53  # (0, 1]
-        u2 = (u[1::2] >> np.uint64(11)).astype(np.float64) * 2.0**-53  # [0, 1)
-        r = np.sqrt(-2.0 * np.log(u1))
-        th = 2.0 * math.pi * u2
-        pair = np.empty(2 * (p1 - p0), dtype=np.float64)
-        pair[0::2] = r * np.cos(th)
-        pair[1::2] = r * np.sin(th)
-        s = g0 - 2 * p0
-        out[pos:pos + m] = pair[s:s + m]
-        pos += m
+    starts = list(range(0, n, _CHUNK))
+    if len(starts) <= 1:
+        for pos in starts:
+            _normal_chunk(out, seed, tensor_id, pos, min(_CHUNK, n - pos), offset)
+        return out
+    import concurrent.futures as cf
+    import os
+
+    workers = min(len(starts), os.cpu_count() or 1, 16)
+    with cf.ThreadPoolExecutor(max_workers=workers) as ex:
+        list(ex.map(lambda pos: _normal_chunk(out, seed, tensor_id, pos, min(_CHUNK, n - pos), offset), starts))
     return out
 
 

@@ -16,6 +16,8 @@ benchmark times (GPU), compared with the oracle element by element.
 """
 from __future__ import annotations
 
+import concurrent.futures as cf
+
 import numpy as np
 import pytest
 import torch
@@ -28,6 +30,7 @@ pytestmark = pytest.mark.gpu
 
 COLS = 1024     # columns of x per oracle dispatch block
 CHUNK = 4096    # tokens per oracle combine chunk
+ORACLE_THREADS = 4
 
 FULL = [
     ep_synth.CONFIGS["prefill"],
@@ -139,10 +142,14 @@ def check_against_oracle(orc, w, b, logits, x):
     assert_route(g, dict(idx=idx, w=w64), logits, w.renormalize)
     assert_layout(g, dict(chunks=ch, worker_begin=wb, **lay))
 
+    # The oracle's blocks and chunks are independent calls into the C library
+    # (ctypes releases the GIL), so a few run at once; each is the oracle as is.
+    pool = cf.ThreadPoolExecutor(max_workers=ORACLE_THREADS)
+
     # dispatch: the whole send buffer and slot_meta, element by element
-    for c0 in range(0, H, COLS):
-        c1 = min(H, c0 + COLS)
-        send_ref, meta_ref = orc.dispatch(np.ascontiguousarray(x[:, c0:c1]), lay["slot"])
+    blocks = [(c0, min(H, c0 + COLS)) for c0 in range(0, H, COLS)]
+    refs = pool.map(lambda c: orc.dispatch(np.ascontiguousarray(x[:, c[0]:c[1]]), lay["slot"]), blocks)
+    for (c0, c1), (send_ref, meta_ref) in zip(blocks, refs):
         got = bf16_from_dev(b.send[:, c0:c1].contiguous())
         assert np.array_equal(got, send_ref), f"send buffer differs in columns [{c0}, {c1})"
         if c0 == 0:
@@ -150,13 +157,16 @@ def check_against_oracle(orc, w, b, logits, x):
         del send_ref, got
 
     # combine: every output element, token chunk by token chunk
-    worst = 0
-    for t0 in range(0, T, CHUNK):
+    def chunk_out(t0):
         t1 = min(T, t0 + CHUNK)
         sub = orc.run_path(logits[t0:t1], x[t0:t1], E=w.E, R=1, k=k, n_groups=w.n_groups,
                            topk_groups=w.topk_groups, renormalize=w.renormalize, ranks_per_node=1, self_rank=0, W=1)
-        assert np.array_equal(sub["idx"], idx[t0:t1])  # the chunk routes its tokens as the whole batch does
-        d = bf16_ulp_distance(bf16_from_dev(b.out[t0:t1]), sub["out"])
+        return t0, t1, sub["idx"], sub["out"]
+
+    worst = 0
+    for t0, t1, sub_idx, sub_out in pool.map(chunk_out, range(0, T, CHUNK)):
+        assert np.array_equal(sub_idx, idx[t0:t1])  # the chunk routes its tokens as the whole batch does
+        d = bf16_ulp_distance(bf16_from_dev(b.out[t0:t1]), sub_out)
         worst = max(worst, int(d.max()))
-        del sub
+    pool.shutdown()
     assert worst <= 1, f"combine differs by {worst} bf16 ulp"
