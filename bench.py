@@ -7,15 +7,19 @@ dispatch and combine is outside the library; its output buffer y is filled once
 before timing with the synthetic expert's rows for this batch, which are the
 same every step because routing is deterministic).
 
-Default workload: prefill-shaped, skewed (T=4096, H=7168, E=256 over R=32,
-top-8, Zipf 1.2 expert popularity). ``--config`` selects another workload.
+Default workload: the largest single-GPU one, the sweep's T=32768 point with
+Zipf 1.2 expert popularity (H=7168, E=256 over R=64, top-8; 8.5 GB moved per
+layer). ``--config`` selects another workload.
 
 Printed: one JSON line (rank 0). ``value`` is achieved algorithmic GB/s of the
 whole step (bytes every step must move at least once / device time), ``e2e``
 the same through the public API with the host<->device copies of the step's
-inputs and result inside the timed region, ``roofline`` the dominant kernel
-against the measured HBM copy bandwidth, ``cpu_baseline`` the CPU oracle on a
-bounded sample of the same workload.
+inputs and result inside the timed region, ``roofline`` the dominant call
+against the measured HBM copy bandwidth (and the 8 TB/s nominal figure),
+``cpu_baseline`` the CPU oracle on a bounded sample of the same workload.
+Unless ``--no-blocks``: ``workloads`` holds the same figures for prefill, mid
+and the other large sweep points, and ``latency`` the per-layer latency at the
+sweep's small T (1, 8, 64; uniform and Zipf) and at decode.
 
 ``--impl reference`` times the CPU oracle (the only reference implementation
 of this path) on the same workload, each step a bounded token sample.
@@ -42,6 +46,14 @@ if str(ROOT) not in sys.path:
 
 METRIC = "dispatch+combine µs/layer and achieved HBM GB/s (fraction of GB300 peak), 1 GPU"
 FALLBACK_HBM_GBS = 6800.0
+SPEC_HBM_GBS = 8000.0  # the GB300's nominal HBM3e bandwidth (~8 TB/s), reported beside the measured copy peak
+# The line's own workload: the largest single-GPU one (8.5 GB moved per layer).
+DEFAULT_WORKLOAD = "sweep-zipf-T32768"
+# The other workloads the >= 70 % target names, each reported in a block of the same line.
+BLOCK_WORKLOADS = ("prefill", "mid", "sweep-uniform-T4096", "sweep-zipf-T4096", "sweep-uniform-T32768")
+# The sweep's small-T latency floor, plus the decode shape.
+LATENCY_WORKLOADS = ("sweep-uniform-T1", "sweep-zipf-T1", "sweep-uniform-T8", "sweep-zipf-T8",
+                     "sweep-uniform-T64", "sweep-zipf-T64", "decode")
 # The files whose contents fix each timed kernel (profiles/dram_traffic.txt keys).
 KERNEL_SOURCES = {
     "route": ["route.cu", "route_token.cuh"],
@@ -59,7 +71,12 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
-    p.add_argument("--config", default="prefill", help="workload name (tiny, decode, prefill, mid, sweep-<dist>-T<n>)")
+    p.add_argument("--config", default=DEFAULT_WORKLOAD,
+                   help="workload name (tiny, decode, prefill, mid, sweep-<dist>-T<n>)")
+    p.add_argument("--no-blocks", action="store_true",
+                   help="time only --config (default: also the other throughput workloads and the small-T latency "
+                        "points, each in a block of its own)")
+    p.add_argument("--latency-steps", type=int, default=100, help="replays per small-T latency point (at least --steps)")
     p.add_argument("--e2e-steps", type=int, default=None, help="steps of the end-to-end leg (default min(steps, 200))")
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU work of the oracle baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -671,53 +688,89 @@ def tff_leg(ep, buf, w, device, flush_l2, K: int) -> dict:
     return out
 
 
-def run_gb300(args):
+def reduce_max_many(values: dict, world: int, device=None) -> dict:
+    """Max over ranks of every value: one all_reduce(MAX) of a float64 vector
+    whose entries follow the sorted keys (every rank passes the same keys)."""
+    if world == 1:
+        return {k: float(v) for k, v in values.items()}
+    import torch
+    import torch.distributed as dist
+
+    keys = sorted(values)
+    t = torch.tensor([float(values[k]) for k in keys], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return {k: float(v) for k, v in zip(keys, t.tolist())}
+
+
+def whole_job(bytes_per_step: int, world: int, steps: int, slowest_total_ms: float) -> tuple[float, float]:
+    """(GB/s of all ranks, ms per step) when every rank moves bytes_per_step in
+    each of `steps` steps and the slowest rank takes slowest_total_ms for them."""
+    ms = slowest_total_ms / steps
+    return world * bytes_per_step / (ms * 1e-3) / 1e9, ms
+
+
+def step_stats_us(per_step_ms: list) -> dict:
+    q = sorted(per_step_ms)
+    return {"median": round(1e3 * q[len(q) // 2], 2), "p10": round(1e3 * q[len(q) // 10], 2),
+            "p90": round(1e3 * q[(9 * len(q)) // 10], 2), "min": round(1e3 * q[0], 2), "max": round(1e3 * q[-1], 2)}
+
+
+class Flusher:
+    """Write 2x L2, then read another 2x L2: the step starts with none of its
+    data in L2 and no dirty line left to write back inside the timed region."""
+
+    def __init__(self, device):
+        import torch
+
+        l2 = torch.cuda.get_device_properties(device).L2_cache_size
+        n = max(2 * l2, 256 << 20)
+        self.w = torch.empty(n, dtype=torch.uint8, device=device)
+        self.r = torch.ones(n // 4, dtype=torch.int32, device=device)
+        self.sink = torch.empty((), dtype=torch.int64, device=device)
+
+    def __call__(self):
+        import torch
+
+        self.w.fill_(1)
+        torch.sum(self.r, dim=0, dtype=torch.int64, out=self.sink)
+
+
+def prepare_layer(ep, w, device):
+    """Buffers of one layer with this batch's inputs and its expert output y
+    (the synthetic expert: each send row scaled by (e + 1) / E), made before timing."""
     import numpy as np
     import torch
 
-    rank, world, local_rank = dist_env()
-    torch.cuda.set_device(local_rank)
-    device = torch.device("cuda", local_rank)
-    if world > 1:
-        import torch.distributed as dist
-
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-
-    import combine_router_softmax_gb300 as ep
     import ep_synth
 
-    w0 = ep_synth.get_workload(args.config)
-    w = rank_workload(w0, rank)
     cfg = ep.EpConfig.from_workload(w)
     logits_np = ep_synth.gate_logits(w.seed, w.T, w.E, w.zipf_s)
     x_np = ep_synth.hidden_bf16_bits(w.seed, w.T, w.H)
-
     buf = ep.LayerBuffers.allocate(cfg, device=device)
     buf.logits.copy_(torch.from_numpy(logits_np))
     buf.x.copy_(torch.from_numpy(x_np.view(np.int16)).view(torch.bfloat16))
-    stream = torch.cuda.current_stream(device)
-    bound = buf.bind(stream)
-
-    # expert output for this batch (outside the timed step)
-    bound.dispatch_fused()
+    buf.bind(torch.cuda.current_stream(device)).dispatch_fused()
     rows = torch.arange(w.T * w.k, device=device, dtype=torch.int32)
     e = torch.searchsorted(buf.expert_offset, rows, right=True) - 1
     buf.y.copy_((buf.send.float() * ((e + 1).float() / w.E)[:, None]).to(torch.bfloat16))
     del rows, e
     torch.cuda.synchronize()
+    return cfg, buf, logits_np, x_np
 
-    l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    flush_w = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=device)
-    flush_r = torch.ones(max(2 * l2, 256 << 20) // 4, dtype=torch.int32, device=device)
-    flush_sink = torch.empty((), dtype=torch.int64, device=device)
 
-    def flush_l2():
-        # Write 2x L2, then read another 2x L2: the step starts with none of its
-        # data in L2 and no dirty line left to write back inside the timed region.
-        flush_w.fill_(1)
-        torch.sum(flush_r, dim=0, dtype=torch.int64, out=flush_sink)
+def measure_workload(ep, w0, args, rank: int, world: int, device, flush_l2, K: int, cpu_seconds: float,
+                     main: bool) -> tuple[dict, object]:
+    """Time one workload the way the JSON line reports it. Returns the
+    workload's block (values already reduced over ranks) and its buffers."""
+    import numpy as np
+    import torch
 
-    calls = step_calls(bound, not args.separate)
+    w = rank_workload(w0, rank)
+    cfg, buf, logits_np, x_np = prepare_layer(ep, w, device)
+    stream = torch.cuda.current_stream(device)
+    bound = buf.bind(stream)
+    fused = not args.separate
+    calls = step_calls(bound, fused)
 
     def step():
         for _, fn in calls:
@@ -727,8 +780,6 @@ def run_gb300(args):
         flush_l2()
         step()
     torch.cuda.synchronize()
-
-    fused = not args.separate
     graph = None if args.no_graph else capture_step_graph(buf, device, fused)
     if graph is not None:
         for _ in range(max(args.warmup, 0)):
@@ -736,10 +787,10 @@ def run_gb300(args):
             graph.replay()
         torch.cuda.synchronize()
 
-    K = args.steps
+    # (1) the calls launched one by one, an event between consecutive calls
     nc = len(calls)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nc + 1)] for _ in range(K)]
-    clocks = ClockSampler(local_rank, enabled=not args.no_clocks)
+    clocks = ClockSampler(torch.cuda.current_device(), enabled=not args.no_clocks)
     time.sleep(0.3 if not args.no_clocks else 0)
     barrier(world)
     torch.cuda.synchronize()
@@ -755,21 +806,17 @@ def run_gb300(args):
     barrier(world)
     wall = time.perf_counter() - wall0
     clk = clocks.stop()
-
     per = {n: [] for n, _ in calls}
     step_ms = []
     for evs in ev:
         for j, (n, _) in enumerate(calls):
             per[n].append(evs[j].elapsed_time(evs[j + 1]))
         step_ms.append(evs[0].elapsed_time(evs[nc]))
-    stream_ms_per_step = reduce_max(sum(step_ms), world, device) / K
-    bytes_step = w.total_bytes()
 
+    # (2) the same calls captured once in a CUDA graph, replayed K times
     if graph is not None:
-        # The same four calls captured once in a CUDA graph, replayed K times
-        # (L2 flushed before each replay, outside the events).
         gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-        clocks = ClockSampler(local_rank, enabled=not args.no_clocks)
+        clocks = ClockSampler(torch.cuda.current_device(), enabled=not args.no_clocks)
         time.sleep(0.3 if not args.no_clocks else 0)
         barrier(world)
         torch.cuda.synchronize()
@@ -786,37 +833,10 @@ def run_gb300(args):
         if gclk is not None:
             clk = gclk
         per_step_ms = [a.elapsed_time(b_) for a, b_ in gev]
-        local_total_ms = sum(per_step_ms)
     else:
         per_step_ms = list(step_ms)
-        local_total_ms = sum(step_ms)
-    q = sorted(per_step_ms)
-    step_stats = {"median": round(1e3 * q[len(q) // 2], 2), "p10": round(1e3 * q[len(q) // 10], 2),
-                  "p90": round(1e3 * q[(9 * len(q)) // 10], 2), "min": round(1e3 * q[0], 2),
-                  "max": round(1e3 * q[-1], 2)}
-    max_total_ms = reduce_max(local_total_ms, world, device)
-    value = world * K * bytes_step / (max_total_ms * 1e-3) / 1e9
-    ms_per_step = max_total_ms / K
 
-    launches_per_step = ep.ep_step_kernel_count(cfg, fused=fused)
-    kb = {n: call_bytes(w, n) for n, _ in calls}
-    kern_ms = {n: sum(v) / len(v) for n, v in per.items()}
-    dom = max(kern_ms, key=kern_ms.get)
-    peak, peak_kind = measured_peak_gbs()
-    achieved = kb[dom] / (kern_ms[dom] * 1e-3) / 1e9
-    # kernels each call launches: ep_dispatch_fused or ep_layout the ones the
-    # step count leaves after the single-kernel calls
-    names = [n for n, _ in calls]
-    multi = "dispatch_fused" if "dispatch_fused" in names else "layout"
-    call_kernels = {n: 1 for n in names}
-    call_kernels[multi] = launches_per_step - (len(names) - 1)
-    by_call = {n: {"us": round(kern_ms[n] * 1e3, 2), "kernels": call_kernels[n],
-                   "algorithmic_bytes": kb[n],
-                   "achieved": round(kb[n] / (kern_ms[n] * 1e-3) / 1e9, 1),
-                   "frac": round(kb[n] / (kern_ms[n] * 1e-3) / 1e9 / peak, 4),
-                   "traffic": ncu_traffic(n, w0.name)} for n in kern_ms}
-
-    # end to end: pinned host inputs in, result out, every step
+    # (3) end to end through the public API: pinned host inputs in, result out, every step
     E2E = args.e2e_steps if args.e2e_steps is not None else min(K, 200)
     h_logits = torch.from_numpy(logits_np).pin_memory()
     h_x = torch.from_numpy(x_np.view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -836,49 +856,61 @@ def run_gb300(args):
         if i >= 3:
             e2e_ev[i - 3][1].record(stream)
     torch.cuda.synchronize()
-    e2e_ms = reduce_max(sum(a.elapsed_time(b) for a, b in e2e_ev), world, device) / E2E
-    e2e_val = world * bytes_step / (e2e_ms * 1e-3) / 1e9
+    assert torch.equal(h_out.to(device), buf.out)  # the result is the one the path computes
+    pipe = e2e_pipelined(ep, buf, cfg, device, fused, graph is not None, h_logits, h_x, E2E)
 
-    # the result must be the one the path computes (cheap self-check of the last step)
-    assert torch.equal(h_out.to(device), buf.out)
+    # slowest rank of every timed total
+    tot = reduce_max_many({"stream": sum(step_ms), "step": sum(per_step_ms),
+                           "e2e": sum(a.elapsed_time(b) for a, b in e2e_ev), "pipe": pipe["total_ms"]},
+                          world, device)
+    bytes_step = w.total_bytes()
+    value, ms_per_step = whole_job(bytes_step, world, K, tot["step"])
+    stream_gbs, stream_ms = whole_job(bytes_step, world, K, tot["stream"])
+    e2e_val, e2e_ms = whole_job(bytes_step, world, E2E, tot["e2e"])
+    pipe_val, pipe_ms = whole_job(bytes_step, world, E2E, tot["pipe"])
 
-    # end to end, pipelined: two buffer sets; step i+1's inputs are copied in
-    # (and step i-1's result out) while step i computes
-    pipe = e2e_pipelined(ep, buf, cfg, device, not args.separate, graph is not None, h_logits, h_x, E2E)
-    pipe_ms = reduce_max(pipe["total_ms"], world, device) / E2E
-    pipe_val = world * bytes_step / (pipe_ms * 1e-3) / 1e9
-
-    line = {
-        "metric": METRIC,
+    launches_per_step = ep.ep_step_kernel_count(cfg, fused=fused)
+    kb = {n: call_bytes(w, n) for n, _ in calls}
+    kern_ms = {n: sum(v) / len(v) for n, v in per.items()}
+    dom = max(kern_ms, key=kern_ms.get)
+    peak, peak_kind = measured_peak_gbs()
+    names = [n for n, _ in calls]
+    multi = "dispatch_fused" if "dispatch_fused" in names else "layout"
+    call_kernels = {n: 1 for n in names}
+    call_kernels[multi] = launches_per_step - (len(names) - 1)
+    by_call = {n: {"us": round(kern_ms[n] * 1e3, 2), "kernels": call_kernels[n],
+                   "algorithmic_bytes": kb[n],
+                   "achieved": round(kb[n] / (kern_ms[n] * 1e-3) / 1e9, 1),
+                   "frac": round(kb[n] / (kern_ms[n] * 1e-3) / 1e9 / peak, 4),
+                   "frac_of_spec": round(kb[n] / (kern_ms[n] * 1e-3) / 1e9 / SPEC_HBM_GBS, 4),
+                   "traffic": ncu_traffic(n, w0.name)} for n in kern_ms}
+    achieved = kb[dom] / (kern_ms[dom] * 1e-3) / 1e9
+    block = {
         "value": round(value, 2),
         "unit": "GB/s",
-        "n_gpus": world,
-        "steps": K,
-        "warmup": args.warmup,
         "ms_per_step": round(ms_per_step, 5),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "bf16 rows, fp32 routing and combine accumulation",
-        "data": "synthetic",
         "config": workload_config(w0, args),
         "us_per_layer": round(ms_per_step * 1e3, 2),
         "timing": ("CUDA graph of the step's C-ABI calls, replayed per step" if graph is not None
                    else "the step's C-ABI calls launched per step"),
-        "calls": [n for n, _ in calls],
-        "stream_us_per_layer": round(stream_ms_per_step * 1e3, 2),
-        "us_per_layer_stats": step_stats,
+        "calls": names,
+        "stream_us_per_layer": round(stream_ms * 1e3, 2),
+        "us_per_layer_stats": step_stats_us(per_step_ms),
         "hbm_fraction": round(value / world / peak, 4),
+        "hbm_fraction_of_spec": round(value / world / SPEC_HBM_GBS, 4),
         "kernel_us": {n: round(v * 1e3, 2) for n, v in kern_ms.items()},
         "roofline": {
             "bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "traffic": ncu_traffic(dom, w0.name),
+            "frac": round(achieved / peak, 4), "frac_of_spec": round(achieved / SPEC_HBM_GBS, 4),
+            "traffic": ncu_traffic(dom, w0.name),
             "algorithmic_bytes_per_launch": kb[dom], "kernels_in_call": call_kernels[dom],
             "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
             if peak_kind == "measured" else "fallback 6.8 TB/s",
+            "spec_peak": SPEC_HBM_GBS,
             "by_call": by_call,
         },
-        "e2e": {"value": round(pipe_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h_logits.numel() * 4 + h_x.numel() * 2,
+        "e2e": {"value": round(pipe_val, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": h_logits.numel() * 4 + h_x.numel() * 2,
                 "d2h_bytes_per_step": h_out.numel() * 2, "ms_per_step": round(pipe_ms, 5), "steps": E2E,
                 "mode": "pipelined: two buffer sets; the H2D copy of step i+1 and the D2H copy of step i-1 run on "
                         "their own streams while step i computes; timed from the first timed H2D to the last D2H",
@@ -888,14 +920,110 @@ def run_gb300(args):
         "clocks": clk,
         "wall_s": round(wall, 3),
     }
+    if rank == 0 and not args.no_cpu_baseline:
+        block["cpu_baseline"] = cpu_baseline(w0, cpu_seconds)
+    del graph
+    return block, buf
+
+
+def latency_point(ep, w0, args, rank: int, world: int, device, flush_l2, K: int) -> dict:
+    """Per-layer latency of one small batch: the step's graph replayed K times,
+    L2 flushed before each replay (outside the events); median and spread over
+    the replays, the slowest rank's median."""
+    import torch
+
+    w = rank_workload(w0, rank)
+    cfg, buf, _, _ = prepare_layer(ep, w, device)
+    fused = not args.separate
+    graph = capture_step_graph(buf, device, fused)
+    stream = torch.cuda.current_stream(device)
+    for _ in range(max(args.warmup, 3)):
+        flush_l2()
+        graph.replay()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, b_ in ev:
+        flush_l2()
+        a.record(stream)
+        graph.replay()
+        b_.record(stream)
+    torch.cuda.synchronize()
+    ms = [a.elapsed_time(b_) for a, b_ in ev]
+    st = step_stats_us(ms)
+    red = reduce_max_many({"median": st["median"], "mean": 1e3 * sum(ms) / K}, world, device)
+    peak, _ = measured_peak_gbs()
+    out = {"us_per_layer": round(red["median"], 2), "us_mean": round(red["mean"], 2), "stats_us": st,
+           "kernels": ep.ep_step_kernel_count(cfg, fused=fused), "bytes_per_step": w.total_bytes(),
+           "hbm_fraction": round(w.total_bytes() / (red["median"] * 1e-6) / 1e9 / peak, 4), "steps": K,
+           "T": w.T, "dist": "zipf 1.2" if w.zipf_s else "uniform"}
+    del graph, buf
+    return out
+
+
+def run_gb300(args):
+    import torch
+
+    rank, world, local_rank = dist_env()
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+
+    import combine_router_softmax_gb300 as ep
+    import ep_synth
+
+    flush_l2 = Flusher(device)
+    K = args.steps
+    w0 = ep_synth.get_workload(args.config)
+    block, buf = measure_workload(ep, w0, args, rank, world, device, flush_l2, K, args.cpu_seconds, main=True)
+
+    line = {
+        "metric": METRIC,
+        "value": block.pop("value"),
+        "unit": block.pop("unit"),
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": block.pop("ms_per_step"),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16 rows, fp32 routing and combine accumulation",
+        "data": "synthetic",
+        "config": block.pop("config"),
+    }
+    line.update(block)
+    # the optional legs run on the main workload's buffers
+    w = rank_workload(w0, rank)
     if args.schedule_ablation:
         line["schedule_ablation"] = schedule_ablation_leg(ep, buf, w, device, flush_l2, min(K, 500))
     if args.tff:
         line["tff"] = tff_leg(ep, buf, w, device, flush_l2, min(K, 500))
     if args.data_as_flag:
         line["data_as_flag"] = data_as_flag_leg(ep, buf, w, device, flush_l2, min(K, 500))
-    if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w0, args.cpu_seconds)
+    del buf
+    torch.cuda.empty_cache()
+
+    if not args.no_blocks:
+        # the other workloads the throughput target names, each timed the same way
+        blocks = {}
+        for name in BLOCK_WORKLOADS:
+            if name == w0.name:
+                continue
+            b, bb = measure_workload(ep, ep_synth.get_workload(name), args, rank, world, device, flush_l2, K,
+                                     args.cpu_seconds / 3, main=False)
+            del bb
+            torch.cuda.empty_cache()
+            blocks[name] = b
+        line["workloads"] = blocks
+        # the sweep's latency floor at small T (and decode), in us per layer
+        LK = max(K, args.latency_steps)
+        line["latency"] = {name: latency_point(ep, ep_synth.get_workload(name), args, rank, world, device,
+                                               flush_l2, LK) for name in LATENCY_WORKLOADS}
+        torch.cuda.empty_cache()
+    if ep.ep_device_error() != 0:
+        raise RuntimeError("a kernel gave up on a bounded wait during the benchmark")
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -143,3 +143,22 @@ def test_rank_static_table_tiles_the_rows_once(R, W):
             assert begin == rank_offset[r] and n == rank_offset[r + 1] - rank_offset[r]
             covered[begin:begin + n] += 1
     assert (covered == 1).all()
+
+
+def test_whole_job_and_step_stats():
+    # 3 ranks, 1.5 GB per step each, 10 steps, slowest rank 4 ms in total -> 0.4 ms per step
+    v, ms = bench.whole_job(1_500_000_000, 3, 10, 4.0)
+    assert ms == pytest.approx(0.4)
+    assert v == pytest.approx(3 * 1.5 / 0.4e-3)
+    st = bench.step_stats_us([0.003, 0.001, 0.002, 0.004, 0.005, 0.006, 0.007, 0.008, 0.009, 0.010])
+    assert st == {"median": 6.0, "p10": 2.0, "p90": 10.0, "min": 1.0, "max": 10.0}
+    assert bench.reduce_max_many({"a": 1, "b": 2.5}, 1) == {"a": 1.0, "b": 2.5}
+
+
+def test_default_workload_is_the_largest_single_gpu_one():
+    names = [w.name for w in ep_synth.sweep_workloads()] + list(ep_synth.CONFIGS)
+    biggest = max(names, key=lambda n: ep_synth.get_workload(n).total_bytes())
+    assert ep_synth.get_workload(bench.DEFAULT_WORKLOAD).total_bytes() == ep_synth.get_workload(biggest).total_bytes()
+    assert bench.parse_args([]).config == bench.DEFAULT_WORKLOAD
+    for n in bench.BLOCK_WORKLOADS + bench.LATENCY_WORKLOADS:
+        ep_synth.get_workload(n)
