@@ -12,29 +12,9 @@ namespace {
 
 constexpr unsigned kBarrierSpinLimit = 1u << 22;  // polls of ~64 ns before giving up
 
-// A launch reports a CTA that gave up on a bounded wait through *n_chunks = -1,
-// the same word that carries the chunk count on success. The CTA that gives up
-// and the CTA that writes the count are different CTAs of one launch with no
-// order between them, so both go through these helpers: the failing CTA first
-// raises the launch's failure word (zeroed before the launch), and the count's
-// writer re-reads that word after its own write and puts -1 back if it is
-// raised. With a full fence on each side, -1 is the final value whenever any
-// CTA failed, whichever of the two writes to n_chunks lands last; a -1 left by
-// an earlier failed call is overwritten by the next successful one.
-__device__ __forceinline__ void mark_launch_failed(unsigned *fail, int32_t *n_chunks) {
-    atomicExch(fail, 1u);
-    __threadfence();
-    atomicExch(n_chunks, -1);
-}
-
-// fail may be null when no CTA of the launch can give up before the count is written.
-__device__ __forceinline__ void publish_chunk_count(int32_t *n_chunks, int32_t count, unsigned *fail) {
-    atomicExch(n_chunks, count);
-    if (fail) {
-        __threadfence();
-        if (atomicOr(fail, 0u) != 0u) atomicExch(n_chunks, -1);
-    }
-}
+// Top bit of a grid barrier's arrival counter: set by a CTA that gave up
+// waiting while the barrier was still incomplete (see grid_barrier).
+constexpr unsigned kBarrierPoison = 0x80000000u;
 
 // ---------------------------------------------------------------------------
 // shared device pieces
@@ -279,7 +259,7 @@ __device__ __forceinline__ int32_t share_bound(int32_t N, int32_t w, int32_t W) 
 // scan over the counts writes its chunks.
 __device__ void build_schedule_two_tiers(const int32_t *s_roff, int32_t R, int32_t W, int32_t ranks_per_node,
                                          int32_t self_rank, ep_chunk *chunks, int32_t *n_chunks,
-                                         int32_t *worker_begin, int *s_warp, int32_t *s_P, unsigned *fail) {
+                                         int32_t *worker_begin, int *s_warp, int32_t *s_P) {
     const int32_t node = self_rank / ranks_per_node;
     const int32_t n_lo = node * ranks_per_node;
     const int32_t n_hi = n_lo + ranks_per_node < R ? n_lo + ranks_per_node : R;
@@ -339,7 +319,7 @@ __device__ void build_schedule_two_tiers(const int32_t *s_roff, int32_t R, int32
     }
     if (threadIdx.x == 0) {
         worker_begin[W] = carry;
-        publish_chunk_count(n_chunks, carry, fail);
+        *n_chunks = carry;
     }
 }
 
@@ -377,7 +357,7 @@ __device__ __forceinline__ ClassRuns class_runs(int c, int32_t R, int32_t nl, in
 template <int NC, int BAR>
 __device__ __noinline__ void build_schedule_nc(const int32_t *s_roff, int32_t R, int32_t W, HopTiers h,
                                                ep_chunk *chunks, int32_t *n_chunks, int32_t *worker_begin,
-                                               int *s_warp, int32_t *s_P, ThreadGroup<BAR> g, unsigned *fail) {
+                                               int *s_warp, int32_t *s_P, ThreadGroup<BAR> g) {
     const int32_t nl = h.self_rank / h.ranks_per_node * h.ranks_per_node;
     const int32_t nh = nl + h.ranks_per_node < R ? nl + h.ranks_per_node : R;
     const int32_t pl = NC == 3 ? h.self_rank / h.ranks_per_pod * h.ranks_per_pod : 0;
@@ -454,22 +434,21 @@ __device__ __noinline__ void build_schedule_nc(const int32_t *s_roff, int32_t R,
     }
     if (g.tid == 0) {
         worker_begin[W] = carry;
-        publish_chunk_count(n_chunks, carry, fail);
+        *n_chunks = carry;
     }
 }
 
 template <int BAR>
 __device__ __forceinline__ void cta_build_schedule(const int32_t *s_roff, int32_t R, int32_t W, HopTiers h,
                                                    ep_chunk *chunks, int32_t *n_chunks, int32_t *worker_begin,
-                                                   int *s_warp, int32_t *s_P, ThreadGroup<BAR> g,
-                                                   unsigned *fail = nullptr) {
+                                                   int *s_warp, int32_t *s_P, ThreadGroup<BAR> g) {
     if (h.ranks_per_pod > 0)
-        build_schedule_nc<3, BAR>(s_roff, R, W, h, chunks, n_chunks, worker_begin, s_warp, s_P, g, fail);
+        build_schedule_nc<3, BAR>(s_roff, R, W, h, chunks, n_chunks, worker_begin, s_warp, s_P, g);
     else if (BAR == 0)
         build_schedule_two_tiers(s_roff, R, W, h.ranks_per_node, h.self_rank, chunks, n_chunks, worker_begin, s_warp,
-                                 s_P, fail);
+                                 s_P);
     else
-        build_schedule_nc<2, BAR>(s_roff, R, W, h, chunks, n_chunks, worker_begin, s_warp, s_P, g, fail);
+        build_schedule_nc<2, BAR>(s_roff, R, W, h, chunks, n_chunks, worker_begin, s_warp, s_P, g);
 }
 
 // ---------------------------------------------------------------------------
@@ -488,8 +467,16 @@ __device__ __forceinline__ void red_release_gpu_add(unsigned *p, unsigned v) {
 
 // Grid barrier for co-resident CTAs: after a CTA barrier, thread 0 arrives
 // with a release add and polls with acquire loads, then a CTA barrier releases
-// the other threads. Bounded: returns false (for every thread of the CTA) if
-// the count did not arrive in time.
+// the other threads. Bounded: a CTA that has polled max_polls times gives up
+// by setting the counter's top bit (kBarrierPoison) with a compare-and-swap
+// that only succeeds on a count below `expected`. So the top bit is set only
+// while the barrier is incomplete, and once set it is seen by every CTA that
+// reads the counter later: they all return false, and no CTA of the launch
+// goes on with another's results missing (in particular none writes a chunk
+// count over the -1 a failing CTA leaves in *n_chunks). If the swap finds that
+// the last arrival came in meanwhile, the CTA goes on as if it had seen it.
+// The success path costs nothing extra: the check reads the value the poll
+// already loaded. The counter must be zero before the launch.
 __device__ bool grid_barrier(unsigned *arrivals, unsigned expected, unsigned max_polls = kBarrierSpinLimit) {
     __shared__ int s_ok;
     __syncthreads();
@@ -499,16 +486,26 @@ __device__ bool grid_barrier(unsigned *arrivals, unsigned expected, unsigned max
         // barrier below order every thread's later reads after the wait. No
         // separate fence is needed on either side.
         red_release_gpu_add(arrivals, 1u);
-        int ok = 1;
-        unsigned spins = 0;
-        while (ld_acquire_gpu(arrivals) < expected) {
+        unsigned spins = 0, v;
+        while ((v = ld_acquire_gpu(arrivals)) < expected) {
             if (++spins > max_polls) {
-                ok = 0;
+                // Each failed swap means the counter moved (an arrival, or another
+                // CTA's poison): at most expected + 1 rounds.
+                for (;;) {
+                    const unsigned prev = atomicCAS(arrivals, v, v | kBarrierPoison);
+                    if (prev == v) {
+                        v |= kBarrierPoison;
+                        break;
+                    }
+                    v = prev;
+                    if ((v & kBarrierPoison) != 0u || v >= expected) break;
+                }
+                __threadfence();  // acquire side for the case that the last arrival did come in
                 break;
             }
             if (spins > 64) __nanosleep(32);
         }
-        s_ok = ok;
+        s_ok = (v & kBarrierPoison) == 0u && v >= expected;
     }
     __syncthreads();
     return s_ok != 0;

@@ -103,7 +103,7 @@ struct FusedArgs {
     int32_t *counts;  // [nb][E] per-tile counts
     int32_t *bases;   // [nb][E] per-tile base inside each expert
     int32_t *totals;  // [E]
-    unsigned *sync;   // [3] arrivals of the two grid barriers, the launch's failure word
+    unsigned *sync;   // [2] arrivals of the two grid barriers
     int32_t *err;
     int32_t T, H, E, R, k, n_groups, topk_groups, renormalize, W;
     HopTiers tiers;
@@ -113,7 +113,7 @@ struct FusedArgs {
 };
 
 template <int VPL>
-__global__ void __launch_bounds__(kFusedThreads) dispatch_fused_kernel(FusedArgs a) {
+__global__ void __launch_bounds__(kFusedThreads, 2) dispatch_fused_kernel(FusedArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int s_warp32[32];
     const SmemLayout L = smem_layout(a.ns, a.row_pad, a.tb, a.k, a.E, a.R, a.n_groups > 1);
@@ -271,12 +271,12 @@ __global__ void __launch_bounds__(kFusedThreads) dispatch_fused_kernel(FusedArgs
             for (int r = threadIdx.x; r <= a.R; r += blockDim.x) s_roff[r] = s_eoff[r * epr];
             __syncthreads();
             cta_build_schedule(s_roff, a.R, a.W, a.tiers, a.chunks, a.n_chunks, a.worker_begin, s_warp32, s_P,
-                               whole_cta(), &a.sync[2]);
+                               whole_cta());
         }
         __syncthreads();
     } else if (threadIdx.x == 0) {
         atomicOr(a.err, kErrFusedWait);
-        mark_launch_failed(&a.sync[2], a.n_chunks);
+        atomicExch(a.n_chunks, -1);
     }
 
     // G. dispatch the tile. When the rows to move are few, a combine launched
@@ -530,8 +530,10 @@ cudaError_t launch_dispatch_fused(const ep_config &c, int32_t W, const float *lo
     a.row_pad = p.row_pad;
     // measured: T = 1..64 (<= 7.3 MB of send rows) gain 1-2 us, T = 256 even, T = 512 (59 MB) loses 1.8 us
     a.early_dependents = (int64_t)c.T * c.k * c.H * 2 <= (int64_t)16 << 20 ? 1 : 0;
-    e = cudaMemsetAsync(a.sync, 0, 3 * sizeof(unsigned), s);
-    if (e != cudaSuccess) return e;
+    if (p.nb + p.sched_cta > 1) {  // a single CTA uses no grid barrier (and the memset costs ~0.5 us at T = 1)
+        e = cudaMemsetAsync(a.sync, 0, 2 * sizeof(unsigned), s);
+        if (e != cudaSuccess) return e;
+    }
     void *args[] = {&a};
     return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(pick_kernel(c.E)),
                                        dim3((unsigned)(p.nb + p.sched_cta)),

@@ -127,9 +127,8 @@ layout_fused_kernel(const int32_t *__restrict__ idx, int32_t T, int32_t E, int32
     const int64_t t_cta = (int64_t)b * tpw * nw;
     cta_rank_tokens(idx, T, E, k, t_cta, cnt, tile_e, tile_r, counts + (int64_t)b * E, 1, tpw);
 
-    // sync[1] is the launch's failure word (zeroed with the barrier's counter).
     if (nb > 1 && !grid_barrier(&sync[0], (unsigned)nb)) {
-        if (threadIdx.x == 0) mark_launch_failed(&sync[1], n_chunks);
+        if (threadIdx.x == 0) atomicExch(n_chunks, -1);
         return;
     }
 
@@ -214,8 +213,7 @@ layout_fused_kernel(const int32_t *__restrict__ idx, int32_t T, int32_t E, int32
     if (b == nb - 1 && !defer_schedule) {
         for (int r = threadIdx.x; r <= R; r += blockDim.x) s_roff[r] = s_eoff[r * epr];
         __syncthreads();
-        cta_build_schedule(s_roff, R, W, tiers, chunks, n_chunks, worker_begin, s_warp32, s_P, whole_cta(),
-                           nb > 1 ? &sync[1] : nullptr);
+        cta_build_schedule(s_roff, R, W, tiers, chunks, n_chunks, worker_begin, s_warp32, s_P, whole_cta());
     }
 }
 
@@ -416,52 +414,50 @@ cudaError_t launch_layout(const ep_config &c, int32_t W, const int32_t *idx, int
 }  // namespace ep
 
 // ---------------------------------------------------------------------------
-// Self-check of the bounded grid barrier and of the failure mark: CTAs 0 and
-// 1 wait at a grid barrier that expects three arrivals while CTA 2 never
-// arrives, so both must give up after max_polls polls, count themselves and
-// mark the launch failed (*n_chunks = -1 on a stand-in word). CTA 2 plays the
-// CTA that writes the chunk count: it waits (bounded) until the failure word
-// is raised and only then writes a count, the order in which a plain store
-// would have hidden the failure. A second kernel turns a surviving count into
-// *gave_up = -1.
+// Self-check of the bounded grid barrier: CTAs 0 and 1 wait at a grid barrier
+// that expects three arrivals; CTA 2 arrives only after one of them has given
+// up (it waits, bounded, for the counter's top bit), the order in which the
+// last arrival would let a CTA go on with a result missing. CTAs 0 and 1 must
+// give up after max_polls polls and count themselves in *gave_up, and CTA 2
+// must see the failure too; a second kernel sets *gave_up = -1 if it did not.
 // ---------------------------------------------------------------------------
 namespace ep {
 namespace {
 
-static __device__ unsigned g_check_words[2];  // barrier arrivals, failure word
-static __device__ int32_t g_check_count;      // stands in for *n_chunks
+static __device__ unsigned g_check_arrivals;
+static __device__ int32_t g_check_late_passed;  // 1: the late CTA passed the barrier
 
-__global__ void bounded_wait_check_kernel(unsigned *words, int32_t *count, unsigned max_polls, int32_t *gave_up) {
+__global__ void bounded_wait_check_kernel(unsigned *arrivals, int32_t *late_passed, unsigned max_polls,
+                                          int32_t *gave_up) {
     if (blockIdx.x < 2) {
-        if (!grid_barrier(&words[0], 3u, max_polls) && threadIdx.x == 0) {
-            atomicAdd(gave_up, 1);
-            mark_launch_failed(&words[1], count);
-        }
-    } else if (threadIdx.x == 0) {
-        const uint64_t limit = 4ull * max_polls + 1024ull;
-        for (uint64_t i = 0; i < limit && atomicOr(&words[1], 0u) == 0u; ++i) __nanosleep(64);
-        publish_chunk_count(count, 123, &words[1]);
+        if (!grid_barrier(arrivals, 3u, max_polls) && threadIdx.x == 0) atomicAdd(gave_up, 1);
+        return;
     }
+    if (threadIdx.x == 0) {
+        const uint64_t limit = 4ull * max_polls + 1024ull;
+        for (uint64_t i = 0; i < limit && (atomicOr(arrivals, 0u) & kBarrierPoison) == 0u; ++i) __nanosleep(64);
+    }
+    if (grid_barrier(arrivals, 3u, max_polls) && threadIdx.x == 0) *late_passed = 1;
 }
 
-__global__ void bounded_wait_verdict_kernel(const int32_t *count, int32_t *gave_up) {
-    if (*count != -1) *gave_up = -1;
+__global__ void bounded_wait_verdict_kernel(const int32_t *late_passed, int32_t *gave_up) {
+    if (*late_passed != 0) *gave_up = -1;
 }
 
 }  // namespace
 
 cudaError_t launch_bounded_wait_check(uint32_t max_polls, int32_t *gave_up, cudaStream_t s) {
-    void *words = nullptr, *count = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&words, g_check_words);
+    void *arrivals = nullptr, *late = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&arrivals, g_check_arrivals);
     if (e != cudaSuccess) return e;
-    if ((e = cudaGetSymbolAddress(&count, g_check_count)) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(words, 0, 2 * sizeof(unsigned), s)) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(count, 0, sizeof(int32_t), s)) != cudaSuccess) return e;
+    if ((e = cudaGetSymbolAddress(&late, g_check_late_passed)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(arrivals, 0, sizeof(unsigned), s)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(late, 0, sizeof(int32_t), s)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(gave_up, 0, sizeof(int32_t), s)) != cudaSuccess) return e;
-    bounded_wait_check_kernel<<<3, 32, 0, s>>>(static_cast<unsigned *>(words), static_cast<int32_t *>(count),
+    bounded_wait_check_kernel<<<3, 32, 0, s>>>(static_cast<unsigned *>(arrivals), static_cast<int32_t *>(late),
                                                max_polls, gave_up);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    bounded_wait_verdict_kernel<<<1, 1, 0, s>>>(static_cast<const int32_t *>(count), gave_up);
+    bounded_wait_verdict_kernel<<<1, 1, 0, s>>>(static_cast<const int32_t *>(late), gave_up);
     return cudaGetLastError();
 }
 

@@ -116,14 +116,15 @@ int ep_version(void);
 ep_status ep_device_error(int32_t *flags);
 
 /* Diagnostics: checks that the library's device-side waits are bounded and
- * that a launch's failure mark survives. Launches two CTAs into a grid barrier
- * (the kind ep_layout and ep_dispatch_fused use) that expects three arrivals,
- * so the wait can never complete; each CTA must give up after max_polls polls
- * (> 0), count itself in *gave_up (device int32, zeroed first) and mark the
- * launch failed the way ep_layout marks *n_chunks = -1. A third CTA then
- * writes a chunk count the way the schedule's writer does, after the failure
- * mark; if that count survives, *gave_up is set to -1. Expected result: 2.
- * The kernels return normally; nothing faults or hangs. */
+ * that a failure cannot be hidden. Launches two CTAs into a grid barrier (the
+ * kind ep_layout and ep_dispatch_fused use) that expects three arrivals, so
+ * the wait cannot complete in time; each CTA must give up after max_polls
+ * polls (> 0) and count itself in *gave_up (device int32, zeroed first). A
+ * third CTA makes the last arrival only after one of them has given up; it
+ * must see the failure as well (in ep_layout that keeps the CTA that writes
+ * the chunk count from overwriting *n_chunks = -1), else *gave_up is set to
+ * -1. Expected result: 2. The kernels return normally; nothing faults or
+ * hangs. */
 ep_status ep_check_bounded_wait(int32_t max_polls, int32_t *gave_up, cudaStream_t stream);
 
 /* Bytes of device scratch that ep_layout needs for `cfg` (it depends on T and
