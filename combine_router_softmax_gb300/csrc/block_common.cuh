@@ -215,7 +215,7 @@ __device__ void cta_rank_tokens(const int32_t *__restrict__ idx, int32_t T, int3
     const int64_t left = (int64_t)T - t_cta;
     const int ntok = left <= 0 ? 0 : (left >= tpw * nw ? tpw * nw : (int)left);
     const int np = ntok * k;
-    for (int i = threadIdx.x; i < np; i += blockDim.x) tile_e[i] = __ldg(idx + t_cta * k + i);
+    for (int i = threadIdx.x; i < np; i += blockDim.x) tile_e[i] = __ldcg(idx + t_cta * k + i);
     cta_rank_pairs(tile_e, np, tpw * k, E, cnt, tile_r, cta_count, stride);
 }
 

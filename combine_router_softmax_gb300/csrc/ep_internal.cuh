@@ -69,15 +69,22 @@ cudaError_t launch_route(const ep_config &c, const float *logits, int32_t *idx, 
                          unsigned *za = nullptr, int na = 0, unsigned *zb = nullptr, int nb = 0,
                          int32_t *zc = nullptr);
 
+// Whether every CTA of the route kernel for c is resident at once on the current device.
+bool route_one_wave(const ep_config &c);
+
 // sync_zeroed: the caller already zeroed the workspace's sync words (skip the memset).
 // defer_schedule: when the layout runs as the single cooperative kernel, leave
 // the chunk schedule to the caller (*deferred = true; chunks, n_chunks and
 // worker_begin are then not written, except n_chunks = -1 on failure).
+// after_route: the single-kernel layout follows the route kernel in the same
+// stream and is launched as its programmatic dependent.
+// zero_ctr: a word the single-kernel layout zeroes before a dependent grid
+// can start (the bulk dispatch's token counter).
 cudaError_t launch_layout(const ep_config &c, int32_t W, const int32_t *idx, int32_t *expert_count,
                           int32_t *expert_offset, int32_t *rank_count, int32_t *rank_offset, int32_t *slot,
                           ep_chunk *chunks, int32_t *n_chunks, int32_t *worker_begin, void *workspace,
                           cudaStream_t s, bool sync_zeroed = false, bool defer_schedule = false,
-                          bool *deferred = nullptr);
+                          bool *deferred = nullptr, bool after_route = false, unsigned *zero_ctr = nullptr);
 
 // Runs two CTAs into a grid barrier that expects three; *gave_up counts the
 // CTAs that stopped waiting after max_polls polls (2 when the bound works).

@@ -480,11 +480,21 @@ cudaError_t launch_dispatch_fused(const ep_config &c, int32_t W, const float *lo
         // dispatch back for it; the route kernel zeroes n_chunks, which the
         // layout sets to -1 if it fails.
         const bool defer = dispatch_uses_bulk(c, slot);
-        cudaError_t e = launch_route(c, logits, topk_idx, topk_w, s, lsync, 2, ctr, 1, defer ? n_chunks : nullptr);
+        // The single-kernel layout zeroes the dispatch counter itself. While
+        // the route kernel runs in one wave the layout is its programmatic
+        // dependent (the dispatch, the layout's dependent, may then start
+        // while the route kernel still runs). Measured: prefill -1.4 us;
+        // with several waves of route CTAs the early grids took resources from
+        // the later ones (T = 32768: +4.6 us), so there the layout waits.
+        const bool single = layout_kernel_count(c) == 1;
+        const bool after_route = single && route_one_wave(c);
+        cudaError_t e = launch_route(c, logits, topk_idx, topk_w, s, lsync, 2, single ? nullptr : ctr, single ? 0 : 1,
+                                     defer ? n_chunks : nullptr);
         if (e != cudaSuccess) return e;
         bool deferred = false;
         e = launch_layout(c, W, topk_idx, expert_count, expert_offset, rank_count, rank_offset, slot, chunks,
-                          n_chunks, worker_begin, workspace, s, true, defer, &deferred);
+                          n_chunks, worker_begin, workspace, s, true, defer, &deferred, after_route,
+                          single ? ctr : nullptr);
         if (e != cudaSuccess) return e;
         const ScheduleTask st{rank_offset, chunks, n_chunks, worker_begin, c.R, W, hop_tiers(c)};
         return launch_dispatch(c, x, slot, send, meta, s, ctr, true, true, deferred ? &st : nullptr);

@@ -107,11 +107,23 @@ layout_fused_kernel(const int32_t *__restrict__ idx, int32_t T, int32_t E, int32
                     int32_t *__restrict__ expert_offset, int32_t *__restrict__ rank_count,
                     int32_t *__restrict__ rank_offset, int32_t *__restrict__ slot, ep_chunk *__restrict__ chunks,
                     int32_t *__restrict__ n_chunks, int32_t *__restrict__ worker_begin, int32_t W,
-                    HopTiers tiers, int32_t defer_schedule, int32_t tpw) {
+                    HopTiers tiers, int32_t defer_schedule, int32_t tpw, unsigned *__restrict__ zero_ctr) {
     extern __shared__ int32_t sm[];
     // A dispatch launched after this kernel may start now and fetch x rows
-    // (it waits for this grid before it reads a slot).
+    // (it waits for this grid before it reads a slot). Its token counter, if
+    // any, is zeroed first: the dispatch grid can start only once every CTA
+    // of this one has passed this point.
+    if (zero_ctr != nullptr && blockIdx.x == 0) {
+        if (threadIdx.x == 0) {
+            *zero_ctr = 0u;
+            __threadfence();
+        }
+        __syncthreads();
+    }
     grid_launch_dependents();
+    // Launched right after the route kernel, this grid may start before that
+    // one has finished: nothing it writes is read before this wait.
+    grid_dependency_wait();
     const int nw = blockDim.x >> 5;
     int32_t *cnt = sm;                         // [nw][E]
     int32_t *tile_e = cnt + nw * E;            // [nw][tpw k]
@@ -384,7 +396,8 @@ int layout_kernel_count(const ep_config &c) {
 cudaError_t launch_layout(const ep_config &c, int32_t W, const int32_t *idx, int32_t *expert_count,
                           int32_t *expert_offset, int32_t *rank_count, int32_t *rank_offset, int32_t *slot,
                           ep_chunk *chunks, int32_t *n_chunks, int32_t *worker_begin, void *workspace,
-                          cudaStream_t s, bool sync_zeroed, bool defer_schedule, bool *deferred) {
+                          cudaStream_t s, bool sync_zeroed, bool defer_schedule, bool *deferred, bool after_route,
+                          unsigned *zero_ctr) {
     if (deferred) *deferred = false;
     int nw = 0, tpw = 32;
     int64_t nb = 0;
@@ -404,9 +417,37 @@ cudaError_t launch_layout(const ep_config &c, int32_t W, const int32_t *idx, int
     HopTiers tiers = hop_tiers(c);
     int32_t defer = defer_schedule ? 1 : 0;
     if (deferred) *deferred = defer_schedule;
+    // Set when a device refused the launch below; the plain cooperative launch
+    // is then used (the same results, the route -> layout gap not hidden).
+    static std::atomic<bool> no_dependent_coop[kMaxDevices_];  // zero-initialised: false
+    int dev = 0;
+    if (after_route && (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices_)) after_route = false;
+    if (after_route && !no_dependent_coop[dev]) {
+        // A cooperative launch that may also start before the route kernel in
+        // front of it has finished (programmatic dependent launch).
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)nb);
+        cfg.blockDim = dim3((unsigned)(nw * 32));
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, layout_fused_kernel, idx, T, E, R, k, nbi, counts, sync,
+                                                 expert_count, expert_offset, rank_count, rank_offset, slot, chunks,
+                                                 n_chunks, worker_begin, W, tiers, defer, tpw, zero_ctr);
+        if (e != cudaErrorInvalidValue && e != cudaErrorNotSupported) return e;
+        cudaGetLastError();  // the launch was refused before anything was enqueued
+        no_dependent_coop[dev] = true;
+    }
     void *args[] = {(void *)&idx, &T, &E, &R, &k, &nbi, (void *)&counts, (void *)&sync, (void *)&expert_count,
                     (void *)&expert_offset, (void *)&rank_count, (void *)&rank_offset, (void *)&slot,
-                    (void *)&chunks, (void *)&n_chunks, (void *)&worker_begin, &W, &tiers, &defer, &tpw};
+                    (void *)&chunks, (void *)&n_chunks, (void *)&worker_begin, &W, &tiers, &defer, &tpw,
+                    (void *)&zero_ctr};
     return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(layout_fused_kernel), dim3((unsigned)nb),
                                        dim3((unsigned)(nw * 32)), args, smem, s);
 }

@@ -21,6 +21,9 @@ route_kernel(const float *__restrict__ logits, int32_t T, int32_t E, int32_t k, 
              float *__restrict__ topk_w, unsigned *__restrict__ zero_a, int n_zero_a, unsigned *__restrict__ zero_b,
              int n_zero_b, int32_t *__restrict__ zero_c) {
     extern __shared__ float s_dyn[];  // [kRouteWarps][E] logits, group-limited routing only
+    // A layout launched after this kernel may start now: it waits for this
+    // grid before it reads anything this one writes.
+    grid_launch_dependents();
     // Reset the counters that later kernels of the same call sequence start from.
     if (blockIdx.x == 0) {
         if ((int)threadIdx.x < n_zero_a) zero_a[threadIdx.x] = 0u;
@@ -53,6 +56,19 @@ cudaError_t launch_vpl(const ep_config &c, const float *logits, int32_t *idx, fl
 }
 
 }  // namespace
+
+bool route_one_wave(const ep_config &c) {
+    const int vpl = (c.E + 31) / 32;
+    const void *fn = vpl <= 1 ? reinterpret_cast<const void *>(route_kernel<1>)
+                   : vpl <= 2 ? reinterpret_cast<const void *>(route_kernel<2>)
+                   : vpl <= 4 ? reinterpret_cast<const void *>(route_kernel<4>)
+                   : vpl <= 8 ? reinterpret_cast<const void *>(route_kernel<8>)
+                   : vpl <= 16 ? reinterpret_cast<const void *>(route_kernel<16>)
+                               : reinterpret_cast<const void *>(route_kernel<32>);
+    const size_t smem = c.n_groups > 1 ? sizeof(float) * kRouteWarps * (size_t)c.E : 0;
+    const int64_t ctas = ((int64_t)c.T + kRouteWarps - 1) / kRouteWarps;
+    return ctas <= (int64_t)current_device_sm_count() * max_blocks_per_sm(fn, kRouteWarps * 32, smem);
+}
 
 cudaError_t launch_route(const ep_config &c, const float *logits, int32_t *idx, float *w, cudaStream_t s,
                          unsigned *za, int na, unsigned *zb, int nb, int32_t *zc) {
