@@ -221,7 +221,7 @@ __device__ void cta_rank_tokens(const int32_t *__restrict__ idx, int32_t T, int3
 
 // Largest i in [0, n) with P[i] <= x, for P non-decreasing with P[0] <= x.
 // 4-ary search: three independent pivot compares narrow the range 4x per step.
-__device__ __forceinline__ int32_t quaternary_search(const int32_t *P, int32_t n, int32_t x) {
+__device__ __noinline__ int32_t quaternary_search(const int32_t *P, int32_t n, int32_t x) {
     int32_t lo = 0, hi = n;  // answer in [lo, hi), P[lo] <= x
     while (hi - lo > 1) {
         const int32_t len = hi - lo;
@@ -278,7 +278,7 @@ __device__ void build_schedule_two_tiers(const int32_t *s_roff, int32_t R, int32
         int32_t first[2] = {0, 0}, last[2] = {-1, -1}, lo[2] = {0, 0}, hi[2] = {0, 0};
         int cnt = 0;
         if (w < W) {
-#pragma unroll
+#pragma unroll 1
             for (int c = 0; c < 2; ++c) {
                 const int32_t *P = c ? P1 : P0;
                 const int32_t n = c ? n1 : n0;
@@ -296,7 +296,7 @@ __device__ void build_schedule_two_tiers(const int32_t *s_roff, int32_t R, int32
         if (w < W) {
             worker_begin[w] = pos0;
             int pos = pos0;
-#pragma unroll
+#pragma unroll 1
             for (int cc = 0; cc < 2; ++cc) {
                 const int c = 1 - cc;  // other-node traffic first
                 const int32_t *P = c ? P1 : P0;

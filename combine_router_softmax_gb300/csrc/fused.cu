@@ -163,8 +163,8 @@ __global__ void __launch_bounds__(kFusedThreads, 2) dispatch_fused_kernel(FusedA
         const int64_t t = t0 + i;
         int e;
         float w;
-        route_token<VPL>(a.logits + t * E, E, k, a.n_groups, a.topk_groups, a.renormalize, lane, glog + warp * E,
-                         cand + warp * 32, pick + warp * 32, e, w);
+        route_token<VPL, true>(a.logits + t * E, E, k, a.n_groups, a.topk_groups, a.renormalize, lane,
+                               glog + warp * E, cand + warp * 32, pick + warp * 32, e, w);
         if (lane < k) {
             tile_e[i * k + lane] = e;
             a.topk_idx[t * k + lane] = e;

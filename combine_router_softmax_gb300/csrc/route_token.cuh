@@ -69,10 +69,91 @@ __device__ __forceinline__ float warp_sort_desc(float s, int lane) {
     return s;
 }
 
+// Group limiting: clears the elig bits of experts outside the topk_groups
+// groups with the largest per-group maximum logit (ties to the lower group).
+template <int VPL>
+__device__ __forceinline__ uint32_t group_limit(const float (&v)[VPL], uint32_t elig, int32_t E, int32_t n_groups,
+                                                int32_t topk_groups, int lane, float *s_glog) {
+    float *sl = s_glog;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E) sl[e] = v[i];
+    }
+    __syncwarp();
+    const int gsize = E / n_groups;
+    float gs = -INFINITY;
+    bool avail = lane < n_groups;
+    if (avail) {
+        gs = sl[lane * gsize];
+        for (int q = 1; q < gsize; ++q) {
+            const float c = sl[lane * gsize + q];
+            if (c > gs) gs = c;
+        }
+    }
+    uint32_t kept = 0;
+    for (int r = 0; r < topk_groups; ++r) {
+        float bv = gs;
+        int bi = avail ? lane : INT_MAX;
+        warp_argmax(bv, bi);
+        kept |= 1u << bi;
+        if (lane == bi) avail = false;
+    }
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && !((kept >> (e / gsize)) & 1u)) elig &= ~(1u << i);
+    }
+    return elig;
+}
+
+// Massive ties (more than 32 candidates): k rounds of arg-max; lane j ends
+// with pick j.
+template <int VPL>
+__device__ __forceinline__ void topk_by_rounds(const float (&v)[VPL], uint32_t elig, int32_t k, int lane,
+                                               float &my_v, int &my_e) {
+    uint32_t avail = elig;
+    for (int j = 0; j < k; ++j) {
+        float bv = -INFINITY;
+        int bi = INT_MAX;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            if (((avail >> i) & 1u) && (bi == INT_MAX || v[i] > bv)) {  // ascending e: strict > keeps the lower index
+                bv = v[i];
+                bi = lane + 32 * i;
+            }
+        }
+        warp_argmax(bv, bi);
+        if ((bi & 31) == lane) avail &= ~(1u << (bi >> 5));
+        if (lane == j) {
+            my_v = bv;
+            my_e = bi;
+        }
+    }
+}
+
+// The same two, out of line: in the fused small-batch kernel, whose time at
+// small T goes largely to fetching its own code after the caches were emptied,
+// rarely taken paths are kept out of the instruction stream of the common one
+// (measured: T = 1 -1.0 us, T = 8 -1.0 us, T = 64 -1.7 us, decode -0.6 us per
+// layer; in the route kernel, with many tokens per launch, they stay inline:
+// there the calls cost 0.6 us at prefill and 2 us at mid).
+template <int VPL>
+__device__ __noinline__ uint32_t group_limit_cold(const float (&v)[VPL], uint32_t elig, int32_t E, int32_t n_groups,
+                                                  int32_t topk_groups, int lane, float *s_glog) {
+    return group_limit<VPL>(v, elig, E, n_groups, topk_groups, lane, s_glog);
+}
+template <int VPL>
+__device__ __noinline__ void topk_by_rounds_cold(const float (&v)[VPL], uint32_t elig, int32_t k, int lane,
+                                                 float &my_v, int &my_e) {
+    topk_by_rounds<VPL>(v, elig, k, lane, my_v, my_e);
+}
+
 // Routes the token whose logits start at `row`; on return lane j < k holds
 // pick j (out_e, out_w). s_glog: E floats (group-limited routing only);
-// s_cand, s_pick: 32 int2 each. The whole warp must call it.
-template <int VPL>
+// s_cand, s_pick: 32 int2 each. The whole warp must call it. kColdOutOfLine:
+// call the out-of-line group limiting and tie fallback.
+template <int VPL, bool kColdOutOfLine = false>
 __device__ __forceinline__ void route_token(const float *__restrict__ row, int32_t E, int32_t k, int32_t n_groups,
                                             int32_t topk_groups, int32_t renormalize, int lane, float *s_glog,
                                             int2 *s_cand, int2 *s_pick, int &out_e, float &out_w) {
@@ -91,36 +172,8 @@ __device__ __forceinline__ void route_token(const float *__restrict__ row, int32
 
     if (n_groups > 1) {
         // Group score = largest logit of the group; keep the topk_groups best.
-        float *sl = s_glog;
-#pragma unroll
-        for (int i = 0; i < VPL; ++i) {
-            const int e = lane + 32 * i;
-            if (e < E) sl[e] = v[i];
-        }
-        __syncwarp();
-        const int gsize = E / n_groups;
-        float gs = -INFINITY;
-        bool avail = lane < n_groups;
-        if (avail) {
-            gs = sl[lane * gsize];
-            for (int q = 1; q < gsize; ++q) {
-                const float c = sl[lane * gsize + q];
-                if (c > gs) gs = c;
-            }
-        }
-        uint32_t kept = 0;
-        for (int r = 0; r < topk_groups; ++r) {
-            float bv = gs;
-            int bi = avail ? lane : INT_MAX;
-            warp_argmax(bv, bi);
-            kept |= 1u << bi;
-            if (lane == bi) avail = false;
-        }
-#pragma unroll
-        for (int i = 0; i < VPL; ++i) {
-            const int e = lane + 32 * i;
-            if (e < E && !((kept >> (e / gsize)) & 1u)) elig &= ~(1u << i);
-        }
+        elig = kColdOutOfLine ? group_limit_cold<VPL>(v, elig, E, n_groups, topk_groups, lane, s_glog)
+                              : group_limit<VPL>(v, elig, E, n_groups, topk_groups, lane, s_glog);
     }
 
     // 1. tau = k-th largest lane maximum.
@@ -173,26 +226,10 @@ __device__ __forceinline__ void route_token(const float *__restrict__ row, int32
             my_v = __int_as_float(pk.x);
             my_e = pk.y;
         }
+    } else if (kColdOutOfLine) {
+        topk_by_rounds_cold<VPL>(v, elig, k, lane, my_v, my_e);  // massive ties
     } else {
-        // Massive ties: k rounds of arg-max.
-        uint32_t avail = elig;
-        for (int j = 0; j < k; ++j) {
-            float bv = -INFINITY;
-            int bi = INT_MAX;
-#pragma unroll
-            for (int i = 0; i < VPL; ++i) {
-                if (((avail >> i) & 1u) && (bi == INT_MAX || v[i] > bv)) {  // ascending e: strict > keeps the lower index
-                    bv = v[i];
-                    bi = lane + 32 * i;
-                }
-            }
-            warp_argmax(bv, bi);
-            if ((bi & 31) == lane) avail &= ~(1u << (bi >> 5));
-            if (lane == j) {
-                my_v = bv;
-                my_e = bi;
-            }
-        }
+        topk_by_rounds<VPL>(v, elig, k, lane, my_v, my_e);  // massive ties
     }
 
     const float m = __shfl_sync(0xffffffffu, my_v, 0);
