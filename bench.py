@@ -333,8 +333,9 @@ def workload_config(w, args, extra=None) -> dict:
 # GPU arm
 # ---------------------------------------------------------------------------
 
-def capture_step_graph(buf, device, fused: bool):
-    """route -> layout -> dispatch -> combine captured once into a CUDA graph.
+def capture_step_graph(buf, device, fused: bool, pre=None):
+    """route -> layout -> dispatch -> combine captured once into a CUDA graph
+    (after ``pre()``, e.g. an L2 flush, when given).
 
     Two eager passes on the capture stream first, so that every lazy set-up
     inside the library (attributes, occupancy, symbol addresses) happens
@@ -347,13 +348,33 @@ def capture_step_graph(buf, device, fused: bool):
     calls = step_calls(bound, fused)
     with torch.cuda.stream(cap):
         for _ in range(2):
+            if pre is not None:
+                pre()
             for _, fn in calls:
                 fn()
     cap.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=cap):
+        if pre is not None:
+            pre()
         for _, fn in calls:
             fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def capture_callable_graph(fn, device):
+    """fn() (torch work on the current stream) captured once into a CUDA graph."""
+    import torch
+
+    cap = torch.cuda.Stream(device)
+    cap.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(cap):
+        fn()
+    cap.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cap):
+        fn()
     torch.cuda.synchronize()
     return g
 
@@ -929,7 +950,9 @@ def measure_workload(ep, w0, args, rank: int, world: int, device, flush_l2, K: i
 def latency_point(ep, w0, args, rank: int, world: int, device, flush_l2, K: int) -> dict:
     """Per-layer latency of one small batch: the step's graph replayed K times,
     L2 flushed before each replay (outside the events); median and spread over
-    the replays, the slowest rank's median."""
+    the replays, the slowest rank's median (``us_per_layer``). Also the step's
+    marginal time inside a graph that holds the flush as well (``in_graph_us``,
+    no graph launch of its own, as in a model that runs its layers in one graph)."""
     import torch
 
     w = rank_workload(w0, rank)
@@ -949,13 +972,35 @@ def latency_point(ep, w0, args, rank: int, world: int, device, flush_l2, K: int)
     torch.cuda.synchronize()
     ms = [a.elapsed_time(b_) for a, b_ in ev]
     st = step_stats_us(ms)
-    red = reduce_max_many({"median": st["median"], "mean": 1e3 * sum(ms) / K}, world, device)
+
+    # The same step inside a graph that also holds the L2 flush, as a layer
+    # runs inside a whole model's graph: its marginal time is the mean replay
+    # time of [flush, step] minus that of [flush] alone (events around each
+    # replay; the launch of the graph itself is paid by both).
+    flush_step = capture_step_graph(buf, device, fused, pre=flush_l2)
+    flush_only = capture_callable_graph(flush_l2, device)
+
+    def mean_us(g, n):
+        for _ in range(3):
+            g.replay()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for a, b_ in evs:
+            a.record(stream)
+            g.replay()
+            b_.record(stream)
+        torch.cuda.synchronize()
+        return 1e3 * sum(a.elapsed_time(b_) for a, b_ in evs) / n
+
+    NG = max(K, 200)
+    in_graph = mean_us(flush_step, NG) - mean_us(flush_only, NG)
+    red = reduce_max_many({"median": st["median"], "mean": 1e3 * sum(ms) / K, "in_graph": in_graph}, world, device)
     peak, _ = measured_peak_gbs()
     out = {"us_per_layer": round(red["median"], 2), "us_mean": round(red["mean"], 2), "stats_us": st,
+           "in_graph_us": round(red["in_graph"], 2), "in_graph_steps": NG,
            "kernels": ep.ep_step_kernel_count(cfg, fused=fused), "bytes_per_step": w.total_bytes(),
            "hbm_fraction": round(w.total_bytes() / (red["median"] * 1e-6) / 1e9 / peak, 4), "steps": K,
            "T": w.T, "dist": "zipf 1.2" if w.zipf_s else "uniform"}
-    del graph, buf
+    del graph, flush_only, flush_step, buf
     return out
 
 
