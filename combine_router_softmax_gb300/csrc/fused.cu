@@ -470,8 +470,9 @@ cudaError_t launch_dispatch_fused(const ep_config &c, int32_t W, const float *lo
                                   void *workspace, cudaStream_t s) {
     FusedPlan p;
     if (!plan_fused(c, &p)) {
-        // Three kernels; the route kernel zeroes the layout's barrier words and
-        // the dispatch counter, so no memset sits between the kernels.
+        // Three kernels; the route kernel zeroes the layout's barrier words (and
+        // the dispatch counter unless the layout does, below), so no memset
+        // sits between the kernels.
         char *ws = static_cast<char *>(workspace);
         unsigned *lsync = reinterpret_cast<unsigned *>(ws + layout_workspace(c).sync_off);
         unsigned *ctr = reinterpret_cast<unsigned *>(ws + fused_counter_offset(c));

@@ -211,8 +211,10 @@ ep_status ep_route(const ep_config *cfg, const float *logits, int32_t *topk_idx,
  * When every layout CTA fits on the GPU at once, the layout is one
  * cooperative launch whose CTAs meet at a grid barrier in the workspace (two
  * words zeroed by an enqueued memset). That wait is bounded: a CTA that gives
- * up sets *n_chunks = -1 and leaves its slots unwritten (this cannot happen
- * under a cooperative launch, which only starts when all CTAs are resident).
+ * up sets *n_chunks = -1 and leaves its slots unwritten, and every other CTA
+ * of the launch then fails too, so no chunk count overwrites the -1 (this
+ * cannot happen under a cooperative launch, which only starts when all CTAs
+ * are resident).
  * Larger T uses three ordinary kernels.
  */
 ep_status ep_layout(const ep_config *cfg, const int32_t *topk_idx,
@@ -251,10 +253,12 @@ ep_status ep_dispatch(const ep_config *cfg, const ep_bf16 *x, const int32_t *slo
  * being computed. It pays off at small T (decode batches), where the phases
  * are latency-bound; when a CTA would have to route more than 8 tokens (T
  * above 8 tokens per resident CTA, about 2400 on a GB300) the call runs the
- * three separate steps instead (the route kernel zeroing the layout's and
- * dispatch's counters, the dispatch taking tokens dynamically and building
- * the chunk schedule in one extra CTA while the others copy rows), with the
- * same results.
+ * three separate steps instead (the route kernel zeroing the layout's
+ * barrier words, the single-kernel layout -- launched as a programmatic
+ * dependent of the route kernel when that one runs in a single wave --
+ * zeroing the dispatch's token counter, the dispatch taking tokens
+ * dynamically and building the chunk schedule in one extra CTA while the
+ * others copy rows), with the same results.
  *
  * workspace : >= ep_dispatch_fused_workspace_size bytes, 256-byte aligned.
  * A CTA that gives up a bounded wait sets ep_device_error bit 1 (2) and
