@@ -779,8 +779,8 @@ def prepare_layer(ep, w, device):
     return cfg, buf, logits_np, x_np
 
 
-def measure_workload(ep, w0, args, rank: int, world: int, device, flush_l2, K: int, cpu_seconds: float,
-                     main: bool) -> tuple[dict, object]:
+def measure_workload(ep, w0, args, rank: int, world: int, device, flush_l2, K: int,
+                     cpu_seconds: float) -> tuple[dict, object]:
     """Time one workload the way the JSON line reports it. Returns the
     workload's block (values already reduced over ranks) and its buffers."""
     import numpy as np
@@ -1021,7 +1021,7 @@ def run_gb300(args):
     flush_l2 = Flusher(device)
     K = args.steps
     w0 = ep_synth.get_workload(args.config)
-    block, buf = measure_workload(ep, w0, args, rank, world, device, flush_l2, K, args.cpu_seconds, main=True)
+    block, buf = measure_workload(ep, w0, args, rank, world, device, flush_l2, K, args.cpu_seconds)
 
     line = {
         "metric": METRIC,
@@ -1057,7 +1057,7 @@ def run_gb300(args):
             if name == w0.name:
                 continue
             b, bb = measure_workload(ep, ep_synth.get_workload(name), args, rank, world, device, flush_l2, K,
-                                     args.cpu_seconds / 3, main=False)
+                                     args.cpu_seconds / 3)
             del bb
             torch.cuda.empty_cache()
             blocks[name] = b
