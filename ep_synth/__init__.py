@@ -15,8 +15,7 @@ of ``seed ^ (tensor_id << 32)``, and the output is the SplitMix64 finaliser of
 that state (Steele, Lea and Flood, "Fast splittable pseudorandom number
 generators", OOPSLA 2014; constants as published by Vigna). Because element
 ``i`` depends only on ``i``, a workload with ``T`` tokens is a prefix of the
-same workload with more tokens, which the full-size parity tests use to check
-sampled tokens.
+same workload with more tokens, which the CPU baseline's token samples use.
 
 Normals come from the Box-Muller transform in float64 (two uniforms per pair,
 both outputs used), then are cast to float32; bf16 activations are the
