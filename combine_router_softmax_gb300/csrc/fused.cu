@@ -26,8 +26,19 @@
 //      bulk-store each row to its k send rows. When the send buffer is small
 //      (<= 16 MB) every CTA signals programmatic dependents here, so that a
 //      combine launched after it can start its prologue early.
+// Up to 64 tokens the split form of the same kernel is used instead (the
+// article's metadata/data decomposition): the tile CTAs (up to 8 tokens each,
+// one per routing warp) stop after F, releasing a per-tile ready flag once
+// their slots are written, and separate data CTAs -- as many as still fit on
+// the GPU, one per send row when there are enough, else one per token --
+// fetch their x row at once, acquire-poll the owning tile's flag (bounded)
+// and bulk-store the rows. Up to 8 tokens the metadata is then one CTA with no
+// grid barrier, and the rows leave from many SMs instead of one (measured per
+// layer: T = 8 21.6 -> 19.5 us, T = 16 22.7 -> 21.0, T = 1 -0.5, T = 64 -0.3; at
+// decode +0.3 and at T = 512 +4 us, so the split form stops at T = 64).
 // Every result equals what ep_route, ep_layout and ep_dispatch write.
 #include "block_common.cuh"
+#include "flag_ops.cuh"
 #include "route_token.cuh"
 
 namespace ep {
@@ -40,11 +51,14 @@ constexpr int kMaxFusedStages = 8;
 constexpr int kMaxFusedCTAs = 1024;
 constexpr uint32_t kFusedMaxPolls = 1u << 22;
 constexpr size_t kFusedSmemLimit = 200 * 1024;
+constexpr int kSplitMaxT = 64;  // split form up to this many tokens
 
 static __device__ int32_t g_fused_error;
 
 struct FusedPlan {
     int nb = 0;       // CTAs (tiles)
+    int n_data = 0;   // split form: data CTAs (0: the tile CTAs move their own rows)
+    int unit_rows = 0;  // split form: rows per data unit (1 or k)
     int tb = 0;       // tokens in the largest tile
     int ns = 0;       // x-row stages per CTA (bulk path), 0 = vector copy
     int row_pad = 0;  // bytes per stage
@@ -110,9 +124,46 @@ struct FusedArgs {
     int32_t nb, tb, ns, row_pad;
     int32_t early_dependents;  // signal dependents at the dispatch phase (small sends only)
     int32_t sched_cta;         // 1: CTA nb holds no tile and builds the chunk schedule
+    // Split form only: n_data data CTAs after the tile (and schedule) CTAs move
+    // the rows in units of unit_rows rows of one token (1, or k = the whole
+    // token); ready[q] is set (release) once tile q's slots are written.
+    int32_t n_data, unit_rows;
+    unsigned *ready;
 };
 
-template <int VPL>
+// The rows of one token (unit_rows of them from top-k position jj0), moved by
+// a data CTA of the split form: wait until the tile that owns the token has
+// published its slots, then bulk-store the staged x row to each slot.
+__device__ __forceinline__ bool split_data_unit(const FusedArgs &a, int64_t t, int jj0, unsigned char *stage,
+                                                uint64_t *bar, uint32_t parity, int lane) {
+    const int32_t row_bytes = a.H * 2;
+    const int64_t rows = (int64_t)a.T * a.k;
+    // tile q holds tokens [floor(q T / nb), floor((q + 1) T / nb)): the owner of t
+    const int q = (int)(((t + 1) * a.nb + a.T - 1) / a.T) - 1;
+    bool seen = false;
+    for (uint32_t polls = 0; polls <= kFusedMaxPolls; ++polls) {
+        if (ld_acquire_u32(a.ready + q) != 0u) {  // every lane acquires: its slot load is ordered after it
+            seen = true;
+            break;
+        }
+        __nanosleep(32);
+    }
+    if (!__all_sync(0xffffffffu, seen)) return false;
+    if (!mbar_wait_bounded(bar, parity, kFusedMaxPolls)) return false;
+    if (a.early_dependents) grid_launch_dependents();
+    if (lane < a.unit_rows) {
+        const int j = jj0 + lane;
+        const int sv = a.slot[t * a.k + j];
+        if (sv >= 0 && (int64_t)sv < rows) {
+            bulk_s2g(a.send + (int64_t)sv * row_bytes, stage, (uint32_t)row_bytes);
+            a.meta[sv] = (int32_t)(t * a.k + j);
+        }
+        bulk_commit();
+    }
+    return true;
+}
+
+template <int VPL, bool kSplit>
 __global__ void __launch_bounds__(kFusedThreads, 2) dispatch_fused_kernel(FusedArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int s_warp32[32];
@@ -148,8 +199,48 @@ __global__ void __launch_bounds__(kFusedThreads, 2) dispatch_fused_kernel(FusedA
     const int np = ntok * k;
     const int32_t row_bytes = a.H * 2;
 
+    if (kSplit && b >= a.nb + a.sched_cta) {
+        // Data CTA (split form): its first x row is fetched at once, while
+        // the tile CTAs compute the metadata; then, unit by unit, it waits for
+        // the owning tile's flag and stores the rows. Warp 0 does it all.
+        if (warp != 0) return;
+        const int64_t n_units = a.unit_rows == k ? (int64_t)a.T : (int64_t)a.T * k;
+        const int64_t j = b - a.nb - a.sched_cta;
+        if (lane == 0) {
+            mbar_init(&bar[0], 1);
+            fence_mbar_init();
+        }
+        __syncwarp();
+        int64_t cur = -1;  // token in the stage
+        uint32_t loads = 0;
+        bool good = true;
+        for (int64_t u = j; good && u < n_units; u += a.n_data) {
+            const int64_t t = a.unit_rows == k ? u : u / k;
+            const int jj0 = a.unit_rows == k ? 0 : (int)(u % k);
+            if (t != cur) {
+                if (cur >= 0) {
+                    if (lane < a.unit_rows) bulk_wait_read<0>();  // the stage's previous row is read out
+                    __syncwarp();
+                }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&bar[0], (uint32_t)row_bytes);
+                    bulk_g2s(stages, a.x + t * row_bytes, (uint32_t)row_bytes, &bar[0]);
+                }
+                ++loads;
+                cur = t;
+            }
+            good = split_data_unit(a, t, jj0, stages, &bar[0], (loads - 1) & 1u, lane);
+        }
+        if (!good) {
+            if (lane == 0) atomicOr(a.err, kErrFusedWait);
+            mbar_wait_bounded(&bar[0], (loads - 1) & 1u, kFusedMaxPolls);  // the last load lands before exit
+        }
+        if (lane < a.unit_rows) bulk_wait<0>();
+        return;
+    }
+
     // 0. start the tile's first x rows into shared memory
-    if (a.ns > 0 && threadIdx.x == 0) {
+    if (!kSplit && a.ns > 0 && threadIdx.x == 0) {
         for (int s = 0; s < a.ns; ++s) mbar_init(&bar[s], 1);
         fence_mbar_init();
         for (int s = 0; s < a.ns && s < ntok; ++s) {
@@ -255,6 +346,13 @@ __global__ void __launch_bounds__(kFusedThreads, 2) dispatch_fused_kernel(FusedA
             tile_s[p] = sv;
             a.slot[t0 * k + p] = sv;
         }
+        if (kSplit && !sched_only) {
+            // The CTA barrier orders every thread's slot stores before the
+            // release store (release is cumulative): a data CTA that acquires
+            // the flag sees the slots.
+            __syncthreads();
+            if (threadIdx.x == 0) st_release_u32(a.ready + b, 1u);
+        }
         const int32_t epr = E / a.R;
         if (b == 0) {
             for (int e = threadIdx.x; e <= E; e += blockDim.x) {
@@ -283,6 +381,7 @@ __global__ void __launch_bounds__(kFusedThreads, 2) dispatch_fused_kernel(FusedA
     // after this kernel may get ready now (it waits for this grid before it
     // touches memory); with more rows its waiting CTAs slowed this phase down.
     if (a.early_dependents) grid_launch_dependents();
+    if (kSplit) return;  // the data CTAs move the rows
     const int64_t rows = (int64_t)a.T * k;
     if (a.ns > 0) {
         if (warp != 0) return;
@@ -347,14 +446,71 @@ __global__ void __launch_bounds__(kFusedThreads, 2) dispatch_fused_kernel(FusedA
 
 using FusedKernel = void (*)(FusedArgs);
 
-FusedKernel pick_kernel(int32_t E) {
+template <bool kSplit>
+FusedKernel pick_kernel_t(int32_t E) {
     const int vpl = (E + 31) / 32;
-    if (vpl <= 1) return dispatch_fused_kernel<1>;
-    if (vpl <= 2) return dispatch_fused_kernel<2>;
-    if (vpl <= 4) return dispatch_fused_kernel<4>;
-    if (vpl <= 8) return dispatch_fused_kernel<8>;
-    if (vpl <= 16) return dispatch_fused_kernel<16>;
-    return dispatch_fused_kernel<32>;
+    if (vpl <= 1) return dispatch_fused_kernel<1, kSplit>;
+    if (vpl <= 2) return dispatch_fused_kernel<2, kSplit>;
+    if (vpl <= 4) return dispatch_fused_kernel<4, kSplit>;
+    if (vpl <= 8) return dispatch_fused_kernel<8, kSplit>;
+    if (vpl <= 16) return dispatch_fused_kernel<16, kSplit>;
+    return dispatch_fused_kernel<32, kSplit>;
+}
+
+FusedKernel pick_kernel(int32_t E, bool split) { return split ? pick_kernel_t<true>(E) : pick_kernel_t<false>(E); }
+
+// Lets a kernel use up to kFusedSmemLimit of dynamic shared memory (once per
+// device and kernel); false if the device refuses.
+bool allow_fused_smem(FusedKernel kern, int dev, int32_t E, bool split) {
+    static std::atomic<bool> attr_set[kMaxDevices_][2][6];  // zero-initialised: false
+    const int vpl = (E + 31) / 32;
+    const int vi = vpl <= 1 ? 0 : vpl <= 2 ? 1 : vpl <= 4 ? 2 : vpl <= 8 ? 3 : vpl <= 16 ? 4 : 5;
+    if (attr_set[dev][split][vi]) return true;
+    if (cudaFuncSetAttribute(reinterpret_cast<const void *>(kern), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kFusedSmemLimit) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    attr_set[dev][split][vi] = true;
+    return true;
+}
+
+// The split form (kernel decomposition with separate data CTAs): tiles of up
+// to 8 tokens (one per routing warp), the schedule CTA when there are several
+// tiles, and as many data CTAs as still fit on the GPU, each moving units of
+// one row (when every row can have its own CTA) or of a whole token. false if
+// the shape does not suit it (then the caller uses the other forms).
+bool plan_split(const ep_config &c, FusedPlan *p) {
+    if (c.T <= 0 || c.T > kSplitMaxT) return false;
+    const int32_t row_bytes = c.H * 2;
+    if (row_bytes < 1024 || row_bytes > 48 * 1024) return false;  // rows move as bulk copies
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices_) return false;
+    const FusedKernel kern = pick_kernel(c.E, true);
+    if (!allow_fused_smem(kern, dev, c.E, true)) return false;
+    const int nb = (int)((c.T + kFusedWarps - 1) / kFusedWarps);
+    if (nb > kMaxFusedCTAs) return false;
+    const int tb = (int)((c.T + nb - 1) / nb);
+    const int sched = nb > 1 ? 1 : 0;
+    const int row_pad = (int)align128((size_t)row_bytes);
+    const SmemLayout L = smem_layout(1, row_pad, tb, c.k, c.E, c.R, c.n_groups > 1);
+    if (L.bytes > kFusedSmemLimit) return false;
+    const int64_t cap = (int64_t)sm_count(dev) * max_blocks_per_sm(reinterpret_cast<const void *>(kern),
+                                                                     kFusedThreads, L.bytes);
+    const int64_t room = cap - nb - sched;
+    if (room < 1) return false;
+    const int64_t pairs = (int64_t)c.T * c.k;
+    const int unit_rows = pairs <= room ? 1 : c.k;
+    const int64_t n_units = unit_rows == 1 ? pairs : c.T;
+    p->nb = nb;
+    p->sched_cta = sched;
+    p->tb = tb;
+    p->ns = 1;
+    p->row_pad = row_pad;
+    p->smem = L.bytes;
+    p->n_data = (int)(n_units < room ? n_units : room);
+    p->unit_rows = unit_rows;
+    return true;
 }
 
 // Choose the tiling: as many CTAs as fit on the GPU at once (two per SM when
@@ -365,18 +521,8 @@ bool plan_fused(const ep_config &c, FusedPlan *p) {
     if (c.T <= 0) return false;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices_) return false;
-    const FusedKernel kern = pick_kernel(c.E);
-    static std::atomic<bool> attr_set[kMaxDevices_][6];  // zero-initialised: false
-    const int vi = ((c.E + 31) / 32 <= 1) ? 0 : ((c.E + 31) / 32 <= 2) ? 1 : ((c.E + 31) / 32 <= 4) ? 2
-                 : ((c.E + 31) / 32 <= 8) ? 3 : ((c.E + 31) / 32 <= 16) ? 4 : 5;
-    if (!attr_set[dev][vi]) {
-        if (cudaFuncSetAttribute(reinterpret_cast<const void *>(kern), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kFusedSmemLimit) != cudaSuccess) {
-            cudaGetLastError();
-            return false;
-        }
-        attr_set[dev][vi] = true;
-    }
+    const FusedKernel kern = pick_kernel(c.E, false);
+    if (!allow_fused_smem(kern, dev, c.E, false)) return false;
     const int32_t row_bytes = c.H * 2;
     const bool bulk = c.k % 4 == 0 && row_bytes >= 1024 && row_bytes <= 48 * 1024;
     const int sms = sm_count(dev);
@@ -450,7 +596,9 @@ size_t fused_counter_offset(const ep_config &c) {
 size_t fused_tables_bytes(const ep_config &c) {
     const int64_t nb = c.T < kMaxFusedCTAs ? c.T : kMaxFusedCTAs;
     const size_t tables = 2 * sizeof(int32_t) * (size_t)nb * (size_t)c.E;
-    return ((tables + sizeof(int32_t) * (size_t)c.E + 255) & ~(size_t)255) + 256;
+    // then the two barrier words and one ready flag per tile (split form)
+    return ((tables + sizeof(int32_t) * (size_t)c.E + 255) & ~(size_t)255) +
+           ((sizeof(unsigned) * (2 + (size_t)kMaxFusedCTAs) + 255) & ~(size_t)255);
 }
 
 size_t fused_workspace_bytes(const ep_config &c) {
@@ -459,7 +607,7 @@ size_t fused_workspace_bytes(const ep_config &c) {
 
 int fused_call_kernels(const ep_config &c) {
     FusedPlan p;
-    if (!plan_fused(c, &p)) return 2 + layout_kernel_count(c);  // route, layout, dispatch
+    if (!plan_split(c, &p) && !plan_fused(c, &p)) return 2 + layout_kernel_count(c);  // route, layout, dispatch
     return 1;
 }
 
@@ -469,7 +617,8 @@ cudaError_t launch_dispatch_fused(const ep_config &c, int32_t W, const float *lo
                                   int32_t *n_chunks, int32_t *worker_begin, ep_bf16 *send, int32_t *meta,
                                   void *workspace, cudaStream_t s) {
     FusedPlan p;
-    if (!plan_fused(c, &p)) {
+    const bool split = plan_split(c, &p);
+    if (!split && !plan_fused(c, &p)) {
         // Three kernels; the route kernel zeroes the layout's barrier words (and
         // the dispatch counter unless the layout does, below), so no memset
         // sits between the kernels.
@@ -539,15 +688,21 @@ cudaError_t launch_dispatch_fused(const ep_config &c, int32_t W, const float *lo
     a.tb = p.tb;
     a.ns = p.ns;
     a.row_pad = p.row_pad;
+    a.n_data = p.n_data;
+    a.unit_rows = p.unit_rows;
+    a.ready = a.sync + 2;
     // measured: T = 1..64 (<= 7.3 MB of send rows) gain 1-2 us, T = 256 even, T = 512 (59 MB) loses 1.8 us
     a.early_dependents = (int64_t)c.T * c.k * c.H * 2 <= (int64_t)16 << 20 ? 1 : 0;
-    if (p.nb + p.sched_cta > 1) {  // a single CTA uses no grid barrier (and the memset costs ~0.5 us at T = 1)
+    if (split) {  // barrier words and the tiles' ready flags
+        e = cudaMemsetAsync(a.sync, 0, (2 + (size_t)p.nb) * sizeof(unsigned), s);
+        if (e != cudaSuccess) return e;
+    } else if (p.nb + p.sched_cta > 1) {  // a single CTA uses no grid barrier (and the memset costs ~0.5 us at T = 1)
         e = cudaMemsetAsync(a.sync, 0, 2 * sizeof(unsigned), s);
         if (e != cudaSuccess) return e;
     }
     void *args[] = {&a};
-    return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(pick_kernel(c.E)),
-                                       dim3((unsigned)(p.nb + p.sched_cta)),
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(pick_kernel(c.E, split)),
+                                       dim3((unsigned)(p.nb + p.sched_cta + p.n_data)),
                                        dim3(kFusedThreads), args, p.smem, s);
 }
 
