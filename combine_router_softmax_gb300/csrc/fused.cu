@@ -26,7 +26,7 @@
 //      bulk-store each row to its k send rows. When the send buffer is small
 //      (<= 16 MB) every CTA signals programmatic dependents here, so that a
 //      combine launched after it can start its prologue early.
-// Up to 64 tokens the split form of the same kernel is used instead (the
+// Up to 160 tokens the split form of the same kernel is used instead (the
 // article's metadata/data decomposition): the tile CTAs (up to 8 tokens each,
 // one per routing warp) stop after F, releasing a per-tile ready flag once
 // their slots are written, and separate data CTAs -- as many as still fit on
@@ -34,8 +34,9 @@
 // fetch their x row at once, acquire-poll the owning tile's flag (bounded)
 // and bulk-store the rows. Up to 8 tokens the metadata is then one CTA with no
 // grid barrier, and the rows leave from many SMs instead of one (measured per
-// layer: T = 8 21.6 -> 19.5 us, T = 16 22.7 -> 21.0, T = 1 -0.5, T = 64 -0.3; at
-// decode +0.3 and at T = 512 +4 us, so the split form stops at T = 64).
+// layer: T = 8 21.6 -> 19.5 us, T = 16 22.7 -> 21.0, T = 96 25.1 -> 23.0, T = 160
+// 28.6 -> 27.3, T = 1 -0.5, T = 64 -0.3; at T = 192 and 256 within +-0.2 us, at
+// T = 512 +4 us, so the split form stops at T = 160).
 // Every result equals what ep_route, ep_layout and ep_dispatch write.
 #include "block_common.cuh"
 #include "flag_ops.cuh"
@@ -51,7 +52,7 @@ constexpr int kMaxFusedStages = 8;
 constexpr int kMaxFusedCTAs = 1024;
 constexpr uint32_t kFusedMaxPolls = 1u << 22;
 constexpr size_t kFusedSmemLimit = 200 * 1024;
-constexpr int kSplitMaxT = 64;  // split form up to this many tokens
+constexpr int kSplitMaxT = 160;  // split form up to this many tokens
 
 static __device__ int32_t g_fused_error;
 

@@ -250,7 +250,7 @@ ep_status ep_dispatch(const ep_config *cfg, const ep_bf16 *x, const int32_t *slo
  * tile of tokens to route, rank and dispatch; the CTAs exchange the per-expert
  * counts through global memory at two bounded grid barriers (in the workspace)
  * and each CTA's x rows are fetched with bulk copies while that metadata is
- * being computed. Up to 64 tokens the rows are moved by separate data CTAs
+ * being computed. Up to 160 tokens the rows are moved by separate data CTAs
  * instead, each waiting (bounded) on a ready flag that the tile holding its
  * token releases once its slots are written. It pays off at small T (decode
  * batches), where the phases

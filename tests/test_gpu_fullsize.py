@@ -82,6 +82,7 @@ GRAPH = [
     ep_synth.get_workload("sweep-zipf-T8"),
     ep_synth.get_workload("sweep-uniform-T64"),
     ep_synth.get_workload("sweep-zipf-T64"),
+    ep_synth.CONFIGS["decode"].with_(name="decode-T160", T=160),  # the largest batch of the split form
     ep_synth.CONFIGS["decode"],
     ep_synth.get_workload("sweep-zipf-T512"),
     ep_synth.CONFIGS["prefill"],

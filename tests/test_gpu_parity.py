@@ -413,13 +413,15 @@ FUSED = [
                       num_workers=152),
     ep_synth.Workload("pods-T4096", T=4096, H=1024, E=256, R=64, k=8, ranks_per_node=4, ranks_per_pod=16,
                       self_rank=5, num_workers=152),
-    # the split form (T <= 64): one row per data CTA, or one token per data CTA when rows outnumber them
+    # the split form (T <= 160): one row per data CTA, or one token per data CTA when rows outnumber them
     ep_synth.Workload("split-k6", T=40, H=1024, E=64, R=8, k=6, num_workers=20),
     ep_synth.Workload("split-k32-E1024", T=50, H=512, E=1024, R=32, k=32, n_groups=32, topk_groups=4,
                       num_workers=152),
     ep_synth.Workload("split-k12-groups", T=57, H=2048, E=96, R=6, k=12, n_groups=6, topk_groups=2,
                       ranks_per_node=2, self_rank=5, num_workers=33),
     ep_synth.CONFIGS["prefill"].with_(name="split-T63-plain", T=63, renormalize=0),
+    ep_synth.CONFIGS["decode"].with_(name="split-T160", T=160),
+    ep_synth.CONFIGS["decode"].with_(name="fused-T161", T=161),
 ] + [w for w in ep_synth.sweep_workloads() if w.T in (1, 8, 64, 512, 4096, 32768)]
 
 
