@@ -86,8 +86,10 @@ cudaError_t launch_layout(const ep_config &c, int32_t W, const int32_t *idx, int
                           cudaStream_t s, bool sync_zeroed = false, bool defer_schedule = false,
                           bool *deferred = nullptr, bool after_route = false, unsigned *zero_ctr = nullptr);
 
-// Runs two CTAs into a grid barrier that expects three; *gave_up counts the
-// CTAs that stopped waiting after max_polls polls (2 when the bound works).
+// Runs two CTAs into a grid barrier that expects three (a third arrives only
+// after one gave up) and one CTA into a wait on a flag nothing sets; *gave_up
+// counts the CTAs that stopped waiting after max_polls polls (3 when the
+// bounds work), or is -1 if the late arrival missed the failure.
 cudaError_t launch_bounded_wait_check(uint32_t max_polls, int32_t *gave_up, cudaStream_t s);
 
 // Kernels launch_layout enqueues for c on the current device (1 fused, or 3).

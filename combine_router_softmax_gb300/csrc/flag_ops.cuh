@@ -1,5 +1,6 @@
-// flag_ops.cuh -- memory operations of the Data-as-Flag kernels (sp.cu, tff.cu):
-// flags stored with release and loaded with acquire at GPU scope, and
+// flag_ops.cuh -- memory operations of the Data-as-Flag kernels (sp.cu, tff.cu)
+// and of the split small-batch dispatch (fused.cu): flags stored with release
+// and loaded with acquire at GPU scope, a bounded warp-wide wait on a flag, and
 // coherent 16-byte loads of data another CTA may still be writing.
 #pragma once
 
@@ -18,6 +19,22 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p) {
     unsigned v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
+}
+
+// Waits, by the whole warp, until *flag is non-zero: every lane polls with an
+// acquire load (so each lane's later loads are ordered after the flag's
+// release), sleeping briefly between polls. Bounded: false after max_polls
+// polls without seeing the flag set.
+__device__ __forceinline__ bool warp_wait_flag(const unsigned *flag, uint32_t max_polls) {
+    bool seen = false;
+    for (uint32_t polls = 0; polls <= max_polls; ++polls) {
+        if (ld_acquire_u32(flag) != 0u) {
+            seen = true;
+            break;
+        }
+        __nanosleep(32);
+    }
+    return __all_sync(0xffffffffu, seen);
 }
 
 // Relaxed (coherent, GPU-scope) 16-byte load: sees a concurrent writer's data.

@@ -141,15 +141,7 @@ __device__ __forceinline__ bool split_data_unit(const FusedArgs &a, int64_t t, i
     const int64_t rows = (int64_t)a.T * a.k;
     // tile q holds tokens [floor(q T / nb), floor((q + 1) T / nb)): the owner of t
     const int q = (int)(((t + 1) * a.nb + a.T - 1) / a.T) - 1;
-    bool seen = false;
-    for (uint32_t polls = 0; polls <= kFusedMaxPolls; ++polls) {
-        if (ld_acquire_u32(a.ready + q) != 0u) {  // every lane acquires: its slot load is ordered after it
-            seen = true;
-            break;
-        }
-        __nanosleep(32);
-    }
-    if (!__all_sync(0xffffffffu, seen)) return false;
+    if (!warp_wait_flag(a.ready + q, kFusedMaxPolls)) return false;  // each lane's slot load is ordered after it
     if (!mbar_wait_bounded(bar, parity, kFusedMaxPolls)) return false;
     if (a.early_dependents) grid_launch_dependents();
     if (lane < a.unit_rows) {

@@ -35,6 +35,7 @@
 #include <climits>
 
 #include "block_common.cuh"
+#include "flag_ops.cuh"
 
 namespace ep {
 
@@ -461,15 +462,22 @@ cudaError_t launch_layout(const ep_config &c, int32_t W, const int32_t *idx, int
 // last arrival would let a CTA go on with a result missing. CTAs 0 and 1 must
 // give up after max_polls polls and count themselves in *gave_up, and CTA 2
 // must see the failure too; a second kernel sets *gave_up = -1 if it did not.
+// CTA 3 runs the split dispatch's warp-wide wait on a ready flag that nothing
+// sets and must give up after max_polls polls as well.
 // ---------------------------------------------------------------------------
 namespace ep {
 namespace {
 
-static __device__ unsigned g_check_arrivals;
+static __device__ unsigned g_check_arrivals[2];  // barrier arrivals, a flag nothing sets
 static __device__ int32_t g_check_late_passed;  // 1: the late CTA passed the barrier
 
 __global__ void bounded_wait_check_kernel(unsigned *arrivals, int32_t *late_passed, unsigned max_polls,
                                           int32_t *gave_up) {
+    if (blockIdx.x == 3) {
+        // the split dispatch's wait on a tile's ready flag, on a flag nothing sets
+        if (threadIdx.x < 32 && !warp_wait_flag(arrivals + 1, max_polls) && threadIdx.x == 0) atomicAdd(gave_up, 1);
+        return;
+    }
     if (blockIdx.x < 2) {
         if (!grid_barrier(arrivals, 3u, max_polls) && threadIdx.x == 0) atomicAdd(gave_up, 1);
         return;
@@ -492,10 +500,10 @@ cudaError_t launch_bounded_wait_check(uint32_t max_polls, int32_t *gave_up, cuda
     cudaError_t e = cudaGetSymbolAddress(&arrivals, g_check_arrivals);
     if (e != cudaSuccess) return e;
     if ((e = cudaGetSymbolAddress(&late, g_check_late_passed)) != cudaSuccess) return e;
-    if ((e = cudaMemsetAsync(arrivals, 0, sizeof(unsigned), s)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(arrivals, 0, 2 * sizeof(unsigned), s)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(late, 0, sizeof(int32_t), s)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(gave_up, 0, sizeof(int32_t), s)) != cudaSuccess) return e;
-    bounded_wait_check_kernel<<<3, 32, 0, s>>>(static_cast<unsigned *>(arrivals), static_cast<int32_t *>(late),
+    bounded_wait_check_kernel<<<4, 32, 0, s>>>(static_cast<unsigned *>(arrivals), static_cast<int32_t *>(late),
                                                max_polls, gave_up);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     bounded_wait_verdict_kernel<<<1, 1, 0, s>>>(static_cast<const int32_t *>(late), gave_up);

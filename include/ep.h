@@ -123,7 +123,9 @@ ep_status ep_device_error(int32_t *flags);
  * third CTA makes the last arrival only after one of them has given up; it
  * must see the failure as well (in ep_layout that keeps the CTA that writes
  * the chunk count from overwriting *n_chunks = -1), else *gave_up is set to
- * -1. Expected result: 2. The kernels return normally; nothing faults or
+ * -1. A fourth CTA waits, as ep_dispatch_fused's data CTAs do, on a ready
+ * flag that nothing sets, and must give up after max_polls polls and count
+ * itself. Expected result: 3. The kernels return normally; nothing faults or
  * hangs. */
 ep_status ep_check_bounded_wait(int32_t max_polls, int32_t *gave_up, cudaStream_t stream);
 
