@@ -71,9 +71,46 @@ __device__ __forceinline__ float warp_sort_desc(float s, int lane) {
 
 // Group limiting: clears the elig bits of experts outside the topk_groups
 // groups with the largest per-group maximum logit (ties to the lower group).
+//
+// When a group is a power-of-two run of at most 32 experts (every group then
+// lies in gsize consecutive lanes of one register), the group maxima come from
+// shuffles inside each run and each group's rank is counted against all the
+// others (lane g < n_groups holds group g); otherwise through shared memory
+// with topk_groups rounds of arg-max. Both keep the same groups.
 template <int VPL>
 __device__ __forceinline__ uint32_t group_limit(const float (&v)[VPL], uint32_t elig, int32_t E, int32_t n_groups,
                                                 int32_t topk_groups, int lane, float *s_glog) {
+    const int gsize = E / n_groups;
+    if (gsize <= 32 && (32 % gsize) == 0) {
+        float gm[VPL];
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            float m = lane + 32 * i < E ? v[i] : -INFINITY;
+            for (int off = gsize >> 1; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+            gm[i] = m;
+        }
+        // lane g < n_groups fetches group g's maximum: register g gsize / 32, lane g gsize % 32
+        const int src = (lane * gsize) & 31, reg = (lane * gsize) >> 5;
+        float gs = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            const float t = __shfl_sync(0xffffffffu, gm[i], src);
+            if (i == reg) gs = t;
+        }
+        const bool mine = lane < n_groups;
+        int rank = 0;  // groups ordered before mine: larger maximum, or equal and lower index
+        for (int g = 0; g < n_groups; ++g) {
+            const float o = __shfl_sync(0xffffffffu, gs, g);
+            rank += (o > gs || (o == gs && g < lane)) ? 1 : 0;
+        }
+        const uint32_t kept = __ballot_sync(0xffffffffu, mine && rank < topk_groups);
+#pragma unroll
+        for (int i = 0; i < VPL; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E && !((kept >> (e / gsize)) & 1u)) elig &= ~(1u << i);
+        }
+        return elig;
+    }
     float *sl = s_glog;
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
@@ -81,7 +118,6 @@ __device__ __forceinline__ uint32_t group_limit(const float (&v)[VPL], uint32_t 
         if (e < E) sl[e] = v[i];
     }
     __syncwarp();
-    const int gsize = E / n_groups;
     float gs = -INFINITY;
     bool avail = lane < n_groups;
     if (avail) {

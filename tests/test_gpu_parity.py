@@ -217,6 +217,16 @@ EDGE = [
     ("pod-ge-R", ep_synth.CONFIGS["decode"].with_(T=200, ranks_per_node=4, ranks_per_pod=128, self_rank=10), None),
     ("pods-E1024", ep_synth.Workload("maxp", T=300, H=64, E=1024, R=1024, k=32, ranks_per_node=8, ranks_per_pod=64,
                                      self_rank=1000, num_workers=152), None),
+    # group sizes around the shuffle path's limits: 24 and 64 experts per group (shared-memory path), one and two
+    # experts per group (shuffle path)
+    ("groups-of-24", ep_synth.Workload("g24", T=200, H=64, E=96, R=4, k=6, n_groups=4, topk_groups=2,
+                                       num_workers=40), None),
+    ("groups-of-64", ep_synth.Workload("g64", T=200, H=64, E=512, R=8, k=8, n_groups=8, topk_groups=3,
+                                       num_workers=40), None),
+    ("groups-of-1", ep_synth.Workload("g1", T=200, H=64, E=32, R=4, k=8, n_groups=32, topk_groups=8,
+                                      num_workers=40), None),
+    ("groups-of-2-ties", ep_synth.Workload("g2", T=300, H=64, E=64, R=4, k=4, n_groups=32, topk_groups=3,
+                                           num_workers=40), "ties"),
 ]
 
 
