@@ -379,6 +379,48 @@ def capture_callable_graph(fn, device):
     return g
 
 
+def graph_call_ms(buf, device, fused: bool, flush_l2, K: int):
+    """Per-call times of the step inside a CUDA graph: the step's graph with an
+    event-record node before each call and after the last (events recorded as
+    graph nodes), replayed K times after 3 warm-up replays, L2 flushed before
+    each replay and the events read after it. Returns {call: [ms, ...]}, or
+    None where this PyTorch cannot record events as graph nodes."""
+    import torch
+
+    cap = torch.cuda.Stream(device)
+    cap.wait_stream(torch.cuda.current_stream(device))
+    calls = step_calls(buf.bind(cap), fused)
+    try:
+        evs = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(len(calls) + 1)]
+    except TypeError:
+        return None
+    with torch.cuda.stream(cap):
+        for _ in range(2):
+            for _, fn in calls:
+                fn()
+    cap.synchronize()
+    g = torch.cuda.CUDAGraph()
+    try:
+        with torch.cuda.graph(g, stream=cap):
+            for j, (_, fn) in enumerate(calls):
+                evs[j].record(cap)
+                fn()
+            evs[-1].record(cap)
+    except RuntimeError:
+        return None
+    torch.cuda.synchronize()
+    per = {n: [] for n, _ in calls}
+    for i in range(K + 3):
+        flush_l2()
+        g.replay()
+        torch.cuda.synchronize()
+        if i >= 3:
+            for j, (n, _) in enumerate(calls):
+                per[n].append(evs[j].elapsed_time(evs[j + 1]))
+    del g
+    return per
+
+
 def step_calls(bound, fused: bool):
     """The C-ABI calls of one step, in order, with the names their bytes are booked under."""
     if fused:
@@ -892,14 +934,24 @@ def measure_workload(ep, w0, args, rank: int, world: int, device, flush_l2, K: i
 
     launches_per_step = ep.ep_step_kernel_count(cfg, fused=fused)
     kb = {n: call_bytes(w, n) for n, _ in calls}
-    kern_ms = {n: sum(v) / len(v) for n, v in per.items()}
+    eager_ms = {n: sum(v) / len(v) for n, v in per.items()}
+    # per-call times inside the step's graph (as the step itself is timed), the
+    # slowest rank's mean; the calls launched one by one as a fallback
+    gper = graph_call_ms(buf, device, fused, flush_l2, K) if graph is not None else None
+    if gper is not None:
+        gmean = reduce_max_many({n: sum(v) / len(v) for n, v in gper.items()}, world, device)
+        kern_ms, call_timing = gmean, "graph"
+    else:
+        kern_ms, call_timing = eager_ms, "eager"
+    eager_ms = reduce_max_many(eager_ms, world, device)
     dom = max(kern_ms, key=kern_ms.get)
     peak, peak_kind = measured_peak_gbs()
     names = [n for n, _ in calls]
     multi = "dispatch_fused" if "dispatch_fused" in names else "layout"
     call_kernels = {n: 1 for n in names}
     call_kernels[multi] = launches_per_step - (len(names) - 1)
-    by_call = {n: {"us": round(kern_ms[n] * 1e3, 2), "kernels": call_kernels[n],
+    by_call = {n: {"us": round(kern_ms[n] * 1e3, 2), "us_eager": round(eager_ms[n] * 1e3, 2),
+                   "kernels": call_kernels[n],
                    "algorithmic_bytes": kb[n],
                    "achieved": round(kb[n] / (kern_ms[n] * 1e-3) / 1e9, 1),
                    "frac": round(kb[n] / (kern_ms[n] * 1e-3) / 1e9 / peak, 4),
@@ -920,6 +972,7 @@ def measure_workload(ep, w0, args, rank: int, world: int, device, flush_l2, K: i
         "hbm_fraction": round(value / world / peak, 4),
         "hbm_fraction_of_spec": round(value / world / SPEC_HBM_GBS, 4),
         "kernel_us": {n: round(v * 1e3, 2) for n, v in kern_ms.items()},
+        "kernel_us_eager": {n: round(v * 1e3, 2) for n, v in eager_ms.items()},
         "roofline": {
             "bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4), "frac_of_spec": round(achieved / SPEC_HBM_GBS, 4),
@@ -928,6 +981,9 @@ def measure_workload(ep, w0, args, rank: int, world: int, device, flush_l2, K: i
             "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
             if peak_kind == "measured" else "fallback 6.8 TB/s",
             "spec_peak": SPEC_HBM_GBS,
+            "by_call_timing": ("each call between event-record nodes of the step's CUDA graph (replayed after an "
+                               "L2 flush)" if call_timing == "graph" else
+                               "each call between events, the calls launched one by one after an L2 flush"),
             "by_call": by_call,
         },
         "e2e": {"value": round(pipe_val, 2), "unit": "GB/s",

@@ -1,6 +1,7 @@
 // block_common.cuh -- CTA-wide building blocks shared by the layout kernels
 // and the fused dispatch: CTA scans, the per-warp ranking of (token, expert)
-// pairs, the chunk schedule and a bounded grid barrier.
+// pairs, the chunk schedule, a bounded grid barrier and a count table that
+// CTAs exchange without one.
 #pragma once
 
 #include <climits>
@@ -509,6 +510,110 @@ __device__ bool grid_barrier(unsigned *arrivals, unsigned expected, unsigned max
     }
     __syncthreads();
     return s_ok != 0;
+}
+
+// ---------------------------------------------------------------------------
+// Count table exchanged without a grid barrier
+// ---------------------------------------------------------------------------
+// CTA b of a cooperative launch publishes its per-expert counts as row b of a
+// [CTA][E] table of 32-bit words in global memory, each entry marked by its top
+// bit (kCountValid), and every CTA reads the whole table by polling each entry
+// until it carries the mark. A reader thus starts on the rows already there
+// while later CTAs still rank, and needs no arrival counter: one round of
+// polls replaces the barrier's arrive-and-poll plus the table read after it.
+// The table must be zero before the launch. Entries are self-contained (one
+// 32-bit word each), so relaxed loads suffice; nothing else crosses CTAs.
+//
+// Bounded: a reader that has polled max_polls times swaps kCountPoison into
+// every entry it still misses (compare-and-swap from zero). The owner publishes
+// with a compare-and-swap from zero too, so a poisoned entry never becomes
+// valid; every CTA needs every entry, so all of them fail and none goes on
+// with a count missing (a CTA that fails writes *n_chunks = -1 and no chunk
+// count can overwrite it). The owner learns from its own swaps that it was
+// late and fails as well.
+constexpr unsigned kCountValid = 0x80000000u;
+constexpr unsigned kCountPoison = 0x40000000u;
+
+__device__ __forceinline__ unsigned ld_relaxed_gpu(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+// Publishes row `row` from own[0, E) (own[e] < 2^30). Each thread swaps at
+// most four entries (E <= 4 blockDim.x); it returns the OR of the values its
+// swaps found, non-zero when an entry was not zero any more (poisoned by a
+// reader that gave up). Read the result late: the swaps complete meanwhile.
+struct TablePublish {
+    unsigned old[4];
+    __device__ __forceinline__ bool late() const { return (old[0] | old[1] | old[2] | old[3]) != 0u; }
+};
+__device__ __forceinline__ TablePublish table_publish(unsigned *row, const int32_t *own, int32_t E) {
+    TablePublish r;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int e = (int)threadIdx.x + i * (int)blockDim.x;
+        r.old[i] = e < E ? atomicCAS(row + e, 0u, kCountValid | (unsigned)own[e]) : 0u;
+    }
+    return r;
+}
+
+// Sums column e of the table over rows q = sub, sub + step, ... < nb (tot)
+// and over those rows below b (pre), polling every entry until it is valid,
+// with up to NB loads in flight; row `skip` is left out (the caller's own,
+// which it holds already: -1 for none). False if it gave up after max_polls
+// rounds of polls (poisoning what it still missed) or met a poisoned entry.
+template <int NB = 32>
+__device__ __forceinline__ bool table_column_sums(unsigned *tab, int32_t E, int e, int sub, int step, int nb,
+                                                  int b, int skip, uint32_t max_polls, int &tot, int &pre) {
+    tot = 0;
+    pre = 0;
+    for (int q0 = sub; q0 < nb; q0 += NB * step) {
+        unsigned cv[NB];
+#pragma unroll
+        for (int u = 0; u < NB; ++u) {
+            const int q = q0 + u * step;
+            cv[u] = q < nb && q != skip ? ld_relaxed_gpu(tab + (int64_t)q * E + e) : kCountValid;
+        }
+        for (uint32_t polls = 0;; ++polls) {
+            bool all = true, poisoned = false;
+#pragma unroll
+            for (int u = 0; u < NB; ++u) {
+                all = all && (cv[u] & kCountValid) != 0u;
+                poisoned = poisoned || cv[u] == kCountPoison;
+            }
+            if (all) break;
+            if (poisoned) return false;
+            if (polls >= max_polls) {
+#pragma unroll
+                for (int u = 0; u < NB; ++u) {
+                    const int q = q0 + u * step;
+                    if ((cv[u] & kCountValid) == 0u) {
+                        const unsigned prev = atomicCAS(tab + (int64_t)q * E + e, 0u, kCountPoison);
+                        cv[u] = prev == 0u ? kCountPoison : prev;
+                    }
+                }
+                bool now = true;
+#pragma unroll
+                for (int u = 0; u < NB; ++u) now = now && (cv[u] & kCountValid) != 0u;
+                if (!now) return false;
+                break;  // the missing entries arrived just in time
+            }
+            if (polls > 64) __nanosleep(32);
+#pragma unroll
+            for (int u = 0; u < NB; ++u) {
+                const int q = q0 + u * step;
+                if ((cv[u] & kCountValid) == 0u) cv[u] = ld_relaxed_gpu(tab + (int64_t)q * E + e);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < NB; ++u) {
+            const int c = (int)(cv[u] & ~kCountValid);  // 0 for the padding past nb and row skip
+            tot += c;
+            pre += q0 + u * step < b ? c : 0;
+        }
+    }
+    return true;
 }
 
 }  // namespace

@@ -38,12 +38,12 @@ constexpr int kMaxGroups = 32;
 
 inline int64_t layout_blocks(int64_t T) { return (T + kLayoutTokens - 1) / kLayoutTokens; }
 
-// Workspace carve-up for ep_layout (offsets 256-byte aligned). The fused path
-// uses [CTA][E] counts at block_counts_off and two sync words at sync_off; the
-// fallback path uses [E][ceil(T/256)] counts at block_counts_off.
+// Workspace carve-up for ep_layout. The single-kernel layout uses a [CTA][E]
+// count table of table_words 32-bit words at block_counts_off, which must be
+// zero when it starts; the fallback path uses [E][ceil(T/256)] counts there.
 struct LayoutWorkspace {
     size_t block_counts_off;
-    size_t sync_off;
+    size_t table_words;
     size_t bytes;
 };
 LayoutWorkspace layout_workspace(const ep_config &c);
@@ -63,7 +63,8 @@ int current_device_sm_count();
 int max_blocks_per_sm(const void *fn, int threads, size_t smem);
 
 // za / zb: optional words (na / nb of them) the route kernel sets to zero for
-// kernels that follow it in the same call sequence.
+// kernels that follow it in the same call sequence (za spread over all its
+// CTAs, zb by its first CTA: nb <= 256).
 // zc: optional int32 word the route kernel also sets to zero.
 cudaError_t launch_route(const ep_config &c, const float *logits, int32_t *idx, float *w, cudaStream_t s,
                          unsigned *za = nullptr, int na = 0, unsigned *zb = nullptr, int nb = 0,
@@ -72,7 +73,9 @@ cudaError_t launch_route(const ep_config &c, const float *logits, int32_t *idx, 
 // Whether every CTA of the route kernel for c is resident at once on the current device.
 bool route_one_wave(const ep_config &c);
 
-// sync_zeroed: the caller already zeroed the workspace's sync words (skip the memset).
+// table_zeroed: the caller already zeroed the single-kernel layout's count
+// table (layout_workspace(c).table_words words at the workspace's start), so
+// no memset is enqueued.
 // defer_schedule: when the layout runs as the single cooperative kernel, leave
 // the chunk schedule to the caller (*deferred = true; chunks, n_chunks and
 // worker_begin are then not written, except n_chunks = -1 on failure).
@@ -83,13 +86,15 @@ bool route_one_wave(const ep_config &c);
 cudaError_t launch_layout(const ep_config &c, int32_t W, const int32_t *idx, int32_t *expert_count,
                           int32_t *expert_offset, int32_t *rank_count, int32_t *rank_offset, int32_t *slot,
                           ep_chunk *chunks, int32_t *n_chunks, int32_t *worker_begin, void *workspace,
-                          cudaStream_t s, bool sync_zeroed = false, bool defer_schedule = false,
+                          cudaStream_t s, bool table_zeroed = false, bool defer_schedule = false,
                           bool *deferred = nullptr, bool after_route = false, unsigned *zero_ctr = nullptr);
 
 // Runs two CTAs into a grid barrier that expects three (a third arrives only
-// after one gave up) and one CTA into a wait on a flag nothing sets; *gave_up
-// counts the CTAs that stopped waiting after max_polls polls (3 when the
-// bounds work), or is -1 if the late arrival missed the failure.
+// after one gave up), one CTA into a wait on a flag nothing sets, and two
+// through a count-table exchange whose second row is published only after the
+// reader gave up; *gave_up counts the CTAs that stopped waiting after
+// max_polls polls or learnt they came too late (5 when the bounds work), or is
+// -1 if a late CTA missed the failure.
 cudaError_t launch_bounded_wait_check(uint32_t max_polls, int32_t *gave_up, cudaStream_t s);
 
 // Kernels launch_layout enqueues for c on the current device (1 fused, or 3).

@@ -612,11 +612,11 @@ cudaError_t launch_dispatch_fused(const ep_config &c, int32_t W, const float *lo
     FusedPlan p;
     const bool split = plan_split(c, &p);
     if (!split && !plan_fused(c, &p)) {
-        // Three kernels; the route kernel zeroes the layout's barrier words (and
-        // the dispatch counter unless the layout does, below), so no memset
-        // sits between the kernels.
+        // Three kernels; the route kernel zeroes the single-kernel layout's
+        // count table (and the dispatch counter unless the layout does, below),
+        // so no memset sits between the kernels.
         char *ws = static_cast<char *>(workspace);
-        unsigned *lsync = reinterpret_cast<unsigned *>(ws + layout_workspace(c).sync_off);
+        unsigned *table = reinterpret_cast<unsigned *>(ws + layout_workspace(c).block_counts_off);
         unsigned *ctr = reinterpret_cast<unsigned *>(ws + fused_counter_offset(c));
         // When the bulk dispatch follows the single-kernel layout, an extra CTA of
         // the dispatch builds the chunk schedule, so the layout does not hold the
@@ -631,8 +631,9 @@ cudaError_t launch_dispatch_fused(const ep_config &c, int32_t W, const float *lo
         // the later ones (T = 32768: +4.6 us), so there the layout waits.
         const bool single = layout_kernel_count(c) == 1;
         const bool after_route = single && route_one_wave(c);
-        cudaError_t e = launch_route(c, logits, topk_idx, topk_w, s, lsync, 2, single ? nullptr : ctr, single ? 0 : 1,
-                                     defer ? n_chunks : nullptr);
+        const int table_words = single ? (int)layout_workspace(c).table_words : 0;
+        cudaError_t e = launch_route(c, logits, topk_idx, topk_w, s, table, table_words, single ? nullptr : ctr,
+                                     single ? 0 : 1, defer ? n_chunks : nullptr);
         if (e != cudaSuccess) return e;
         bool deferred = false;
         e = launch_layout(c, W, topk_idx, expert_count, expert_offset, rank_count, rank_offset, slot, chunks,

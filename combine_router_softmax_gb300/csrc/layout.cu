@@ -15,11 +15,12 @@
 //    deterministic.
 //
 //  * fused path (one cooperative launch, all CTAs co-resident): each CTA
-//    publishes its per-expert counts, then meets the others at a bounded grid
-//    barrier (an arrival counter polled with acquire loads, no SyncAll-style
-//    second kernel). Every CTA then reads the whole [CTA][expert] count table
-//    and computes, redundantly and in parallel, the expert offsets and its
-//    own prefix inside each expert's segment, and writes its final slots.
+//    publishes its per-expert counts as one row of a [CTA][expert] table,
+//    every entry marked valid, and reads the whole table by polling each
+//    entry until it is marked (bounded; no grid barrier, no SyncAll-style
+//    second kernel: see block_common.cuh). Every CTA computes, redundantly and
+//    in parallel, the expert offsets and its own prefix inside each expert's
+//    segment, and writes its final slots.
 //    CTA 0 writes the counts/offsets and the last CTA the chunk schedule,
 //    unless the caller defers the schedule to the dispatch kernel that
 //    follows (its extra CTA builds it while the other CTAs copy rows).
@@ -93,18 +94,22 @@ LayoutWorkspace layout_workspace(const ep_config &c) {
     w.block_counts_off = 0;
     const LayoutTiling t = fused_tiling(c.T, c.E, c.R, c.k);
     const int64_t nbf = t.nw > 0 ? t.nb : nb;
-    w.sync_off = align256(sizeof(int32_t) * (size_t)nbf * (size_t)c.E);
+    w.table_words = (size_t)nbf * (size_t)c.E;
     const size_t fallback = align256(sizeof(int32_t) * (size_t)nb * (size_t)c.E);
-    const size_t fused = w.sync_off + 256;
+    const size_t fused = align256(sizeof(int32_t) * w.table_words);
     w.bytes = c.T == 0 ? 0 : (fallback > fused ? fallback : fused);
     return w;
 }
 
 namespace {
 
-__global__ void __launch_bounds__(kFusedMaxWarps * 32)
+// kMaxThreads: the CTA size the instance is compiled for (512, or 1024 for
+// 32 warps, which leaves 64 registers a thread: there the table is read 16
+// entries at a time instead of 32).
+template <int kMaxThreads>
+__global__ void __launch_bounds__(kMaxThreads)
 layout_fused_kernel(const int32_t *__restrict__ idx, int32_t T, int32_t E, int32_t R, int32_t k, int32_t nb,
-                    int32_t *__restrict__ counts, unsigned *__restrict__ sync, int32_t *__restrict__ expert_count,
+                    int32_t *__restrict__ counts, int32_t *__restrict__ expert_count,
                     int32_t *__restrict__ expert_offset, int32_t *__restrict__ rank_count,
                     int32_t *__restrict__ rank_offset, int32_t *__restrict__ slot, ep_chunk *__restrict__ chunks,
                     int32_t *__restrict__ n_chunks, int32_t *__restrict__ worker_begin, int32_t W,
@@ -136,42 +141,43 @@ layout_fused_kernel(const int32_t *__restrict__ idx, int32_t T, int32_t E, int32
     int32_t *s_P = s_roff + R + 1;             // [R+3] class prefix sums (schedule)
     __shared__ int s_warp32[32];
 
-    const int b = blockIdx.x;
-    const int64_t t_cta = (int64_t)b * tpw * nw;
-    cta_rank_tokens(idx, T, E, k, t_cta, cnt, tile_e, tile_r, counts + (int64_t)b * E, 1, tpw);
-
-    if (nb > 1 && !grid_barrier(&sync[0], (unsigned)nb)) {
-        if (threadIdx.x == 0) atomicExch(n_chunks, -1);
-        return;
-    }
-
-    // Expert totals over all CTAs and this CTA's prefix inside each expert.
-    // tpe threads share a column of the [CTA][E] table, each summing every
-    // tpe-th row; integer adds into shared memory make the order irrelevant.
+    __shared__ int s_fail;
+    if (threadIdx.x == 0) s_fail = 0;
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         s_tot[e] = 0;
         s_pre[e] = 0;
     }
-    __syncthreads();
-    {
+
+    const int b = blockIdx.x;
+    const int64_t t_cta = (int64_t)b * tpw * nw;
+    // s_eoff holds this CTA's per-expert counts until the table has been read.
+    cta_rank_tokens(idx, T, E, k, t_cta, cnt, tile_e, tile_r, s_eoff, 1, tpw);
+
+    // Publish them as row b of the count table and read every CTA's row
+    // (block_common.cuh: entries marked valid, polled, no grid barrier).
+    unsigned *tab = reinterpret_cast<unsigned *>(counts);
+    const TablePublish pub = nb > 1 ? table_publish(tab + (int64_t)b * E, s_eoff, E) : TablePublish{};
+
+    // Expert totals over all CTAs and this CTA's prefix inside each expert.
+    // tpe warps share 32 consecutive columns of the table (a lane per column,
+    // so each load of a warp is one 128-byte line), each summing every tpe-th
+    // row of the other CTAs (this CTA's own counts come from shared memory);
+    // integer adds into shared memory make the order irrelevant. (s_tot and
+    // s_pre were zeroed before the rank phase, whose CTA barriers order that.)
+    if (nb == 1) {
+        for (int e = threadIdx.x; e < E; e += blockDim.x) s_tot[e] = s_eoff[e];
+    } else {
         const int tpe = threads_per_expert(E, nw);
-        const int sub = (int)threadIdx.x % tpe;
-        for (int e = (int)threadIdx.x / tpe; e < E; e += blockDim.x / tpe) {
-            int tot = 0, pre = 0;
-            // rows sub, sub + tpe, ...: issue up to 32 loads before using any
-            for (int q0 = sub; q0 < nb; q0 += 32 * tpe) {
-                int cv[32];
-#pragma unroll
-                for (int u = 0; u < 32; ++u) {
-                    const int q = q0 + u * tpe;
-                    cv[u] = q < nb ? __ldcg(counts + (int64_t)q * E + e) : 0;
-                }
-#pragma unroll
-                for (int u = 0; u < 32; ++u) {
-                    tot += cv[u];
-                    pre += q0 + u * tpe < b ? cv[u] : 0;
-                }
+        const int warp = (int)threadIdx.x >> 5;
+        const int sub = warp % tpe;
+        for (int e = (warp / tpe) * 32 + ((int)threadIdx.x & 31); e < E; e += (nw / tpe) * 32) {
+            int tot, pre;
+            if (!table_column_sums<kMaxThreads <= 512 ? 32 : 16>(tab, E, e, sub, tpe, nb, b, b, kBarrierSpinLimit,
+                                                                 tot, pre)) {
+                s_fail = 1;
+                break;
             }
+            if (sub == 0) tot += s_eoff[e];
             if (tpe == 1) {
                 s_tot[e] = tot;
                 s_pre[e] = pre;
@@ -181,7 +187,12 @@ layout_fused_kernel(const int32_t *__restrict__ idx, int32_t T, int32_t E, int32
             }
         }
     }
+    if (pub.late()) s_fail = 1;
     __syncthreads();
+    if (s_fail) {
+        if (threadIdx.x == 0) atomicExch(n_chunks, -1);
+        return;
+    }
 
     // Exclusive scan of the totals: each thread scans a contiguous run.
     {
@@ -361,6 +372,12 @@ cudaError_t launch_fallback(const ep_config &c, int32_t W, const int32_t *idx, i
 
 }  // namespace
 
+// The layout_fused_kernel instance for CTAs of nw warps.
+static const void *layout_fused_fn(int nw) {
+    return nw * 32 <= 512 ? reinterpret_cast<const void *>(layout_fused_kernel<512>)
+                          : reinterpret_cast<const void *>(layout_fused_kernel<1024>);
+}
+
 static bool layout_fused_fits(const ep_config &c, int *nw_out, int64_t *nb_out, int *tpw_out = nullptr) {
     if (c.T == 0) return false;
     const LayoutTiling t = fused_tiling(c.T, c.E, c.R, c.k);
@@ -372,14 +389,16 @@ static bool layout_fused_fits(const ep_config &c, int *nw_out, int64_t *nb_out, 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices_) return false;
     if (!attr_set[dev]) {
-        if (cudaFuncSetAttribute(layout_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(layout_fused_kernel<512>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kFusedSmemBudget) != cudaSuccess ||
+            cudaFuncSetAttribute(layout_fused_kernel<1024>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)kFusedSmemBudget) != cudaSuccess) {
             cudaGetLastError();
             return false;
         }
         attr_set[dev] = true;
     }
-    const int per_sm = max_blocks_per_sm(reinterpret_cast<const void *>(layout_fused_kernel), nw * 32, smem);
+    const int per_sm = max_blocks_per_sm(layout_fused_fn(nw), nw * 32, smem);
     if (nb > (int64_t)sm_count(dev) * per_sm) return false;
     *nw_out = nw;
     *nb_out = nb;
@@ -397,7 +416,7 @@ int layout_kernel_count(const ep_config &c) {
 cudaError_t launch_layout(const ep_config &c, int32_t W, const int32_t *idx, int32_t *expert_count,
                           int32_t *expert_offset, int32_t *rank_count, int32_t *rank_offset, int32_t *slot,
                           ep_chunk *chunks, int32_t *n_chunks, int32_t *worker_begin, void *workspace,
-                          cudaStream_t s, bool sync_zeroed, bool defer_schedule, bool *deferred, bool after_route,
+                          cudaStream_t s, bool table_zeroed, bool defer_schedule, bool *deferred, bool after_route,
                           unsigned *zero_ctr) {
     if (deferred) *deferred = false;
     int nw = 0, tpw = 32;
@@ -406,11 +425,9 @@ cudaError_t launch_layout(const ep_config &c, int32_t W, const int32_t *idx, int
         return launch_fallback(c, W, idx, expert_count, expert_offset, rank_count, rank_offset, slot, chunks,
                                n_chunks, worker_begin, workspace, s);
 
-    const LayoutWorkspace ws = layout_workspace(c);
     int32_t *counts = static_cast<int32_t *>(workspace);
-    unsigned *sync = reinterpret_cast<unsigned *>(static_cast<char *>(workspace) + ws.sync_off);
-    if (nb > 1 && !sync_zeroed) {
-        cudaError_t e = cudaMemsetAsync(sync, 0, 2 * sizeof(unsigned), s);
+    if (nb > 1 && !table_zeroed) {
+        cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * (size_t)nb * (size_t)c.E, s);
         if (e != cudaSuccess) return e;
     }
     const size_t smem = fused_smem_bytes(nw, tpw, c.E, c.R, c.k);
@@ -438,18 +455,23 @@ cudaError_t launch_layout(const ep_config &c, int32_t W, const int32_t *idx, int
         attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 2;
-        const cudaError_t e = cudaLaunchKernelEx(&cfg, layout_fused_kernel, idx, T, E, R, k, nbi, counts, sync,
-                                                 expert_count, expert_offset, rank_count, rank_offset, slot, chunks,
-                                                 n_chunks, worker_begin, W, tiers, defer, tpw, zero_ctr);
+        const cudaError_t e =
+            nw * 32 <= 512
+                ? cudaLaunchKernelEx(&cfg, layout_fused_kernel<512>, idx, T, E, R, k, nbi, counts, expert_count,
+                                     expert_offset, rank_count, rank_offset, slot, chunks, n_chunks, worker_begin, W,
+                                     tiers, defer, tpw, zero_ctr)
+                : cudaLaunchKernelEx(&cfg, layout_fused_kernel<1024>, idx, T, E, R, k, nbi, counts, expert_count,
+                                     expert_offset, rank_count, rank_offset, slot, chunks, n_chunks, worker_begin, W,
+                                     tiers, defer, tpw, zero_ctr);
         if (e != cudaErrorInvalidValue && e != cudaErrorNotSupported) return e;
         cudaGetLastError();  // the launch was refused before anything was enqueued
         no_dependent_coop[dev] = true;
     }
-    void *args[] = {(void *)&idx, &T, &E, &R, &k, &nbi, (void *)&counts, (void *)&sync, (void *)&expert_count,
+    void *args[] = {(void *)&idx, &T, &E, &R, &k, &nbi, (void *)&counts, (void *)&expert_count,
                     (void *)&expert_offset, (void *)&rank_count, (void *)&rank_offset, (void *)&slot,
                     (void *)&chunks, (void *)&n_chunks, (void *)&worker_begin, &W, &tiers, &defer, &tpw,
                     (void *)&zero_ctr};
-    return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(layout_fused_kernel), dim3((unsigned)nb),
+    return cudaLaunchCooperativeKernel(layout_fused_fn(nw), dim3((unsigned)nb),
                                        dim3((unsigned)(nw * 32)), args, smem, s);
 }
 
@@ -463,16 +485,38 @@ cudaError_t launch_layout(const ep_config &c, int32_t W, const int32_t *idx, int
 // give up after max_polls polls and count themselves in *gave_up, and CTA 2
 // must see the failure too; a second kernel sets *gave_up = -1 if it did not.
 // CTA 3 runs the split dispatch's warp-wide wait on a ready flag that nothing
-// sets and must give up after max_polls polls as well.
+// sets and must give up after max_polls polls as well. CTAs 4 and 5 exchange
+// a two-row count table the way the single-kernel layout does: CTA 4 publishes
+// row 0 and reads both rows, but row 1 is published by CTA 5 only after CTA 4
+// has given up and poisoned it; both must fail (a successful late publish also
+// makes the second kernel set -1).
 // ---------------------------------------------------------------------------
 namespace ep {
 namespace {
 
 static __device__ unsigned g_check_arrivals[2];  // barrier arrivals, a flag nothing sets
-static __device__ int32_t g_check_late_passed;  // 1: the late CTA passed the barrier
+static __device__ unsigned g_check_table[2];     // a count table of two rows and one expert
+static __device__ int32_t g_check_late_passed;  // 1: a late CTA went on
 
-__global__ void bounded_wait_check_kernel(unsigned *arrivals, int32_t *late_passed, unsigned max_polls,
-                                          int32_t *gave_up) {
+__global__ void bounded_wait_check_kernel(unsigned *arrivals, unsigned *table, int32_t *late_passed,
+                                          unsigned max_polls, int32_t *gave_up) {
+    if (blockIdx.x >= 4) {
+        if (threadIdx.x != 0) return;
+        const int32_t own = 1;
+        if (blockIdx.x == 4) {
+            table_publish(table, &own, 1);
+            int tot, pre;
+            if (!table_column_sums(table, 1, 0, 0, 1, 2, 0, -1, max_polls, tot, pre)) atomicAdd(gave_up, 1);
+            return;
+        }
+        const uint64_t limit = 4ull * max_polls + 1024ull;
+        for (uint64_t i = 0; i < limit && ld_relaxed_gpu(table + 1) != kCountPoison; ++i) __nanosleep(64);
+        if (table_publish(table + 1, &own, 1).late())
+            atomicAdd(gave_up, 1);
+        else
+            *late_passed = 1;
+        return;
+    }
     if (blockIdx.x == 3) {
         // the split dispatch's wait on a tile's ready flag, on a flag nothing sets
         if (threadIdx.x < 32 && !warp_wait_flag(arrivals + 1, max_polls) && threadIdx.x == 0) atomicAdd(gave_up, 1);
@@ -496,15 +540,17 @@ __global__ void bounded_wait_verdict_kernel(const int32_t *late_passed, int32_t 
 }  // namespace
 
 cudaError_t launch_bounded_wait_check(uint32_t max_polls, int32_t *gave_up, cudaStream_t s) {
-    void *arrivals = nullptr, *late = nullptr;
+    void *arrivals = nullptr, *table = nullptr, *late = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&arrivals, g_check_arrivals);
     if (e != cudaSuccess) return e;
+    if ((e = cudaGetSymbolAddress(&table, g_check_table)) != cudaSuccess) return e;
     if ((e = cudaGetSymbolAddress(&late, g_check_late_passed)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(arrivals, 0, 2 * sizeof(unsigned), s)) != cudaSuccess) return e;
+    if ((e = cudaMemsetAsync(table, 0, 2 * sizeof(unsigned), s)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(late, 0, sizeof(int32_t), s)) != cudaSuccess) return e;
     if ((e = cudaMemsetAsync(gave_up, 0, sizeof(int32_t), s)) != cudaSuccess) return e;
-    bounded_wait_check_kernel<<<4, 32, 0, s>>>(static_cast<unsigned *>(arrivals), static_cast<int32_t *>(late),
-                                               max_polls, gave_up);
+    bounded_wait_check_kernel<<<6, 32, 0, s>>>(static_cast<unsigned *>(arrivals), static_cast<unsigned *>(table),
+                                               static_cast<int32_t *>(late), max_polls, gave_up);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     bounded_wait_verdict_kernel<<<1, 1, 0, s>>>(static_cast<const int32_t *>(late), gave_up);
     return cudaGetLastError();

@@ -24,9 +24,10 @@ route_kernel(const float *__restrict__ logits, int32_t T, int32_t E, int32_t k, 
     // A layout launched after this kernel may start now: it waits for this
     // grid before it reads anything this one writes.
     grid_launch_dependents();
-    // Reset the counters that later kernels of the same call sequence start from.
+    // Reset what later kernels of the same call sequence start from: zero_a
+    // (the layout's count table) over all CTAs, the rest by the first.
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_zero_a; i += gridDim.x * blockDim.x) zero_a[i] = 0u;
     if (blockIdx.x == 0) {
-        if ((int)threadIdx.x < n_zero_a) zero_a[threadIdx.x] = 0u;
         if ((int)threadIdx.x < n_zero_b) zero_b[threadIdx.x] = 0u;
         if (threadIdx.x == 0 && zero_c) *zero_c = 0;
     }

@@ -117,16 +117,20 @@ ep_status ep_device_error(int32_t *flags);
 
 /* Diagnostics: checks that the library's device-side waits are bounded and
  * that a failure cannot be hidden. Launches two CTAs into a grid barrier (the
- * kind ep_layout and ep_dispatch_fused use) that expects three arrivals, so
- * the wait cannot complete in time; each CTA must give up after max_polls
- * polls (> 0) and count itself in *gave_up (device int32, zeroed first). A
- * third CTA makes the last arrival only after one of them has given up; it
- * must see the failure as well (in ep_layout that keeps the CTA that writes
- * the chunk count from overwriting *n_chunks = -1), else *gave_up is set to
- * -1. A fourth CTA waits, as ep_dispatch_fused's data CTAs do, on a ready
- * flag that nothing sets, and must give up after max_polls polls and count
- * itself. Expected result: 3. The kernels return normally; nothing faults or
- * hangs. */
+ * kind ep_dispatch_fused uses) that expects three arrivals, so the wait cannot
+ * complete in time; each CTA must give up after max_polls polls (> 0) and
+ * count itself in *gave_up (device int32, zeroed first). A third CTA makes the
+ * last arrival only after one of them has given up; it must see the failure
+ * as well, else *gave_up is set to -1. A fourth CTA waits, as
+ * ep_dispatch_fused's data CTAs do, on a ready flag that nothing sets, and
+ * must give up after max_polls polls and count itself. A fifth and a sixth CTA
+ * exchange a two-row count table the way ep_layout's CTAs do: the fifth
+ * publishes its row and polls for the other, which the sixth publishes only
+ * after the fifth has given up; both must count themselves (the sixth learns
+ * from its publish that it came too late; in ep_layout that keeps a late CTA
+ * from going on and a chunk count from overwriting *n_chunks = -1), else
+ * *gave_up is set to -1. Expected result: 5. The kernels return normally;
+ * nothing faults or hangs. */
 ep_status ep_check_bounded_wait(int32_t max_polls, int32_t *gave_up, cudaStream_t stream);
 
 /* Bytes of device scratch that ep_layout needs for `cfg` (it depends on T and
@@ -211,12 +215,15 @@ ep_status ep_route(const ep_config *cfg, const float *logits, int32_t *topk_idx,
  *                 256-byte aligned; else EP_ERR_CAPACITY / EP_ERR_INVALID_ARG
  *
  * When every layout CTA fits on the GPU at once, the layout is one
- * cooperative launch whose CTAs meet at a grid barrier in the workspace (two
- * words zeroed by an enqueued memset). That wait is bounded: a CTA that gives
- * up sets *n_chunks = -1 and leaves its slots unwritten, and every other CTA
- * of the launch then fails too, so no chunk count overwrites the -1 (this
- * cannot happen under a cooperative launch, which only starts when all CTAs
- * are resident).
+ * cooperative launch whose CTAs exchange their per-expert counts through a
+ * [CTA][E] table in the workspace (zeroed by an enqueued memset when there is
+ * more than one CTA): each CTA publishes its row with every entry marked
+ * valid and polls the others' entries until they are, with no grid barrier.
+ * That wait is bounded: a CTA that gives up marks the entries it still misses
+ * as failed, sets *n_chunks = -1 and leaves its slots unwritten; every other
+ * CTA, including the late owner of those entries, then fails too, so no chunk
+ * count overwrites the -1 (this cannot happen under a cooperative launch,
+ * which only starts when all CTAs are resident).
  * Larger T uses three ordinary kernels.
  */
 ep_status ep_layout(const ep_config *cfg, const int32_t *topk_idx,
@@ -438,7 +445,7 @@ ep_status ep_combine(const ep_config *cfg, const ep_bf16 *y, const int32_t *slot
  * cudaMalloc, cudaFree or other allocating routine.
  *  - Limit: shapes whose ep_layout_workspace_size exceeds
  *    EP_LAYOUT_STATIC_SCRATCH_BYTES return EP_ERR_CAPACITY with nothing
- *    enqueued. That size is max(a(4 E ceil(T / 256)), a(4 E n) + 256) bytes,
+ *    enqueued. That size is max(a(4 E ceil(T / 256)), a(4 E n)) bytes,
  *    a() rounding up to a multiple of 256 and n <= max(ceil(T / 256), 64)
  *    the single-kernel layout's CTA count: E = 256 allows T <= 262144 tokens
  *    (exactly 1 MiB at T = 262144).
