@@ -1008,7 +1008,9 @@ def latency_point(ep, w0, args, rank: int, world: int, device, flush_l2, K: int)
     L2 flushed before each replay (outside the events); median and spread over
     the replays, the slowest rank's median (``us_per_layer``). Also the step's
     marginal time inside a graph that holds the flush as well (``in_graph_us``,
-    no graph launch of its own, as in a model that runs its layers in one graph)."""
+    no graph launch of its own, as in a model that runs its layers in one graph),
+    and the step timed right after the same step on another layer's buffers
+    (``after_other_layer_us``: its data flushed, the kernels' code warm)."""
     import torch
 
     w = rank_workload(w0, rank)
@@ -1049,14 +1051,39 @@ def latency_point(ep, w0, args, rank: int, world: int, device, flush_l2, K: int)
 
     NG = max(K, 200)
     in_graph = mean_us(flush_step, NG) - mean_us(flush_only, NG)
-    red = reduce_max_many({"median": st["median"], "mean": 1e3 * sum(ms) / K, "in_graph": in_graph}, world, device)
+
+    # The step right after the same calls on another layer's buffers (same
+    # shapes, its own inputs): L2 flushed before that other layer, so this
+    # step's data is as cold as after the flush, but the kernels' code is warm,
+    # as in a model whose layers run these kernels one after another.
+    _, buf2, _, _ = prepare_layer(ep, rank_workload(w0.with_(seed=w0.seed + 1000), rank), device)
+    other = capture_step_graph(buf2, device, fused)
+    for _ in range(3):
+        flush_l2()
+        other.replay()
+        graph.replay()
+    ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, b_ in ev2:
+        flush_l2()
+        other.replay()
+        a.record(stream)
+        graph.replay()
+        b_.record(stream)
+    torch.cuda.synchronize()
+    ms2 = [a.elapsed_time(b_) for a, b_ in ev2]
+
+    red = reduce_max_many({"median": st["median"], "mean": 1e3 * sum(ms) / K, "in_graph": in_graph,
+                           "other_median": step_stats_us(ms2)["median"], "other_mean": 1e3 * sum(ms2) / K},
+                          world, device)
     peak, _ = measured_peak_gbs()
     out = {"us_per_layer": round(red["median"], 2), "us_mean": round(red["mean"], 2), "stats_us": st,
            "in_graph_us": round(red["in_graph"], 2), "in_graph_steps": NG,
+           "after_other_layer_us": {"median": round(red["other_median"], 2), "mean": round(red["other_mean"], 2),
+                                    "steps": K},
            "kernels": ep.ep_step_kernel_count(cfg, fused=fused), "bytes_per_step": w.total_bytes(),
            "hbm_fraction": round(w.total_bytes() / (red["median"] * 1e-6) / 1e9 / peak, 4), "steps": K,
            "T": w.T, "dist": "zipf 1.2" if w.zipf_s else "uniform"}
-    del graph, flush_only, flush_step, buf
+    del graph, flush_only, flush_step, buf, other, buf2
     return out
 
 
