@@ -37,6 +37,8 @@
 // layer: T = 8 21.6 -> 19.5 us, T = 16 22.7 -> 21.0, T = 96 25.1 -> 23.0, T = 160
 // 28.6 -> 27.3, T = 1 -0.5, T = 64 -0.3; at T = 192 and 256 within +-0.2 us, at
 // T = 512 +4 us, so the split form stops at T = 160).
+// The barrier words and ready flags are zeroed by a one-CTA kernel launched
+// just before, of which the fused kernel is a programmatic dependent.
 // Every result equals what ep_route, ep_layout and ep_dispatch write.
 #include "block_common.cuh"
 #include "flag_ops.cuh"
@@ -156,6 +158,15 @@ __device__ __forceinline__ bool split_data_unit(const FusedArgs &a, int64_t t, i
     return true;
 }
 
+// Zeroes the fused kernel's barrier words and ready flags. The fused kernel,
+// launched right after it as its programmatic dependent, loads x rows, routes
+// and ranks meanwhile, and waits for this grid only before it touches them
+// (a memset node in its place cost 1.5-2 us per call at small T).
+__global__ void __launch_bounds__(256) fused_zero_kernel(unsigned *p, int n) {
+    grid_launch_dependents();
+    for (int i = threadIdx.x; i < n; i += blockDim.x) p[i] = 0u;
+}
+
 template <int VPL, bool kSplit>
 __global__ void __launch_bounds__(kFusedThreads, 2) dispatch_fused_kernel(FusedArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -219,6 +230,7 @@ __global__ void __launch_bounds__(kFusedThreads, 2) dispatch_fused_kernel(FusedA
                     mbar_arrive_expect_tx(&bar[0], (uint32_t)row_bytes);
                     bulk_g2s(stages, a.x + t * row_bytes, (uint32_t)row_bytes, &bar[0]);
                 }
+                if (cur < 0) grid_dependency_wait();  // the ready flags are zeroed by the grid before this one
                 ++loads;
                 cur = t;
             }
@@ -263,7 +275,9 @@ __global__ void __launch_bounds__(kFusedThreads, 2) dispatch_fused_kernel(FusedA
     if (!sched_only) cta_rank_pairs(tile_e, np, ppw, E, cnt, tile_r, a.counts + (int64_t)b * E, 1);
 
     // C. (a single CTA needs no grid barrier: after a CTA barrier its own
-    // global writes are visible to all its threads)
+    // global writes are visible to all its threads). The barrier words and
+    // ready flags are zeroed by the grid launched before this one.
+    grid_dependency_wait();
     bool ok = arrivals > 1 ? grid_barrier(&a.sync[0], arrivals) : (__syncthreads(), true);
 
     // D. column scan: CTA b owns experts b, b + nb, ...; all their counts over
@@ -600,8 +614,9 @@ size_t fused_workspace_bytes(const ep_config &c) {
 
 int fused_call_kernels(const ep_config &c) {
     FusedPlan p;
-    if (!plan_split(c, &p) && !plan_fused(c, &p)) return 2 + layout_kernel_count(c);  // route, layout, dispatch
-    return 1;
+    const bool split = plan_split(c, &p);
+    if (!split && !plan_fused(c, &p)) return 2 + layout_kernel_count(c);  // route, layout, dispatch
+    return split || p.nb + p.sched_cta > 1 ? 2 : 1;  // (the zeroing kernel,) the fused kernel
 }
 
 cudaError_t launch_dispatch_fused(const ep_config &c, int32_t W, const float *logits, const ep_bf16 *x,
@@ -687,17 +702,41 @@ cudaError_t launch_dispatch_fused(const ep_config &c, int32_t W, const float *lo
     a.ready = a.sync + 2;
     // measured: T = 1..64 (<= 7.3 MB of send rows) gain 1-2 us, T = 256 even, T = 512 (59 MB) loses 1.8 us
     a.early_dependents = (int64_t)c.T * c.k * c.H * 2 <= (int64_t)16 << 20 ? 1 : 0;
-    if (split) {  // barrier words and the tiles' ready flags
-        e = cudaMemsetAsync(a.sync, 0, (2 + (size_t)p.nb) * sizeof(unsigned), s);
-        if (e != cudaSuccess) return e;
-    } else if (p.nb + p.sched_cta > 1) {  // a single CTA uses no grid barrier (and the memset costs ~0.5 us at T = 1)
-        e = cudaMemsetAsync(a.sync, 0, 2 * sizeof(unsigned), s);
-        if (e != cudaSuccess) return e;
+    // The barrier words and (split form) the tiles' ready flags are zeroed by a
+    // one-CTA kernel in front of the fused one; a single CTA of the single-role
+    // form uses neither.
+    const int n_zero = split ? 2 + p.nb : (p.nb + p.sched_cta > 1 ? 2 : 0);
+    if (n_zero > 0) {
+        fused_zero_kernel<<<1, 256, 0, s>>>(a.sync, n_zero);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    const FusedKernel kern = pick_kernel(c.E, split);
+    const dim3 grid((unsigned)(p.nb + p.sched_cta + p.n_data));
+    // Set when a device refused the cooperative launch with the dependent-launch
+    // attribute; the plain cooperative launch is then used (the same results).
+    static std::atomic<bool> no_dependent_coop[kMaxDevices_];  // zero-initialised: false
+    int dev = 0;
+    if (n_zero > 0 && current_device(&dev) == cudaSuccess && !no_dependent_coop[dev]) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(kFusedThreads);
+        cfg.dynamicSmemBytes = p.smem;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        e = cudaLaunchKernelEx(&cfg, kern, a);
+        if (e != cudaErrorInvalidValue && e != cudaErrorNotSupported) return e;
+        cudaGetLastError();  // the launch was refused before anything was enqueued
+        no_dependent_coop[dev] = true;
     }
     void *args[] = {&a};
-    return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(pick_kernel(c.E, split)),
-                                       dim3((unsigned)(p.nb + p.sched_cta + p.n_data)),
-                                       dim3(kFusedThreads), args, p.smem, s);
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void *>(kern), grid, dim3(kFusedThreads), args, p.smem,
+                                       s);
 }
 
 }  // namespace ep

@@ -261,14 +261,15 @@ ep_status ep_dispatch(const ep_config *cfg, const ep_bf16 *x, const int32_t *slo
  * and each CTA's x rows are fetched with bulk copies while that metadata is
  * being computed. Up to 160 tokens the rows are moved by separate data CTAs
  * instead, each waiting (bounded) on a ready flag that the tile holding its
- * token releases once its slots are written. It pays off at small T (decode
- * batches), where the phases
- * are latency-bound; when a CTA would have to route more than 8 tokens (T
- * above 8 tokens per resident CTA, about 2400 on a GB300) the call runs the
- * three separate steps instead (the route kernel zeroing the layout's
- * barrier words, the single-kernel layout -- launched as a programmatic
- * dependent of the route kernel when that one runs in a single wave --
- * zeroing the dispatch's token counter, the dispatch taking tokens
+ * token releases once its slots are written. The barrier words and flags are
+ * zeroed by a one-CTA kernel launched just before the fused kernel, which is
+ * its programmatic dependent. It pays off at small T (decode batches), where
+ * the phases are latency-bound; when a CTA would have to route more than 8
+ * tokens (T above 8 tokens per resident CTA, about 2400 on a GB300) the call
+ * runs the three separate steps instead (the route kernel zeroing the
+ * layout's count table, the single-kernel layout -- launched as a
+ * programmatic dependent of the route kernel when that one runs in a single
+ * wave -- zeroing the dispatch's token counter, the dispatch taking tokens
  * dynamically and building the chunk schedule in one extra CTA while the
  * others copy rows), with the same results.
  *
