@@ -225,7 +225,13 @@ def ncu_traffic(kernel: str, workload: str):
         ent = data[workload][kernel]
     except (KeyError, ValueError):
         return None
-    if ent.get("source_sha256_16") != kernel_source_hash(kernel):
+    # an entry summed from other kernels' captures (the dispatch call at large
+    # T runs route, layout and dispatch kernels) is valid while all of them are
+    parts = ent.get("components")
+    if parts:
+        if any(data[workload].get(c, {}).get("source_sha256_16") != kernel_source_hash(c) for c in parts):
+            return None
+    elif ent.get("source_sha256_16") != kernel_source_hash(kernel):
         return None
     return ent.get("dram_bytes_per_launch")
 

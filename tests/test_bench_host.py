@@ -81,13 +81,18 @@ def test_code_only_ignores_comments_and_blank_space():
 def test_traffic_summary_entries_are_complete():
     data = json.loads((bench.ROOT / "profiles" / "dram_traffic.txt").read_text())
     assert "ncu" in data["command"] and "--clock-control none" in data["command"]
-    for kernel, ent in data["prefill"].items():
-        assert kernel in bench.KERNEL_SOURCES
-        assert isinstance(ent["dram_bytes_per_launch"], int) and ent["dram_bytes_per_launch"] > 0
-        assert len(ent["source_sha256_16"]) == 16
-    p = data["prefill"]
-    assert p["dispatch_fused"]["dram_bytes_per_launch"] == sum(
-        p[k]["dram_bytes_per_launch"] for k in ("route", "layout", "dispatch"))
+    for workload in ("prefill", "sweep-zipf-T32768"):
+        for kernel, ent in data[workload].items():
+            assert kernel in bench.KERNEL_SOURCES
+            assert isinstance(ent["dram_bytes_per_launch"], int) and ent["dram_bytes_per_launch"] > 0
+            if "components" in ent:  # summed from other captures: valid while each of them is
+                assert all(c in data[workload] and "components" not in data[workload][c] for c in ent["components"])
+            else:
+                assert len(ent["source_sha256_16"]) == 16
+        p = data[workload]
+        assert p["dispatch_fused"]["components"] == ["route", "layout", "dispatch"]
+        assert p["dispatch_fused"]["dram_bytes_per_launch"] == sum(
+            p[k]["dram_bytes_per_launch"] for k in ("route", "layout", "dispatch"))
 
 
 def test_traffic_is_dropped_once_the_kernel_source_changes(monkeypatch):
@@ -98,6 +103,17 @@ def test_traffic_is_dropped_once_the_kernel_source_changes(monkeypatch):
     monkeypatch.setattr(bench, "kernel_source_hash", lambda k: "0" * 16)
     assert bench.ncu_traffic(kernel, "prefill") is None
     assert bench.ncu_traffic(kernel, "no-such-workload") is None
+
+
+def test_summed_traffic_follows_its_components(monkeypatch):
+    data = json.loads((bench.ROOT / "profiles" / "dram_traffic.txt").read_text())
+    p = data["prefill"]
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda k: p[k].get("source_sha256_16", "?"))
+    assert bench.ncu_traffic("dispatch_fused", "prefill") == p["dispatch_fused"]["dram_bytes_per_launch"]
+    # one component changed: the sum is dropped too
+    monkeypatch.setattr(bench, "kernel_source_hash",
+                        lambda k: "0" * 16 if k == "layout" else p[k].get("source_sha256_16", "?"))
+    assert bench.ncu_traffic("dispatch_fused", "prefill") is None
 
 
 def test_clock_sampler_with_a_fake_nvidia_smi(tmp_path, monkeypatch):
