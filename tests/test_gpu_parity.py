@@ -361,9 +361,13 @@ def test_route_unaligned_logits(ep, orc):
     assert_route(dict(idx=idx.cpu().numpy(), w=w.cpu().numpy()), dict(idx=r_idx, w=r_w), logits, 1)
 
 
-@pytest.mark.parametrize("T,E,R,k,rpp", [(400_000, 256, 32, 8, 0), (160_000, 1024, 64, 32, 32)])
+@pytest.mark.parametrize("T,E,R,k,rpp", [(400_000, 256, 32, 8, 0), (160_000, 1024, 64, 32, 32),
+                                          (100_000, 256, 32, 8, 0), (20_000, 1024, 64, 32, 0)])
 def test_layout_many_ctas(ep, orc, T, E, R, k, rpp):
-    """T beyond one co-resident grid: the three-kernel layout path."""
+    """T beyond one co-resident grid: the three-kernel layout path (T = 400000, 160000). And single-kernel
+    layouts of more than 64 CTAs, whose count table takes a thread several batches of polled loads: T = 100000
+    (98 CTAs of 32 warps, 16 loads per batch) and T = 20000 at E = 1024 (79 CTAs of 8 warps, 4 columns and
+    79 rows per thread, 32 loads per batch)."""
     rng = np.random.default_rng(T)
     base = rng.integers(0, E, size=(T, 1))
     step = rng.integers(1, E // k + 1, size=(T, 1))
