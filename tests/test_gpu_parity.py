@@ -439,6 +439,13 @@ FUSED = [
     ep_synth.CONFIGS["prefill"].with_(name="split-T63-plain", T=63, renormalize=0),
     ep_synth.CONFIGS["decode"].with_(name="split-T160", T=160),
     ep_synth.CONFIGS["decode"].with_(name="fused-T161", T=161),
+    # just above the small-batch kernel's range (route, layout and dispatch kernels; ragged last layout CTA)
+    ep_synth.Workload("three-kernels-groups-T3001", T=3001, H=1024, E=128, R=16, k=8, n_groups=8, topk_groups=4,
+                      num_workers=152),
+    ep_synth.Workload("three-kernels-g24-T2500", T=2500, H=1024, E=96, R=6, k=6, n_groups=4, topk_groups=2,
+                      ranks_per_node=2, self_rank=5, num_workers=33),
+    ep_synth.Workload("three-kernels-E1024-T2600", T=2600, H=512, E=1024, R=32, k=32, num_workers=152),
+    ep_synth.CONFIGS["prefill"].with_(name="three-kernels-plain-T4095", T=4095, renormalize=0),
 ] + [w for w in ep_synth.sweep_workloads() if w.T in (1, 8, 64, 512, 4096, 32768)]
 
 
