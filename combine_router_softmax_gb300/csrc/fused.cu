@@ -55,6 +55,11 @@ constexpr int kMaxFusedCTAs = 1024;
 constexpr uint32_t kFusedMaxPolls = 1u << 22;
 constexpr size_t kFusedSmemLimit = 200 * 1024;
 constexpr int kSplitMaxT = 160;  // split form up to this many tokens
+// Above this many tokens the route, layout and dispatch kernels beat the fused
+// kernel (measured per layer, E = 256, k = 8, H = 7168: T = 1536 78.4 against
+// 81.1 us, T = 2000 98.0 against 94.9, T = 2400 113.7 against 110.2; the lines
+// cross near 1760).
+constexpr int kFusedMaxT = 1760;
 
 static __device__ int32_t g_fused_error;
 
@@ -525,7 +530,7 @@ bool plan_split(const ep_config &c, FusedPlan *p) {
 // of each other in size. false if the fused kernel
 // cannot run this shape (then the caller runs the three separate steps).
 bool plan_fused(const ep_config &c, FusedPlan *p) {
-    if (c.T <= 0) return false;
+    if (c.T <= 0 || c.T > kFusedMaxT) return false;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices_) return false;
     const FusedKernel kern = pick_kernel(c.E, false);

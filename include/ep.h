@@ -264,9 +264,8 @@ ep_status ep_dispatch(const ep_config *cfg, const ep_bf16 *x, const int32_t *slo
  * token releases once its slots are written. The barrier words and flags are
  * zeroed by a one-CTA kernel launched just before the fused kernel, which is
  * its programmatic dependent. It pays off at small T (decode batches), where
- * the phases are latency-bound; when a CTA would have to route more than 8
- * tokens (T above 8 tokens per resident CTA, about 2400 on a GB300) the call
- * runs the three separate steps instead (the route kernel zeroing the
+ * the phases are latency-bound; above 1760 tokens (measured: there the
+ * separate kernels are faster) the call runs the three separate steps instead (the route kernel zeroing the
  * layout's count table, the single-kernel layout -- launched as a
  * programmatic dependent of the route kernel when that one runs in a single
  * wave -- zeroing the dispatch's token counter, the dispatch taking tokens

@@ -439,7 +439,10 @@ FUSED = [
     ep_synth.CONFIGS["prefill"].with_(name="split-T63-plain", T=63, renormalize=0),
     ep_synth.CONFIGS["decode"].with_(name="split-T160", T=160),
     ep_synth.CONFIGS["decode"].with_(name="fused-T161", T=161),
-    # just above the small-batch kernel's range (route, layout and dispatch kernels; ragged last layout CTA)
+    # either side of the small-batch kernel's upper bound (1760 tokens)
+    ep_synth.CONFIGS["decode"].with_(name="fused-T1760", T=1760),
+    ep_synth.CONFIGS["decode"].with_(name="three-kernels-T1761", T=1761),
+    # above the small-batch kernel's range (route, layout and dispatch kernels; ragged last layout CTA)
     ep_synth.Workload("three-kernels-groups-T3001", T=3001, H=1024, E=128, R=16, k=8, n_groups=8, topk_groups=4,
                       num_workers=152),
     ep_synth.Workload("three-kernels-g24-T2500", T=2500, H=1024, E=96, R=6, k=6, n_groups=4, topk_groups=2,
