@@ -277,7 +277,9 @@ __global__ void __launch_bounds__(kFusedThreads, 2) dispatch_fused_kernel(FusedA
 
     // B. rank the tile's pairs; publish the tile's counts
     const int ppw = np > 0 ? (np + kFusedWarps - 1) / kFusedWarps : 1;
-    if (!sched_only) cta_rank_pairs(tile_e, np, ppw, E, cnt, tile_r, a.counts + (int64_t)b * E, 1);
+    // (a single CTA keeps its counts in shared memory: they are the totals)
+    if (!sched_only)
+        cta_rank_pairs(tile_e, np, ppw, E, cnt, tile_r, arrivals == 1 ? s_tot : a.counts + (int64_t)b * E, 1);
 
     // C. (a single CTA needs no grid barrier: after a CTA barrier its own
     // global writes are visible to all its threads). The barrier words and
@@ -287,9 +289,9 @@ __global__ void __launch_bounds__(kFusedThreads, 2) dispatch_fused_kernel(FusedA
 
     // D. column scan: CTA b owns experts b, b + nb, ...; all their counts over
     // every tile are read in one batch, then scanned over the tiles. (A single
-    // CTA skips it: its counts are the totals, its bases zero; step F reads
-    // them straight from its published counts, one global round trip fewer:
-    // T = 1 and 8 -1 to -1.9 us per layer.)
+    // CTA skips it and the global reads of step F: its counts, kept in shared
+    // memory, are the totals and its bases are zero: T = 1 and 8 -1.4 to -2.3
+    // us per layer.)
     if (ok && !sched_only && arrivals > 1) {
         const int nb = a.nb;
         const int my_n = b < E ? (E - b + nb - 1) / nb : 0;
@@ -336,7 +338,6 @@ __global__ void __launch_bounds__(kFusedThreads, 2) dispatch_fused_kernel(FusedA
         // F. expert offsets and this tile's slots
         for (int e = threadIdx.x; e < E; e += blockDim.x) {
             if (arrivals == 1) {
-                s_tot[e] = __ldcg(a.counts + e);
                 s_base[e] = 0;
             } else {
                 s_tot[e] = __ldcg(a.totals + e);
