@@ -15,6 +15,8 @@
 //      tiles in one batch and publishes each tile's base inside each of those
 //      experts and their totals;
 //   E. bounded grid barrier;
+//      (up to 16384 pairs, D and E give way to C': every CTA reads all of
+//      topk_idx, written in A, and counts the totals and its bases itself);
 //   F. each CTA reads its tile's bases and the totals, scans the totals into
 //      expert offsets and writes its slots; CTA 0 writes counts and offsets.
 //      The chunk schedule is built by one extra CTA that holds no tile (it
@@ -60,6 +62,7 @@ constexpr int kSplitMaxT = 160;  // split form up to this many tokens
 // 81.1 us, T = 2000 98.0 against 94.9, T = 2400 113.7 against 110.2; the lines
 // cross near 1760).
 constexpr int kFusedMaxT = 1760;
+constexpr int64_t kHistMaxPairs = 16384;
 
 static __device__ int32_t g_fused_error;
 
@@ -137,6 +140,10 @@ struct FusedArgs {
     // token); ready[q] is set (release) once tile q's slots are written.
     int32_t n_data, unit_rows;
     unsigned *ready;
+    // 1: after barrier C every CTA reads all of topk_idx and counts, in shared
+    // memory, every expert's pairs (the totals) and those of the tokens before
+    // its tile (its bases); steps D and E are skipped.
+    int32_t hist;
 };
 
 // The rows of one token (unit_rows of them from top-k position jj0), moved by
@@ -259,6 +266,11 @@ __global__ void __launch_bounds__(kFusedThreads, 2) dispatch_fused_kernel(FusedA
         }
     }
 
+    if (a.hist)
+        for (int e = threadIdx.x; e < E; e += blockDim.x) {
+            s_tot[e] = 0;
+            s_base[e] = 0;
+        }
     // A. route the tile, one warp per token
     for (int i = warp; i < ntok; i += kFusedWarps) {
         const int64_t t = t0 + i;
@@ -279,20 +291,43 @@ __global__ void __launch_bounds__(kFusedThreads, 2) dispatch_fused_kernel(FusedA
     const int ppw = np > 0 ? (np + kFusedWarps - 1) / kFusedWarps : 1;
     // (a single CTA keeps its counts in shared memory: they are the totals)
     if (!sched_only)
-        cta_rank_pairs(tile_e, np, ppw, E, cnt, tile_r, arrivals == 1 ? s_tot : a.counts + (int64_t)b * E, 1);
+        cta_rank_pairs(tile_e, np, ppw, E, cnt, tile_r,
+                       arrivals == 1 ? s_tot : (a.hist ? s_col : a.counts + (int64_t)b * E), 1);
 
     // C. (a single CTA needs no grid barrier: after a CTA barrier its own
     // global writes are visible to all its threads). The barrier words and
     // ready flags are zeroed by the grid launched before this one.
     grid_dependency_wait();
     bool ok = arrivals > 1 ? grid_barrier(&a.sync[0], arrivals) : (__syncthreads(), true);
+    // C'. (hist) every tile's picks are in topk_idx now: the expert totals and
+    // this tile's bases counted from them directly, 8 loads in flight a thread.
+    if (ok && a.hist) {
+        const int64_t n = (int64_t)a.T * k, before = t0 * k;
+        for (int64_t i0 = threadIdx.x; i0 < n; i0 += 8 * (int64_t)blockDim.x) {
+            int ev[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int64_t i = i0 + (int64_t)u * blockDim.x;
+                ev[u] = i < n ? __ldcg(a.topk_idx + i) : -1;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int64_t i = i0 + (int64_t)u * blockDim.x;
+                const int e = ev[u];
+                if ((unsigned)e < (unsigned)E) {
+                    atomicAdd(&s_tot[e], 1);
+                    if (i < before) atomicAdd(&s_base[e], 1);
+                }
+            }
+        }
+    }
 
     // D. column scan: CTA b owns experts b, b + nb, ...; all their counts over
     // every tile are read in one batch, then scanned over the tiles. (A single
     // CTA skips it and the global reads of step F: its counts, kept in shared
     // memory, are the totals and its bases are zero: T = 1 and 8 -1.4 to -2.3
     // us per layer.)
-    if (ok && !sched_only && arrivals > 1) {
+    if (ok && !sched_only && arrivals > 1 && !a.hist) {
         const int nb = a.nb;
         const int my_n = b < E ? (E - b + nb - 1) / nb : 0;
         const int nv = my_n * nb;
@@ -332,14 +367,14 @@ __global__ void __launch_bounds__(kFusedThreads, 2) dispatch_fused_kernel(FusedA
         }
     }
     // E.
-    if (ok) ok = arrivals > 1 ? grid_barrier(&a.sync[1], arrivals) : (__syncthreads(), true);
+    if (ok) ok = arrivals > 1 && !a.hist ? grid_barrier(&a.sync[1], arrivals) : (__syncthreads(), true);
 
     if (ok) {
         // F. expert offsets and this tile's slots
         for (int e = threadIdx.x; e < E; e += blockDim.x) {
             if (arrivals == 1) {
                 s_base[e] = 0;
-            } else {
+            } else if (!a.hist) {
                 s_tot[e] = __ldcg(a.totals + e);
                 if (!sched_only) s_base[e] = __ldcg(a.bases + (int64_t)b * E + e);
             }
@@ -714,6 +749,11 @@ cudaError_t launch_dispatch_fused(const ep_config &c, int32_t W, const float *lo
     a.n_data = p.n_data;
     a.unit_rows = p.unit_rows;
     a.ready = a.sync + 2;
+    // Up to kHistMaxPairs pairs every CTA reads all of topk_idx after the first
+    // barrier instead of the column scan and the second barrier (measured per
+    // layer: T = 64 -1.6 us, T = 160 -2.1, decode -2.3, T = 512 -2.1, T = 1024
+    // -1.6, T = 1760 +-0.3).
+    a.hist = p.nb + p.sched_cta > 1 && (int64_t)c.T * c.k <= kHistMaxPairs ? 1 : 0;
     // measured: T = 1..64 (<= 7.3 MB of send rows) gain 1-2 us, T = 256 even, T = 512 (59 MB) loses 1.8 us
     a.early_dependents = (int64_t)c.T * c.k * c.H * 2 <= (int64_t)16 << 20 ? 1 : 0;
     // The barrier words and (split form) the tiles' ready flags are zeroed by a

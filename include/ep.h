@@ -257,7 +257,9 @@ ep_status ep_dispatch(const ep_config *cfg, const ep_bf16 *x, const int32_t *slo
  * Follows the UBEP article's "Kernel Decomposition": instead of separate
  * phases joined by global barriers, one cooperative kernel gives every CTA a
  * tile of tokens to route, rank and dispatch; the CTAs exchange the per-expert
- * counts through global memory at two bounded grid barriers (in the workspace)
+ * counts through global memory at bounded grid barriers (in the workspace; up
+ * to 16384 (token, expert) pairs one barrier, after which every CTA counts
+ * the totals and its bases from all of topk_idx)
  * and each CTA's x rows are fetched with bulk copies while that metadata is
  * being computed. Up to 160 tokens the rows are moved by separate data CTAs
  * instead, each waiting (bounded) on a ready flag that the tile holding its
