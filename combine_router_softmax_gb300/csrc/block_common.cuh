@@ -478,15 +478,20 @@ __device__ __forceinline__ void red_release_gpu_add(unsigned *p, unsigned v) {
 // the last arrival came in meanwhile, the CTA goes on as if it had seen it.
 // The success path costs nothing extra: the check reads the value the poll
 // already loaded. The counter must be zero before the launch.
-__device__ bool grid_barrier(unsigned *arrivals, unsigned expected, unsigned max_polls = kBarrierSpinLimit) {
-    __shared__ int s_ok;
+//
+// grid_arrive and grid_wait are its two halves, for a CTA with work of its own
+// (touching nothing the other CTAs wait for) between its arrival and its wait.
+__device__ __forceinline__ void grid_arrive(unsigned *arrivals) {
     __syncthreads();
+    // The CTA barrier above orders every thread's writes before this release
+    // add (release is cumulative); the acquire loads in grid_wait and its CTA
+    // barrier order every thread's later reads after the wait. No separate
+    // fence is needed on either side.
+    if (threadIdx.x == 0) red_release_gpu_add(arrivals, 1u);
+}
+__device__ __forceinline__ bool grid_wait(unsigned *arrivals, unsigned expected, unsigned max_polls = kBarrierSpinLimit) {
+    __shared__ int s_ok;
     if (threadIdx.x == 0) {
-        // The CTA barrier above orders every thread's writes before this
-        // release add (release is cumulative); the acquire loads and the CTA
-        // barrier below order every thread's later reads after the wait. No
-        // separate fence is needed on either side.
-        red_release_gpu_add(arrivals, 1u);
         unsigned spins = 0, v;
         while ((v = ld_acquire_gpu(arrivals)) < expected) {
             if (++spins > max_polls) {
@@ -510,6 +515,10 @@ __device__ bool grid_barrier(unsigned *arrivals, unsigned expected, unsigned max
     }
     __syncthreads();
     return s_ok != 0;
+}
+__device__ bool grid_barrier(unsigned *arrivals, unsigned expected, unsigned max_polls = kBarrierSpinLimit) {
+    grid_arrive(arrivals);
+    return grid_wait(arrivals, expected, max_polls);
 }
 
 // ---------------------------------------------------------------------------

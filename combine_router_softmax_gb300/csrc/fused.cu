@@ -179,7 +179,11 @@ __global__ void __launch_bounds__(256) fused_zero_kernel(unsigned *p, int n) {
     for (int i = threadIdx.x; i < n; i += blockDim.x) p[i] = 0u;
 }
 
-template <int VPL, bool kSplit>
+// kSolo: the split form with a single tile CTA (up to 8 tokens), compiled
+// without the grid barriers and the multi-CTA count steps it never runs (at
+// these sizes the kernel's time follows its code size: it is fetched from HBM
+// after the cache flush).
+template <int VPL, bool kSplit, bool kSolo>
 __global__ void __launch_bounds__(kFusedThreads, 2) dispatch_fused_kernel(FusedArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int s_warp32[32];
@@ -207,8 +211,9 @@ __global__ void __launch_bounds__(kFusedThreads, 2) dispatch_fused_kernel(FusedA
     // The schedule CTA (index nb, when present) holds no tile: it only joins the
     // two grid barriers, then builds the chunk schedule while the tile CTAs
     // write their slots and rows.
-    const bool sched_only = a.sched_cta && b == a.nb;
-    const unsigned arrivals = (unsigned)(a.nb + a.sched_cta);
+    const bool sched_only = !kSolo && a.sched_cta && b == a.nb;
+    const unsigned arrivals = kSolo ? 1u : (unsigned)(a.nb + a.sched_cta);
+    const bool hist = !kSolo && a.hist;
     // tile b = tokens [floor(b T / nb), floor((b + 1) T / nb)): every CTA within one token of the others
     const int64_t t0 = sched_only ? a.T : (int64_t)b * a.T / a.nb;
     const int ntok = sched_only ? 0 : (int)((int64_t)(b + 1) * a.T / a.nb - t0);  // may be 0 when T < nb
@@ -266,7 +271,7 @@ __global__ void __launch_bounds__(kFusedThreads, 2) dispatch_fused_kernel(FusedA
         }
     }
 
-    if (a.hist)
+    if (hist)
         for (int e = threadIdx.x; e < E; e += blockDim.x) {
             s_tot[e] = 0;
             s_base[e] = 0;
@@ -288,20 +293,28 @@ __global__ void __launch_bounds__(kFusedThreads, 2) dispatch_fused_kernel(FusedA
     __syncthreads();
 
     // B. rank the tile's pairs; publish the tile's counts
-    const int ppw = np > 0 ? (np + kFusedWarps - 1) / kFusedWarps : 1;
-    // (a single CTA keeps its counts in shared memory: they are the totals)
-    if (!sched_only)
-        cta_rank_pairs(tile_e, np, ppw, E, cnt, tile_r,
-                       arrivals == 1 ? s_tot : (a.hist ? s_col : a.counts + (int64_t)b * E), 1);
-
     // C. (a single CTA needs no grid barrier: after a CTA barrier its own
     // global writes are visible to all its threads). The barrier words and
     // ready flags are zeroed by the grid launched before this one.
-    grid_dependency_wait();
-    bool ok = arrivals > 1 ? grid_barrier(&a.sync[0], arrivals) : (__syncthreads(), true);
+    const int ppw = np > 0 ? (np + kFusedWarps - 1) / kFusedWarps : 1;
+    bool ok;
+    if (hist) {
+        // The others need only this tile's picks (in topk_idx since A): arrive
+        // first, rank while they arrive (the counts stay in shared memory).
+        grid_dependency_wait();
+        grid_arrive(&a.sync[0]);
+        if (!sched_only) cta_rank_pairs(tile_e, np, ppw, E, cnt, tile_r, s_col, 1);
+        ok = grid_wait(&a.sync[0], arrivals);
+    } else {
+        // (a single CTA keeps its counts in shared memory: they are the totals)
+        if (!sched_only)
+            cta_rank_pairs(tile_e, np, ppw, E, cnt, tile_r, arrivals == 1 ? s_tot : a.counts + (int64_t)b * E, 1);
+        grid_dependency_wait();
+        ok = arrivals > 1 ? grid_barrier(&a.sync[0], arrivals) : (__syncthreads(), true);
+    }
     // C'. (hist) every tile's picks are in topk_idx now: the expert totals and
     // this tile's bases counted from them directly, 8 loads in flight a thread.
-    if (ok && a.hist) {
+    if (ok && hist) {
         const int64_t n = (int64_t)a.T * k, before = t0 * k;
         for (int64_t i0 = threadIdx.x; i0 < n; i0 += 8 * (int64_t)blockDim.x) {
             int ev[8];
@@ -327,7 +340,7 @@ __global__ void __launch_bounds__(kFusedThreads, 2) dispatch_fused_kernel(FusedA
     // CTA skips it and the global reads of step F: its counts, kept in shared
     // memory, are the totals and its bases are zero: T = 1 and 8 -1.4 to -2.3
     // us per layer.)
-    if (ok && !sched_only && arrivals > 1 && !a.hist) {
+    if (ok && !sched_only && arrivals > 1 && !hist) {
         const int nb = a.nb;
         const int my_n = b < E ? (E - b + nb - 1) / nb : 0;
         const int nv = my_n * nb;
@@ -367,14 +380,14 @@ __global__ void __launch_bounds__(kFusedThreads, 2) dispatch_fused_kernel(FusedA
         }
     }
     // E.
-    if (ok) ok = arrivals > 1 && !a.hist ? grid_barrier(&a.sync[1], arrivals) : (__syncthreads(), true);
+    if (ok) ok = arrivals > 1 && !hist ? grid_barrier(&a.sync[1], arrivals) : (__syncthreads(), true);
 
     if (ok) {
         // F. expert offsets and this tile's slots
         for (int e = threadIdx.x; e < E; e += blockDim.x) {
             if (arrivals == 1) {
                 s_base[e] = 0;
-            } else if (!a.hist) {
+            } else if (!hist) {
                 s_tot[e] = __ldcg(a.totals + e);
                 if (!sched_only) s_base[e] = __ldcg(a.bases + (int64_t)b * E + e);
             }
@@ -421,7 +434,7 @@ __global__ void __launch_bounds__(kFusedThreads, 2) dispatch_fused_kernel(FusedA
             }
             if (threadIdx.x == 0) a.rank_offset[a.R] = s_eoff[E];
         }
-        if (a.sched_cta ? sched_only : b == a.nb - 1) {
+        if (!kSolo && a.sched_cta ? sched_only : b == a.nb - 1) {
             for (int r = threadIdx.x; r <= a.R; r += blockDim.x) s_roff[r] = s_eoff[r * epr];
             __syncthreads();
             cta_build_schedule(s_roff, a.R, a.W, a.tiers, a.chunks, a.n_chunks, a.worker_begin, s_warp32, s_P,
@@ -502,32 +515,36 @@ __global__ void __launch_bounds__(kFusedThreads, 2) dispatch_fused_kernel(FusedA
 
 using FusedKernel = void (*)(FusedArgs);
 
-template <bool kSplit>
+template <bool kSplit, bool kSolo>
 FusedKernel pick_kernel_t(int32_t E) {
     const int vpl = (E + 31) / 32;
-    if (vpl <= 1) return dispatch_fused_kernel<1, kSplit>;
-    if (vpl <= 2) return dispatch_fused_kernel<2, kSplit>;
-    if (vpl <= 4) return dispatch_fused_kernel<4, kSplit>;
-    if (vpl <= 8) return dispatch_fused_kernel<8, kSplit>;
-    if (vpl <= 16) return dispatch_fused_kernel<16, kSplit>;
-    return dispatch_fused_kernel<32, kSplit>;
+    if (vpl <= 1) return dispatch_fused_kernel<1, kSplit, kSolo>;
+    if (vpl <= 2) return dispatch_fused_kernel<2, kSplit, kSolo>;
+    if (vpl <= 4) return dispatch_fused_kernel<4, kSplit, kSolo>;
+    if (vpl <= 8) return dispatch_fused_kernel<8, kSplit, kSolo>;
+    if (vpl <= 16) return dispatch_fused_kernel<16, kSplit, kSolo>;
+    return dispatch_fused_kernel<32, kSplit, kSolo>;
 }
 
-FusedKernel pick_kernel(int32_t E, bool split) { return split ? pick_kernel_t<true>(E) : pick_kernel_t<false>(E); }
+// form 0: single-role, 1: split, 2: split with a single tile CTA
+FusedKernel pick_kernel(int32_t E, int form) {
+    return form == 2 ? pick_kernel_t<true, true>(E) : form == 1 ? pick_kernel_t<true, false>(E)
+                                                                : pick_kernel_t<false, false>(E);
+}
 
 // Lets a kernel use up to kFusedSmemLimit of dynamic shared memory (once per
 // device and kernel); false if the device refuses.
-bool allow_fused_smem(FusedKernel kern, int dev, int32_t E, bool split) {
-    static std::atomic<bool> attr_set[kMaxDevices_][2][6];  // zero-initialised: false
+bool allow_fused_smem(FusedKernel kern, int dev, int32_t E, int form) {
+    static std::atomic<bool> attr_set[kMaxDevices_][3][6];  // zero-initialised: false
     const int vpl = (E + 31) / 32;
     const int vi = vpl <= 1 ? 0 : vpl <= 2 ? 1 : vpl <= 4 ? 2 : vpl <= 8 ? 3 : vpl <= 16 ? 4 : 5;
-    if (attr_set[dev][split][vi]) return true;
+    if (attr_set[dev][form][vi]) return true;
     if (cudaFuncSetAttribute(reinterpret_cast<const void *>(kern), cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kFusedSmemLimit) != cudaSuccess) {
         cudaGetLastError();
         return false;
     }
-    attr_set[dev][split][vi] = true;
+    attr_set[dev][form][vi] = true;
     return true;
 }
 
@@ -542,9 +559,10 @@ bool plan_split(const ep_config &c, FusedPlan *p) {
     if (row_bytes < 1024 || row_bytes > 48 * 1024) return false;  // rows move as bulk copies
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices_) return false;
-    const FusedKernel kern = pick_kernel(c.E, true);
-    if (!allow_fused_smem(kern, dev, c.E, true)) return false;
     const int nb = (int)((c.T + kFusedWarps - 1) / kFusedWarps);
+    const int form = nb == 1 ? 2 : 1;
+    const FusedKernel kern = pick_kernel(c.E, form);
+    if (!allow_fused_smem(kern, dev, c.E, form)) return false;
     if (nb > kMaxFusedCTAs) return false;
     const int tb = (int)((c.T + nb - 1) / nb);
     const int sched = nb > 1 ? 1 : 0;
@@ -577,8 +595,8 @@ bool plan_fused(const ep_config &c, FusedPlan *p) {
     if (c.T <= 0 || c.T > kFusedMaxT) return false;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices_) return false;
-    const FusedKernel kern = pick_kernel(c.E, false);
-    if (!allow_fused_smem(kern, dev, c.E, false)) return false;
+    const FusedKernel kern = pick_kernel(c.E, 0);
+    if (!allow_fused_smem(kern, dev, c.E, 0)) return false;
     const int32_t row_bytes = c.H * 2;
     const bool bulk = c.k % 4 == 0 && row_bytes >= 1024 && row_bytes <= 48 * 1024;
     const int sms = sm_count(dev);
@@ -764,7 +782,7 @@ cudaError_t launch_dispatch_fused(const ep_config &c, int32_t W, const float *lo
         fused_zero_kernel<<<1, 256, 0, s>>>(a.sync, n_zero);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    const FusedKernel kern = pick_kernel(c.E, split);
+    const FusedKernel kern = pick_kernel(c.E, split ? (p.nb == 1 && p.sched_cta == 0 ? 2 : 1) : 0);
     const dim3 grid((unsigned)(p.nb + p.sched_cta + p.n_data));
     // Set when a device refused the cooperative launch with the dependent-launch
     // attribute; the plain cooperative launch is then used (the same results).
