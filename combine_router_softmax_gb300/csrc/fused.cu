@@ -329,7 +329,7 @@ cudaError_t launch_dispatch_fused(const ep_config &c, int32_t W, const float *lo
     // barrier instead of the column scan and the second barrier (measured per
     // layer: T = 64 -1.6 us, T = 160 -2.1, decode -2.3, T = 512 -2.1, T = 1024
     // -1.6, T = 1760 +-0.3).
-    a.hist = p.nb + p.sched_cta > 1 && (int64_t)c.T * c.k <= kHistMaxPairs ? 1 : 0;
+    a.hist = p.nb + p.sched_cta > 1 && (split || (int64_t)c.T * c.k <= kHistMaxPairs) ? 1 : 0;
     // measured: T = 1..64 (<= 7.3 MB of send rows) gain 1-2 us, T = 256 even, T = 512 (59 MB) loses 1.8 us
     a.early_dependents = (int64_t)c.T * c.k * c.H * 2 <= (int64_t)16 << 20 ? 1 : 0;
     // The barrier words and (split form) the tiles' ready flags are zeroed by a

@@ -152,7 +152,9 @@ __global__ void __launch_bounds__(kFusedThreads, 2) dispatch_fused_kernel(FusedA
     // write their slots and rows.
     const bool sched_only = !kSolo && a.sched_cta && b == a.nb;
     const unsigned arrivals = kSolo ? 1u : (unsigned)(a.nb + a.sched_cta);
-    const bool hist = !kSolo && a.hist;
+    // (the split form moves at most 160 tokens' pairs: always the count of all
+    // picks, and its instances carry no column scan)
+    const bool hist = !kSolo && (kSplit || a.hist);
     // tile b = tokens [floor(b T / nb), floor((b + 1) T / nb)): every CTA within one token of the others
     const int64_t t0 = sched_only ? a.T : (int64_t)b * a.T / a.nb;
     const int ntok = sched_only ? 0 : (int)((int64_t)(b + 1) * a.T / a.nb - t0);  // may be 0 when T < nb
