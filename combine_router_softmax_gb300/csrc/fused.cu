@@ -15,8 +15,11 @@
 //      tiles in one batch and publishes each tile's base inside each of those
 //      experts and their totals;
 //   E. bounded grid barrier;
-//      (up to 16384 pairs, D and E give way to C': every CTA reads all of
-//      topk_idx, written in A, and counts the totals and its bases itself);
+//      Up to 16384 pairs (every split-form launch, and the single-role form
+//      at small k) D and E give way to C': the CTAs arrive at barrier C as
+//      soon as A has stored their picks in topk_idx, rank while the others
+//      arrive, and then every CTA reads all of topk_idx and counts the totals
+//      and its bases itself, in shared memory;
 //   F. each CTA reads its tile's bases and the totals, scans the totals into
 //      expert offsets and writes its slots; CTA 0 writes counts and offsets.
 //      The chunk schedule is built by one extra CTA that holds no tile (it
@@ -35,7 +38,8 @@
 // the GPU, one per send row when there are enough, else one per token --
 // fetch their x row at once, acquire-poll the owning tile's flag (bounded)
 // and bulk-store the rows. Up to 8 tokens the metadata is then one CTA with no
-// grid barrier, and the rows leave from many SMs instead of one (measured per
+// grid barrier (its own kernel instance, in fused_solo.cu; its counts stay in
+// shared memory), and the rows leave from many SMs instead of one (measured per
 // layer: T = 8 21.6 -> 19.5 us, T = 16 22.7 -> 21.0, T = 96 25.1 -> 23.0, T = 160
 // 28.6 -> 27.3, T = 1 -0.5, T = 64 -0.3; at T = 192 and 256 within +-0.2 us, at
 // T = 512 +4 us, so the split form stops at T = 160).
