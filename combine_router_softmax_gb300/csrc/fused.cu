@@ -166,6 +166,11 @@ bool plan_fused(const ep_config &c, FusedPlan *p) {
     for (int per_sm = 2; per_sm >= 1; --per_sm) {
         int nb = sms * per_sm - 1;  // one resident slot kept for the schedule CTA
         if (nb > kMaxFusedCTAs) nb = kMaxFusedCTAs;
+        // Up to 1024 tokens, at most 128 tiles (two to eight tokens each in
+        // place of one or two: decode -0.8 us per layer, T = 192 -0.5, T = 512
+        // -0.9, T = 1024 -1.9; above 1024 the 8-token tiles that the same count
+        // would need measured 5-9 us slower than the smaller ones).
+        if (c.T <= 1024 && nb > kFusedTileCap) nb = kFusedTileCap;
         if (nb > c.T) nb = c.T;
         if (nb < 1) nb = 1;
         const int tb = (int)((c.T + nb - 1) / nb);  // largest tile

@@ -24,6 +24,7 @@ constexpr int kSplitMaxT = 160;  // split form up to this many tokens
 // cross near 1760).
 constexpr int kFusedMaxT = 1760;
 constexpr int64_t kHistMaxPairs = 16384;
+constexpr int kFusedTileCap = 128;  // single-role form up to 1024 tokens: at most this many tiles
 
 size_t align128(size_t b) { return (b + 127) & ~(size_t)127; }
 
