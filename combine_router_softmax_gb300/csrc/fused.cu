@@ -32,12 +32,12 @@
 //      (<= 16 MB) every CTA signals programmatic dependents here, so that a
 //      combine launched after it can start its prologue early.
 // Up to 160 tokens the split form of the same kernel is used instead (the
-// article's metadata/data decomposition): the tile CTAs (up to 8 tokens each,
-// one per routing warp) stop after F, releasing a per-tile ready flag once
-// their slots are written, and separate data CTAs -- as many as still fit on
-// the GPU, one per send row when there are enough, else one per token --
-// fetch their x row at once, acquire-poll the owning tile's flag (bounded)
-// and bulk-store the rows. Up to 8 tokens the metadata is then one CTA with no
+// article's metadata/data decomposition): the tile CTAs (up to 4 tokens each
+// up to T = 64, else up to 8, one per routing warp) stop after F, releasing
+// a per-tile ready flag once their slots are written, and separate data CTAs
+// -- as many as still fit on the GPU, one per send row when there are enough,
+// else one per token -- fetch their x row at once, acquire-poll the owning
+// tile's flag (bounded) and bulk-store the rows. Up to 4 tokens the metadata is then one CTA with no
 // grid barrier (its own kernel instance, in fused_solo.cu; its counts stay in
 // shared memory), and the rows leave from many SMs instead of one (measured per
 // layer: T = 8 21.6 -> 19.5 us, T = 16 22.7 -> 21.0, T = 96 25.1 -> 23.0, T = 160
@@ -111,7 +111,7 @@ bool allow_fused_smem(FusedKernel kern, int dev, int32_t E, int form) {
 }
 
 // The split form (kernel decomposition with separate data CTAs): tiles of up
-// to 8 tokens (one per routing warp), the schedule CTA when there are several
+// to 4 or 8 tokens, the schedule CTA when there are several
 // tiles, and as many data CTAs as still fit on the GPU, each moving units of
 // one row (when every row can have its own CTA) or of a whole token. false if
 // the shape does not suit it (then the caller uses the other forms).
@@ -121,7 +121,12 @@ bool plan_split(const ep_config &c, FusedPlan *p) {
     if (row_bytes < 1024 || row_bytes > 48 * 1024) return false;  // rows move as bulk copies
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices_) return false;
-    const int nb = (int)((c.T + kFusedWarps - 1) / kFusedWarps);
+    // Tiles of 4 tokens up to T = 64, else 8 (one per routing warp). Measured
+    // per layer against 8 everywhere, on two boxes: T = 8 (two tiles instead
+    // of one CTA with no barrier) -0.5 and -1.5 us, T = 64 -1.5 and +-0.1,
+    // T = 16 +-0.1; at T = 96 and 160 tiles of 4 were even or +0.3.
+    const int tile = c.T <= 64 ? 4 : kFusedWarps;
+    const int nb = (int)((c.T + tile - 1) / tile);
     const int form = nb == 1 ? 2 : 1;
     const FusedKernel kern = pick_kernel(c.E, form);
     if (!allow_fused_smem(kern, dev, c.E, form)) return false;

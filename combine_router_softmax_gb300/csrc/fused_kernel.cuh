@@ -119,7 +119,7 @@ __device__ __forceinline__ bool split_data_unit(const FusedArgs &a, int64_t t, i
     return true;
 }
 
-// kSolo: the split form with a single tile CTA (up to 8 tokens), compiled
+// kSolo: the split form with a single tile CTA (up to 4 tokens), compiled
 // without the grid barriers and the multi-CTA count steps it never runs (at
 // these sizes the kernel's time follows its code size: it is fetched from HBM
 // after the cache flush).

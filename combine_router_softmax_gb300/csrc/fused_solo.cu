@@ -1,5 +1,5 @@
 // fused_solo.cu -- the split form of the small-batch dispatch kernel with a
-// single tile (metadata) CTA, up to 8 tokens (fused_kernel.cuh), compiled in a
+// single tile (metadata) CTA, up to 4 tokens (fused_kernel.cuh), compiled in a
 // module of its own: beside the other instances it slowed those down.
 #include "fused_kernel.cuh"
 
