@@ -437,6 +437,10 @@ FUSED = [
     ep_synth.Workload("split-k12-groups", T=57, H=2048, E=96, R=6, k=12, n_groups=6, topk_groups=2,
                       ranks_per_node=2, self_rank=5, num_workers=33),
     ep_synth.CONFIGS["prefill"].with_(name="split-T63-plain", T=63, renormalize=0),
+    # tiles of 4 tokens up to T = 64, else 8: a single tile CTA of 3 tokens, tiles of 3 and 2, then 9 tiles of 8/7
+    ep_synth.CONFIGS["decode"].with_(name="split-T3", T=3),
+    ep_synth.CONFIGS["decode"].with_(name="split-T5", T=5),
+    ep_synth.CONFIGS["decode"].with_(name="split-T65", T=65),
     ep_synth.CONFIGS["decode"].with_(name="split-T160", T=160),
     ep_synth.CONFIGS["decode"].with_(name="fused-T161", T=161),
     # either side of the small-batch kernel's upper bound (1760 tokens)
