@@ -60,8 +60,8 @@ KERNEL_SOURCES = {
     "layout": ["layout.cu", "block_common.cuh"],
     "dispatch": ["dispatch.cu"],
     # the call runs the fused kernel at small T, else route + layout + dispatch kernels
-    "dispatch_fused": ["fused.cu", "fused_kernel.cuh", "fused_solo.cu", "block_common.cuh", "route_token.cuh", "route.cu",
-                       "layout.cu", "dispatch.cu"],
+    "dispatch_fused": ["fused.cu", "fused_kernel.cuh", "block_common.cuh", "route_token.cuh", "route.cu", "layout.cu",
+                       "dispatch.cu"],
     "combine": ["combine.cu"],
 }
 

@@ -37,12 +37,12 @@
 // a per-tile ready flag once their slots are written, and separate data CTAs
 // -- as many as still fit on the GPU, one per send row when there are enough,
 // else one per token -- fetch their x row at once, acquire-poll the owning
-// tile's flag (bounded) and bulk-store the rows. Up to 4 tokens the metadata is then one CTA with no
-// grid barrier (its own kernel instance, in fused_solo.cu; its counts stay in
-// shared memory), and the rows leave from many SMs instead of one (measured per
-// layer: T = 8 21.6 -> 19.5 us, T = 16 22.7 -> 21.0, T = 96 25.1 -> 23.0, T = 160
-// 28.6 -> 27.3, T = 1 -0.5, T = 64 -0.3; at T = 192 and 256 within +-0.2 us, at
-// T = 512 +4 us, so the split form stops at T = 160).
+// tile's flag (bounded) and bulk-store the rows; the schedule CTA is there
+// even for a single tile. The rows leave from many SMs instead of a few
+// (measured per layer against the single-role form: T = 8 21.6 -> 19.5 us,
+// T = 16 22.7 -> 21.0, T = 96 25.1 -> 23.0, T = 160 28.6 -> 27.3, T = 1 -0.5,
+// T = 64 -0.3; at T = 192 and 256 within +-0.2 us, at T = 512 +4 us, so the
+// split form stops at T = 160).
 // The barrier words and ready flags are zeroed by a one-CTA kernel launched
 // just before, of which the fused kernel is a programmatic dependent.
 // Every result equals what ep_route, ep_layout and ep_dispatch write.
@@ -75,29 +75,26 @@ __global__ void __launch_bounds__(256) fused_zero_kernel(unsigned *p, int n) {
 
 using FusedKernel = void (*)(FusedArgs);
 
-template <bool kSplit, bool kSolo>
+template <bool kSplit>
 FusedKernel pick_kernel_t(int32_t E) {
     const int vpl = (E + 31) / 32;
-    if (vpl <= 1) return dispatch_fused_kernel<1, kSplit, kSolo>;
-    if (vpl <= 2) return dispatch_fused_kernel<2, kSplit, kSolo>;
-    if (vpl <= 4) return dispatch_fused_kernel<4, kSplit, kSolo>;
-    if (vpl <= 8) return dispatch_fused_kernel<8, kSplit, kSolo>;
-    if (vpl <= 16) return dispatch_fused_kernel<16, kSplit, kSolo>;
-    return dispatch_fused_kernel<32, kSplit, kSolo>;
+    if (vpl <= 1) return dispatch_fused_kernel<1, kSplit>;
+    if (vpl <= 2) return dispatch_fused_kernel<2, kSplit>;
+    if (vpl <= 4) return dispatch_fused_kernel<4, kSplit>;
+    if (vpl <= 8) return dispatch_fused_kernel<8, kSplit>;
+    if (vpl <= 16) return dispatch_fused_kernel<16, kSplit>;
+    return dispatch_fused_kernel<32, kSplit>;
 }
 
-// form 0: single-role, 1: split, 2: split with a single tile CTA
+// form 0: single-role, 1: split
 FusedKernel pick_kernel(int32_t E, int form) {
-    // (the instance with a single tile CTA lives in its own module, fused_solo.cu:
-    // built beside the others it slowed them down at T = 64..512 by 1-2 us)
-    return form == 2 ? reinterpret_cast<FusedKernel>(const_cast<void *>(fused_solo_kernel(E)))
-                     : form == 1 ? pick_kernel_t<true, false>(E) : pick_kernel_t<false, false>(E);
+    return form == 1 ? pick_kernel_t<true>(E) : pick_kernel_t<false>(E);
 }
 
 // Lets a kernel use up to kFusedSmemLimit of dynamic shared memory (once per
 // device and kernel); false if the device refuses.
 bool allow_fused_smem(FusedKernel kern, int dev, int32_t E, int form) {
-    static std::atomic<bool> attr_set[kMaxDevices_][3][6];  // zero-initialised: false
+    static std::atomic<bool> attr_set[kMaxDevices_][2][6];  // zero-initialised: false
     const int vpl = (E + 31) / 32;
     const int vi = vpl <= 1 ? 0 : vpl <= 2 ? 1 : vpl <= 4 ? 2 : vpl <= 8 ? 3 : vpl <= 16 ? 4 : 5;
     if (attr_set[dev][form][vi]) return true;
@@ -122,17 +119,21 @@ bool plan_split(const ep_config &c, FusedPlan *p) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices_) return false;
     // Tiles of 4 tokens up to T = 64, else 8 (one per routing warp). Measured
-    // per layer against 8 everywhere, on two boxes: T = 8 (two tiles instead
-    // of one CTA with no barrier) -0.5 and -1.5 us, T = 64 -1.5 and +-0.1,
-    // T = 16 +-0.1; at T = 96 and 160 tiles of 4 were even or +0.3.
+    // per layer against 8 everywhere, on two boxes: T = 8 (two tiles and the
+    // schedule CTA instead of one tile CTA that also built the schedule) -0.5
+    // and -1.5 us, T = 64 -1.5 and +-0.1, T = 16 +-0.1; at T = 96 and 160
+    // tiles of 4 were even or +0.3.
     const int tile = c.T <= 64 ? 4 : kFusedWarps;
     const int nb = (int)((c.T + tile - 1) / tile);
-    const int form = nb == 1 ? 2 : 1;
-    const FusedKernel kern = pick_kernel(c.E, form);
-    if (!allow_fused_smem(kern, dev, c.E, form)) return false;
+    const FusedKernel kern = pick_kernel(c.E, 1);
+    if (!allow_fused_smem(kern, dev, c.E, 1)) return false;
     if (nb > kMaxFusedCTAs) return false;
     const int tb = (int)((c.T + nb - 1) / nb);
-    const int sched = nb > 1 ? 1 : 0;
+    // The schedule CTA even for a single tile: it builds the chunk schedule
+    // while the tile CTA writes its slots, at the price of a grid barrier
+    // (measured against one tile CTA doing both, compiled as an instance of its
+    // own without the barrier: T = 1 +-0.05 and -0.25 us, T = 2 -0.1, T = 4 -0.8).
+    const int sched = 1;
     const int row_pad = (int)align128((size_t)row_bytes);
     const SmemLayout L = smem_layout(1, row_pad, tb, c.k, c.E, c.R, c.n_groups > 1);
     if (L.bytes > kFusedSmemLimit) return false;
@@ -354,7 +355,7 @@ cudaError_t launch_dispatch_fused(const ep_config &c, int32_t W, const float *lo
         fused_zero_kernel<<<1, 256, 0, s>>>(a.sync, n_zero);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    const FusedKernel kern = pick_kernel(c.E, split ? (p.nb == 1 && p.sched_cta == 0 ? 2 : 1) : 0);
+    const FusedKernel kern = pick_kernel(c.E, split ? 1 : 0);
     const dim3 grid((unsigned)(p.nb + p.sched_cta + p.n_data));
     // Set when a device refused the cooperative launch with the dependent-launch
     // attribute; the plain cooperative launch is then used (the same results).

@@ -1,6 +1,5 @@
 // fused_kernel.cuh -- the small-batch dispatch kernel of ep_dispatch_fused
-// (fused.cu has its description and the host code; fused_solo.cu compiles
-// its single-metadata-CTA instances, in a module of their own).
+// (fused.cu has its description and the host code).
 #pragma once
 
 #include "block_common.cuh"
@@ -119,11 +118,8 @@ __device__ __forceinline__ bool split_data_unit(const FusedArgs &a, int64_t t, i
     return true;
 }
 
-// kSolo: the split form with a single tile CTA (up to 4 tokens), compiled
-// without the grid barriers and the multi-CTA count steps it never runs (at
-// these sizes the kernel's time follows its code size: it is fetched from HBM
-// after the cache flush).
-template <int VPL, bool kSplit, bool kSolo>
+// kSplit: the split form (tile CTAs, the schedule CTA, data CTAs).
+template <int VPL, bool kSplit>
 __global__ void __launch_bounds__(kFusedThreads, 2) dispatch_fused_kernel(FusedArgs a) {
     extern __shared__ __align__(128) unsigned char smem[];
     __shared__ int s_warp32[32];
@@ -151,11 +147,11 @@ __global__ void __launch_bounds__(kFusedThreads, 2) dispatch_fused_kernel(FusedA
     // The schedule CTA (index nb, when present) holds no tile: it only joins the
     // two grid barriers, then builds the chunk schedule while the tile CTAs
     // write their slots and rows.
-    const bool sched_only = !kSolo && a.sched_cta && b == a.nb;
-    const unsigned arrivals = kSolo ? 1u : (unsigned)(a.nb + a.sched_cta);
+    const bool sched_only = a.sched_cta && b == a.nb;
+    const unsigned arrivals = (unsigned)(a.nb + a.sched_cta);
     // (the split form moves at most 160 tokens' pairs: always the count of all
     // picks, and its instances carry no column scan)
-    const bool hist = !kSolo && (kSplit || a.hist);
+    const bool hist = kSplit || a.hist;
     // tile b = tokens [floor(b T / nb), floor((b + 1) T / nb)): every CTA within one token of the others
     const int64_t t0 = sched_only ? a.T : (int64_t)b * a.T / a.nb;
     const int ntok = sched_only ? 0 : (int)((int64_t)(b + 1) * a.T / a.nb - t0);  // may be 0 when T < nb
@@ -377,7 +373,7 @@ __global__ void __launch_bounds__(kFusedThreads, 2) dispatch_fused_kernel(FusedA
             }
             if (threadIdx.x == 0) a.rank_offset[a.R] = s_eoff[E];
         }
-        if (!kSolo && a.sched_cta ? sched_only : b == a.nb - 1) {
+        if (a.sched_cta ? sched_only : b == a.nb - 1) {
             for (int r = threadIdx.x; r <= a.R; r += blockDim.x) s_roff[r] = s_eoff[r * epr];
             __syncthreads();
             cta_build_schedule(s_roff, a.R, a.W, a.tiers, a.chunks, a.n_chunks, a.worker_begin, s_warp32, s_P,
@@ -457,8 +453,5 @@ __global__ void __launch_bounds__(kFusedThreads, 2) dispatch_fused_kernel(FusedA
 }
 
 }  // namespace
-
-// The single-metadata-CTA split-form instance for E experts (fused_solo.cu).
-const void *fused_solo_kernel(int32_t E);
 
 }  // namespace ep
