@@ -36,7 +36,7 @@
 // up to T = 64, else up to 8, one per routing warp) stop after F, releasing
 // a per-tile ready flag once their slots are written, and separate data CTAs
 // -- as many as still fit on the GPU, one per send row when there are enough,
-// else one per token -- fetch their x row at once, acquire-poll the owning
+// else one per 2, 4, ... rows of a token -- fetch their x row at once, acquire-poll the owning
 // tile's flag (bounded) and bulk-store the rows; the schedule CTA is there
 // even for a single tile. The rows leave from many SMs instead of a few
 // (measured per layer against the single-role form: T = 8 21.6 -> 19.5 us,
@@ -56,7 +56,7 @@ static __device__ int32_t g_fused_error;
 struct FusedPlan {
     int nb = 0;       // CTAs (tiles)
     int n_data = 0;   // split form: data CTAs (0: the tile CTAs move their own rows)
-    int unit_rows = 0;  // split form: rows per data unit (1 or k)
+    int unit_rows = 0;  // split form: rows per data unit (1, 2, 4, ... or k)
     int tb = 0;       // tokens in the largest tile
     int ns = 0;       // x-row stages per CTA (bulk path), 0 = vector copy
     int row_pad = 0;  // bytes per stage
@@ -108,10 +108,9 @@ bool allow_fused_smem(FusedKernel kern, int dev, int32_t E, int form) {
 }
 
 // The split form (kernel decomposition with separate data CTAs): tiles of up
-// to 4 or 8 tokens, the schedule CTA when there are several
-// tiles, and as many data CTAs as still fit on the GPU, each moving units of
-// one row (when every row can have its own CTA) or of a whole token. false if
-// the shape does not suit it (then the caller uses the other forms).
+// to 4 or 8 tokens, the schedule CTA, and as many data CTAs as still fit on
+// the GPU, each moving units of a few of a token's rows. false if the shape
+// does not suit it (then the caller uses the other forms).
 bool plan_split(const ep_config &c, FusedPlan *p) {
     if (c.T <= 0 || c.T > kSplitMaxT) return false;
     const int32_t row_bytes = c.H * 2;
@@ -141,9 +140,14 @@ bool plan_split(const ep_config &c, FusedPlan *p) {
                                                                      kFusedThreads, L.bytes);
     const int64_t room = cap - nb - sched;
     if (room < 1) return false;
-    const int64_t pairs = (int64_t)c.T * c.k;
-    const int unit_rows = pairs <= room ? 1 : c.k;
-    const int64_t n_units = unit_rows == 1 ? pairs : c.T;
+    // A data CTA per unit of unit_rows of a token's k send rows: the fewest
+    // rows (1, 2, 4, ... or all k) that give every unit a CTA of its own
+    // (measured against whole tokens once rows outnumber the CTAs: T = 40 -0.9
+    // and -1.4 us per layer, T = 64, 96 and 128 within +-0.1).
+    int unit_rows = 1;
+    while (unit_rows < c.k && (int64_t)c.T * ((c.k + unit_rows - 1) / unit_rows) > room) unit_rows *= 2;
+    if (unit_rows > c.k) unit_rows = c.k;
+    const int64_t n_units = (int64_t)c.T * ((c.k + unit_rows - 1) / unit_rows);
     p->nb = nb;
     p->sched_cta = sched;
     p->tb = tb;

@@ -84,8 +84,9 @@ struct FusedArgs {
     int32_t early_dependents;  // signal dependents at the dispatch phase (small sends only)
     int32_t sched_cta;         // 1: CTA nb holds no tile and builds the chunk schedule
     // Split form only: n_data data CTAs after the tile (and schedule) CTAs move
-    // the rows in units of unit_rows rows of one token (1, or k = the whole
-    // token); ready[q] is set (release) once tile q's slots are written.
+    // the rows in units of unit_rows rows of one token (1, 2, 4, ... or k = the
+    // whole token; the last unit of a token may hold fewer); ready[q] is set
+    // (release) once tile q's slots are written.
     int32_t n_data, unit_rows;
     unsigned *ready;
     // 1: after barrier C every CTA reads all of topk_idx and counts, in shared
@@ -94,7 +95,7 @@ struct FusedArgs {
     int32_t hist;
 };
 
-// The rows of one token (unit_rows of them from top-k position jj0), moved by
+// The rows of one token (up to unit_rows of them from top-k position jj0), moved by
 // a data CTA of the split form: wait until the tile that owns the token has
 // published its slots, then bulk-store the staged x row to each slot.
 __device__ __forceinline__ bool split_data_unit(const FusedArgs &a, int64_t t, int jj0, unsigned char *stage,
@@ -108,7 +109,7 @@ __device__ __forceinline__ bool split_data_unit(const FusedArgs &a, int64_t t, i
     if (a.early_dependents) grid_launch_dependents();
     if (lane < a.unit_rows) {
         const int j = jj0 + lane;
-        const int sv = a.slot[t * a.k + j];
+        const int sv = j < a.k ? a.slot[t * a.k + j] : -1;
         if (sv >= 0 && (int64_t)sv < rows) {
             bulk_s2g(a.send + (int64_t)sv * row_bytes, stage, (uint32_t)row_bytes);
             a.meta[sv] = (int32_t)(t * a.k + j);
@@ -163,7 +164,8 @@ __global__ void __launch_bounds__(kFusedThreads, 2) dispatch_fused_kernel(FusedA
         // the tile CTAs compute the metadata; then, unit by unit, it waits for
         // the owning tile's flag and stores the rows. Warp 0 does it all.
         if (warp != 0) return;
-        const int64_t n_units = a.unit_rows == k ? (int64_t)a.T : (int64_t)a.T * k;
+        const int upt = (k + a.unit_rows - 1) / a.unit_rows;  // units per token
+        const int64_t n_units = (int64_t)a.T * upt;
         const int64_t j = b - a.nb - a.sched_cta;
         if (lane == 0) {
             mbar_init(&bar[0], 1);
@@ -174,8 +176,8 @@ __global__ void __launch_bounds__(kFusedThreads, 2) dispatch_fused_kernel(FusedA
         uint32_t loads = 0;
         bool good = true;
         for (int64_t u = j; good && u < n_units; u += a.n_data) {
-            const int64_t t = a.unit_rows == k ? u : u / k;
-            const int jj0 = a.unit_rows == k ? 0 : (int)(u % k);
+            const int64_t t = upt == 1 ? u : u / upt;
+            const int jj0 = upt == 1 ? 0 : (int)(u - t * upt) * a.unit_rows;
             if (t != cur) {
                 if (cur >= 0) {
                     if (lane < a.unit_rows) bulk_wait_read<0>();  // the stage's previous row is read out
