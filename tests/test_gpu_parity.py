@@ -525,8 +525,10 @@ def test_layout_tiling_boundaries(ep, orc, T):
     assert_layout(g, r)
 
 
-@pytest.mark.parametrize("T", [2423, 2424, 2425, 2431, 2432, 2433])
-def test_dispatch_fused_range_end(ep, T):
+# either side of the small-batch kernel's upper bound (1760 tokens; above it the call runs the route, layout
+# and dispatch kernels), and 16 tokens per CTA on 152 SMs and one more
+@pytest.mark.parametrize("T", [1759, 1760, 1761, 1762, 2432, 2433])
+def test_dispatch_fused_form_boundary(ep, T):
     w = ep_synth.CONFIGS["prefill"].with_(name=f"prefill-T{T}", T=T)
     logits = torch.from_numpy(ep_synth.gate_logits(w.seed, w.T, w.E, w.zipf_s)).cuda()
     x = bf16_to_dev(ep_synth.hidden_bf16_bits(w.seed, w.T, w.H))
